@@ -1,0 +1,190 @@
+"""Oracle for one windowed-KV-cache GroupQueryAttention step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library never
+imports, links or calls it, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``gqaw_oracle.c`` (plain C, fp64 accumulation).  This module
+compiles it with gcc and marshals numpy arrays into it; it does no arithmetic of
+the method itself except resolving the default scale ``1/sqrt(head_size)``
+(mobius issue #111 "GQA In-Place KV Cache: Investigation Report", Part 1.3, the
+``scale`` attribute).
+
+Every function here cites the passage it follows inside ``gqaw_oracle.c``.
+Functions without an independent pin: none (see ``tests/test_oracle_pins.py``),
+except that the order "softcap first, bias after" is a reading of the pages and is
+parity unpinned beyond that reading.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqaw_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_gqaw.so")
+
+F32 = 0
+BF16 = 1
+
+_ERRORS = {
+    1: "malformed sizes",
+    2: "seqlens_k[b] + 1 - S < 0 for some item",
+    3: "T_b > total_sequence_length for some item",
+    4: "out of memory",
+}
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [
+        ("batch_size", ctypes.c_int64),
+        ("sequence_length", ctypes.c_int64),
+        ("num_heads", ctypes.c_int64),
+        ("kv_num_heads", ctypes.c_int64),
+        ("head_size", ctypes.c_int64),
+        ("capacity", ctypes.c_int64),
+        ("local_window_size", ctypes.c_int64),
+        ("scale", ctypes.c_double),
+        ("softcap", ctypes.c_double),
+        ("dtype", ctypes.c_int64),
+        ("query", ctypes.c_void_p),
+        ("key", ctypes.c_void_p),
+        ("value", ctypes.c_void_p),
+        ("past_key", ctypes.c_void_p),
+        ("past_value", ctypes.c_void_p),
+        ("present_key", ctypes.c_void_p),
+        ("present_value", ctypes.c_void_p),
+        ("seqlens_k", ctypes.c_void_p),
+        ("total_sequence_length", ctypes.c_int64),
+        ("attention_bias", ctypes.c_void_p),
+        ("bias_stride_b", ctypes.c_int64),
+        ("bias_stride_h", ctypes.c_int64),
+        ("bias_stride_s", ctypes.c_int64),
+        ("output", ctypes.c_void_p),
+        ("output_f64", ctypes.c_void_p),
+        ("resident_len", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``liboracle_gqaw.so`` next to its source."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        # -ffp-contract=off: no fused multiply-add, so results do not depend on the host ISA.
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        lib.oracle_resident_len.restype = ctypes.c_int64
+        lib.oracle_resident_len.argtypes = [ctypes.c_int64] * 3
+        lib.oracle_round_bf16.restype = ctypes.c_uint16
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_step.restype = ctypes.c_int
+        lib.oracle_step.argtypes = [ctypes.POINTER(_Args)]
+        _lib = lib
+    return _lib
+
+
+def resident_len(T: int, C: int, W: int) -> int:
+    """L(T) of PR #32419 "Specify GroupQueryAttention windowed KV cache layout contract",
+    Description (the resident-count formula)."""
+    return int(_load().oracle_resident_len(int(T), int(C), int(W)))
+
+
+def round_bf16(x: float) -> int:
+    """bfloat16 bits nearest to ``x`` (ties to even), from fp64 in one rounding."""
+    return int(_load().oracle_round_bf16(float(x)))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _elem_dtype(dtype: int):
+    return np.float32 if dtype == F32 else np.uint16
+
+
+def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_length,
+         num_heads, kv_num_heads, local_window_size, scale=0.0, softcap=0.0,
+         attention_bias=None, bias_strides=None, dtype=F32):
+    """One windowed GQA step on host arrays.
+
+    Arrays are numpy: float32 for ``dtype=F32``; uint16 bfloat16 bit patterns for
+    ``dtype=BF16``.  Shapes: query (B,S,Nq*D); key/value (B,S,Nkv*D);
+    past_key/past_value (B,Nkv,C,D); seqlens_k int32 (B,).  ``attention_bias`` is a
+    float32 array indexed ``[b*sb + h*sh + s*ss + j]`` with ``bias_strides=(sb,sh,ss)``
+    in elements (0 broadcasts); if ``bias_strides`` is None the bias must be a
+    contiguous (B|1, Nq|1, S, total) array and its broadcast strides are derived.
+
+    Returns dict(output, output_f64, present_key, present_value, resident_len).
+    The present arrays start as copies of the past arrays; rows [0, L) are written.
+    ``scale == 0`` selects 1/sqrt(head_size).
+    """
+    lib = _load()
+    et = _elem_dtype(dtype)
+    query = np.ascontiguousarray(query, dtype=et)
+    key = np.ascontiguousarray(key, dtype=et)
+    value = np.ascontiguousarray(value, dtype=et)
+    past_key = np.ascontiguousarray(past_key, dtype=et)
+    past_value = np.ascontiguousarray(past_value, dtype=et)
+    seqlens_k = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    B, Nkv, C, D = past_key.shape
+    S = query.shape[1]
+    if query.shape != (B, S, num_heads * D) or key.shape != (B, S, kv_num_heads * D):
+        raise ValueError("oracle.step: shape mismatch")
+    if Nkv != kv_num_heads or value.shape != key.shape or past_value.shape != past_key.shape:
+        raise ValueError("oracle.step: shape mismatch")
+    present_key = past_key.copy()
+    present_value = past_value.copy()
+    output = np.zeros((B, S, num_heads * D), dtype=et)
+    output_f64 = np.zeros((B, S, num_heads * D), dtype=np.float64)
+    resident = np.zeros((B,), dtype=np.int32)
+    sb = sh = ss = 0
+    if attention_bias is not None:
+        attention_bias = np.ascontiguousarray(attention_bias, dtype=np.float32)
+        if bias_strides is None:
+            bb, bh, bs, bt = attention_bias.shape
+            if bt != total_sequence_length or bs != S:
+                raise ValueError("oracle.step: bias must be (B|1, Nq|1, S, total_sequence_length)")
+            ss = bt
+            sh = 0 if bh == 1 else bs * bt
+            sb = 0 if bb == 1 else bh * bs * bt
+        else:
+            sb, sh, ss = (int(v) for v in bias_strides)
+    a = _Args(
+        batch_size=B, sequence_length=S, num_heads=num_heads, kv_num_heads=kv_num_heads,
+        head_size=D, capacity=C, local_window_size=local_window_size,
+        scale=float(scale) if scale else 1.0 / math.sqrt(D), softcap=float(softcap),
+        dtype=dtype, query=_ptr(query), key=_ptr(key), value=_ptr(value),
+        past_key=_ptr(past_key), past_value=_ptr(past_value),
+        present_key=_ptr(present_key), present_value=_ptr(present_value),
+        seqlens_k=_ptr(seqlens_k), total_sequence_length=int(total_sequence_length),
+        attention_bias=_ptr(attention_bias), bias_stride_b=sb, bias_stride_h=sh,
+        bias_stride_s=ss, output=_ptr(output), output_f64=_ptr(output_f64),
+        resident_len=_ptr(resident),
+    )
+    rc = lib.oracle_step(ctypes.byref(a))
+    if rc != 0:
+        raise ValueError("oracle.step: " + _ERRORS.get(rc, "error %d" % rc))
+    return {
+        "output": output,
+        "output_f64": output_f64,
+        "present_key": present_key,
+        "present_value": present_value,
+        "resident_len": resident,
+    }

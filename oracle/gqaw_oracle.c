@@ -1,0 +1,252 @@
+/*
+ * gqaw_oracle.c -- reference oracle for one windowed-KV-cache GroupQueryAttention step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, fp64-accumulating CPU
+ * statement of what the step computes.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load it.  The product path (the CUDA library)
+ * shares no code, header, table or helper with it and never calls it.
+ *
+ * Sources (web pages; the contract is stated in prose and one formula):
+ *  [P1] onnxruntime PR #32419 "Specify GroupQueryAttention windowed KV cache layout
+ *       contract", Description: the resident-count formula L(T), the row layout
+ *       (row i holds absolute position T - L + i), multi-token steps, the rollback
+ *       rule, and attention_bias in absolute key coordinates.  Its review thread:
+ *       T is taken per batch item, T_b = seqlens_k[b] + 1.
+ *  [P2] onnxruntime PR #31142 "[CPU] Add windowed kv cache for GQA", Key design
+ *       decisions: drifting layout, block compaction, staging; review thread:
+ *       64-bit planner arithmetic, past length P = seqlens_k[b] + 1 - S.
+ *  [P3] onnxruntime/mobius issue #111 "GQA In-Place KV Cache: Investigation Report",
+ *       Part 1.1 (inputs/outputs) and 1.3 (num_heads, kv_num_heads, scale, softcap).
+ *  [P4] onnxruntime PR #34226 "Fix CPU Attention causal mask for q_len=1 with
+ *       past_key and kv_len > 1", Description: key j is visible to query i iff
+ *       j <= i + past_sequence_length.
+ *
+ * Readings taken where the pages are silent (each is listed in the design notes):
+ *  - window: query at absolute position i sees keys j with i - W < j <= i (W keys
+ *    including itself), the causal rule of [P4] combined with the local window;
+ *  - logit order: z = softcap * tanh(scale * q.k / softcap) (if softcap > 0),
+ *    then + attention_bias[b, h, s, j];
+ *  - head grouping: query head h reads kv head h / (num_heads / kv_num_heads);
+ *  - multi-token steps with batch > 1 are allowed; every item uses the same S and
+ *    its own P_b = T_b - S; P_b < 0 is an error;
+ *  - the output is rounded once, from fp64, to the cache dtype (round to nearest
+ *    even).
+ *
+ * Precision: every input element is widened exactly to double; dot products,
+ * softcap, softmax and the weighted sum are evaluated in double in ascending key
+ * order; present rows are bit copies.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+enum {
+  ORACLE_OK = 0,
+  ORACLE_EARGS = 1,     /* malformed sizes */
+  ORACLE_EPAST = 2,     /* seqlens_k[b] + 1 - S < 0 for some item */
+  ORACLE_ETOTAL = 3,    /* T_b > total_sequence_length for some item */
+  ORACLE_ENOMEM = 4
+};
+
+typedef struct oracle_args {
+  int64_t batch_size;        /* B */
+  int64_t sequence_length;   /* S, new tokens in this step */
+  int64_t num_heads;         /* Nq */
+  int64_t kv_num_heads;      /* Nkv */
+  int64_t head_size;         /* D */
+  int64_t capacity;          /* C, dimension 2 of past_key */
+  int64_t local_window_size; /* W */
+  double scale;              /* already resolved: the caller passes 1/sqrt(D) for the default */
+  double softcap;            /* 0: disabled */
+  int64_t dtype;             /* ORACLE_F32 or ORACLE_BF16; all tensors but bias share it */
+  const void *query;         /* (B, S, Nq*D) */
+  const void *key;           /* (B, S, Nkv*D) */
+  const void *value;         /* (B, S, Nkv*D) */
+  const void *past_key;      /* (B, Nkv, C, D), read only */
+  const void *past_value;    /* (B, Nkv, C, D), read only */
+  void *present_key;         /* (B, Nkv, C, D), distinct from past; rows [0, L) written */
+  void *present_value;       /* (B, Nkv, C, D) */
+  const int32_t *seqlens_k;  /* (B,) */
+  int64_t total_sequence_length;
+  const float *attention_bias; /* NULL or element [b*sb + h*sh + s*ss + j] */
+  int64_t bias_stride_b, bias_stride_h, bias_stride_s;
+  void *output;              /* (B, S, Nq*D) in dtype */
+  double *output_f64;        /* NULL or (B, S, Nq*D), before the final rounding */
+  int32_t *resident_len;     /* NULL or (B,), L(T_b) after the step */
+} oracle_args;
+
+/* [P1] Description, resident-count formula:
+ *   L(T) = T                          if T <= C
+ *   L(T) = T - G * ceil((T - C) / G)  otherwise,   G = C - W + 1.
+ * Evaluated in 64-bit integers ([P2] review thread). */
+int64_t oracle_resident_len(int64_t T, int64_t C, int64_t W) {
+  int64_t G, blocks;
+  if (T <= C) return T;
+  G = C - W + 1;
+  blocks = (T - C + G - 1) / G; /* ceil for positive operands */
+  return T - G * blocks;
+}
+
+/* Round a double to the nearest bfloat16, ties to even, in one step.
+ * bfloat16 keeps 8 significant bits and the float exponent range. */
+uint16_t oracle_round_bf16(double x) {
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  double a = fabs(x), r, y;
+  int e, q;
+  float f;
+  uint32_t bits;
+  if (isnan(x)) return 0x7fc0u;
+  if (a == 0.0) return sign;
+  if (isinf(x)) return (uint16_t)(sign | 0x7f80u);
+  frexp(a, &e);            /* a = m * 2^e, m in [0.5, 1) */
+  q = e - 8;               /* spacing of 8-significant-bit numbers near a */
+  if (q < -133) q = -133;  /* spacing of bfloat16 subnormals */
+  r = nearbyint(ldexp(a, -q)); /* default rounding mode: nearest, ties to even */
+  y = ldexp(r, q);
+  if (y > 3.38953138925153547590470800371487867e38) return (uint16_t)(sign | 0x7f80u);
+  f = (float)y; /* exact: y has at most 9 significant bits */
+  memcpy(&bits, &f, 4);
+  return (uint16_t)(sign | (bits >> 16));
+}
+
+static double load_elem(const void *base, int64_t idx, int64_t dtype) {
+  if (dtype == ORACLE_F32) {
+    float f;
+    memcpy(&f, (const char *)base + idx * 4, 4);
+    return (double)f;
+  } else {
+    uint16_t h;
+    uint32_t bits;
+    float f;
+    memcpy(&h, (const char *)base + idx * 2, 2);
+    bits = ((uint32_t)h) << 16;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+  }
+}
+
+static void store_elem(void *base, int64_t idx, int64_t dtype, double v) {
+  if (dtype == ORACLE_F32) {
+    float f = (float)v; /* C conversion: round to nearest even */
+    memcpy((char *)base + idx * 4, &f, 4);
+  } else {
+    uint16_t h = oracle_round_bf16(v);
+    memcpy((char *)base + idx * 2, &h, 2);
+  }
+}
+
+/* Element offset of row r (0-based) of slice (b, kvh) in a (B, Nkv, C, D) cache. */
+static int64_t cache_row(const oracle_args *a, int64_t b, int64_t kvh, int64_t r) {
+  return ((b * a->kv_num_heads + kvh) * a->capacity + r) * a->head_size;
+}
+
+/* Element offset of new token s of kv head kvh in a (B, S, Nkv*D) input. */
+static int64_t input_row(const oracle_args *a, int64_t b, int64_t s, int64_t kvh) {
+  return ((b * a->sequence_length + s) * a->kv_num_heads + kvh) * a->head_size;
+}
+
+/* One step for one batch item.  The virtual sequence X of item b has Lp + S rows:
+ * X[r] = past row r for r < Lp, else new token r - Lp.  X[r] holds absolute
+ * position P - Lp + r ([P1] row layout applied to the past length P). */
+static int step_item(const oracle_args *a, int64_t b, double *z, double *acc) {
+  const int64_t S = a->sequence_length, D = a->head_size, W = a->local_window_size;
+  const int64_t Nq = a->num_heads, Nkv = a->kv_num_heads, C = a->capacity;
+  const int64_t group = Nq / Nkv;
+  const int64_t esize = a->dtype == ORACLE_F32 ? 4 : 2;
+  const int64_t T = (int64_t)a->seqlens_k[b] + 1; /* [P1] review: T_b = seqlens_k[b] + 1 */
+  const int64_t P = T - S;                         /* [P2] review: past length */
+  int64_t Lp, Lt, first_pos, s, h, kvh, r, d, j;
+
+  if (P < 0) return ORACLE_EPAST;
+  if (T > a->total_sequence_length) return ORACLE_ETOTAL;
+  Lp = oracle_resident_len(P, C, W);
+  Lt = oracle_resident_len(T, C, W);
+  first_pos = P - Lp; /* absolute position of X[0] */
+
+  /* Attention ([P4] causal rule, local window of W keys, [P3] scale/softcap,
+   * [P1] absolute-column attention_bias). */
+  for (s = 0; s < S; ++s) {
+    const int64_t i = P + s; /* absolute position of query s */
+    int64_t jlo = i - W + 1;
+    if (jlo < 0) jlo = 0;
+    if (jlo < first_pos) jlo = first_pos; /* never taken: Lp >= min(P, W) */
+    for (h = 0; h < Nq; ++h) {
+      const int64_t qoff = ((b * S + s) * Nq + h) * D;
+      double zmax = -INFINITY, denom = 0.0;
+      kvh = h / group;
+      for (j = jlo; j <= i; ++j) {
+        const int64_t xr = j - first_pos;
+        const void *kb = xr < Lp ? a->past_key : a->key;
+        const int64_t koff = xr < Lp ? cache_row(a, b, kvh, xr) : input_row(a, b, xr - Lp, kvh);
+        double dot = 0.0, zj;
+        for (d = 0; d < D; ++d)
+          dot += load_elem(a->query, qoff + d, a->dtype) * load_elem(kb, koff + d, a->dtype);
+        zj = a->scale * dot;
+        if (a->softcap > 0.0) zj = a->softcap * tanh(zj / a->softcap);
+        if (a->attention_bias)
+          zj += (double)a->attention_bias[b * a->bias_stride_b + h * a->bias_stride_h +
+                                          s * a->bias_stride_s + j];
+        z[j - jlo] = zj;
+        if (zj > zmax) zmax = zj;
+      }
+      for (d = 0; d < D; ++d) acc[d] = 0.0;
+      for (j = jlo; j <= i; ++j) {
+        const int64_t xr = j - first_pos;
+        const void *vb = xr < Lp ? a->past_value : a->value;
+        const int64_t voff = xr < Lp ? cache_row(a, b, kvh, xr) : input_row(a, b, xr - Lp, kvh);
+        const double p = exp(z[j - jlo] - zmax);
+        denom += p;
+        for (d = 0; d < D; ++d) acc[d] += p * load_elem(vb, voff + d, a->dtype);
+      }
+      for (d = 0; d < D; ++d) {
+        const double o = acc[d] / denom;
+        store_elem(a->output, qoff + d, a->dtype, o);
+        if (a->output_f64) a->output_f64[qoff + d] = o;
+      }
+    }
+  }
+
+  /* Present layout ([P1] row layout): row r holds absolute position T - Lt + r,
+   * i.e. X[Lp + S - Lt + r].  Bit copies; rows [Lt, C) are left as they are. */
+  for (kvh = 0; kvh < Nkv; ++kvh) {
+    for (r = 0; r < Lt; ++r) {
+      const int64_t xr = Lp + S - Lt + r;
+      const int64_t src = xr < Lp ? cache_row(a, b, kvh, xr) : input_row(a, b, xr - Lp, kvh);
+      const void *ksrc = xr < Lp ? a->past_key : a->key;
+      const void *vsrc = xr < Lp ? a->past_value : a->value;
+      const int64_t dst = cache_row(a, b, kvh, r);
+      memcpy((char *)a->present_key + dst * esize, (const char *)ksrc + src * esize, D * esize);
+      memcpy((char *)a->present_value + dst * esize, (const char *)vsrc + src * esize, D * esize);
+    }
+  }
+  if (a->resident_len) a->resident_len[b] = (int32_t)Lt;
+  return ORACLE_OK;
+}
+
+/* Items are independent; the step is item by item.  Returns ORACLE_OK or the first
+ * error met (items before it are already written). */
+int oracle_step(const oracle_args *a) {
+  int64_t b, nz;
+  double *z, *acc;
+  int rc = ORACLE_OK;
+  if (a->batch_size < 0 || a->sequence_length < 1 || a->num_heads < 1 || a->kv_num_heads < 1 ||
+      a->num_heads % a->kv_num_heads != 0 || a->head_size < 1 || a->capacity < 1 ||
+      a->local_window_size < 1 || a->local_window_size > a->capacity ||
+      (a->dtype != ORACLE_F32 && a->dtype != ORACLE_BF16))
+    return ORACLE_EARGS;
+  nz = a->local_window_size;
+  z = (double *)malloc(sizeof(double) * (size_t)nz);
+  acc = (double *)malloc(sizeof(double) * (size_t)a->head_size);
+  if (!z || !acc) {
+    free(z);
+    free(acc);
+    return ORACLE_ENOMEM;
+  }
+  for (b = 0; b < a->batch_size && rc == ORACLE_OK; ++b) rc = step_item(a, b, z, acc);
+  free(z);
+  free(acc);
+  return rc;
+}
