@@ -1,0 +1,621 @@
+"""Benchmark of the windowed-GQA step on GB300; prints one JSON line.
+
+Default workload (``longctx-decode``): B=64, 32 query / 8 kv heads, head size 128,
+bf16 caches, W=4096, C=5120, per-item contexts ~ U[4096, 32768]; each step is one
+decode token for all 64 items through the C ABI.  The K/V window read per step
+(about 1.07 GB) is larger than the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl gqaw|reference]
+                    [--workload longctx-decode|pages-decode|slack-decode|verify8|longctx-prefill]
+                    [--no-extra] [--no-cpu-baseline]
+
+``--impl reference`` times the oracle (the plain fp64 CPU implementation) on this
+host's cores on the same workload, each step a bounded sample of items.
+
+Under torchrun (WORLD_SIZE > 1) every rank runs its own independent replica of the
+workload (different seeds, no exchange): weak scaling, no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "windowed-GQA decode tokens/s; KV HBM GB/s as % of GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ workloads
+
+
+def workload_spec(name):
+    import workloads as wl
+
+    if name == "longctx-decode":
+        return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False)
+    if name == "longctx-prefill":
+        sh = wl.SHAPES["longctx"]
+        return dict(shape=sh, S=512, lo=4096, hi=32768, bias=False, graph=False, accept=False, B=8)
+    if name == "pages-decode":
+        return dict(shape=wl.SHAPES["pages"], S=1, lo=8192, hi=8192, bias=False, graph=True, accept=False)
+    if name == "slack-decode":
+        return dict(shape=wl.SHAPES["slack"], S=1, lo=128, hi=160, bias=False, graph=True, accept=False)
+    if name == "verify8":
+        return dict(shape=wl.SHAPES["verify8"], S=8, lo=6000, hi=6000, bias=True, graph=True, accept=True)
+    raise SystemExit("unknown workload " + name)
+
+
+def resident_len(T, C, W):
+    """L(T) through the C ABI (host function of the library)."""
+    from sliding_window_gqa_02_gb300 import gqaw
+
+    return gqaw.gqaw_resident_len(int(T), int(C), int(W))
+
+
+def algorithmic_bytes(sh, S, T_before, B):
+    """Bytes the step must move (in-window cache rows + new rows read, append written,
+    compaction read + written, Q in, output out), per item, from the pre-step lengths.
+    Bias bytes are added by the caller."""
+    e = 2 if sh.dtype == "bf16" else 4
+    row = sh.Nkv * sh.D * e * 2  # K and V of one position, all kv heads
+    attn = comp = app = 0
+    for b in range(B):
+        P = int(T_before[b])
+        T = P + S
+        Lp, Lt = resident_len(P, sh.C, sh.W), resident_len(T, sh.C, sh.W)
+        kept = Lt - S
+        seed = Lp + S - Lt
+        attn += row * (min(P, sh.W - 1) + S)
+        app += row * min(S, Lt)
+        if seed > 0 and kept > 0:
+            comp += row * 2 * kept
+    qo = B * S * sh.Nq * sh.D * e * 2
+    return attn + qo, attn + app + comp + qo
+
+
+def visible_columns(S, T_before, W):
+    n = 0
+    for P in T_before:
+        for s in range(S):
+            n += min(int(P) + s + 1, W)
+    return n
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms in a background process."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if t0 <= t <= t1]
+        window = "timed region"
+        if not rows:  # timed region shorter than the sampling period: nearest samples
+            rows = [r for t, r in self.rows if t0 - 1.0 <= t <= t1 + 1.0]
+            window = "timed region +- 1 s"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if len(r) > 2 and num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if len(r) > 2 and num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows), "window": window}
+
+
+# ------------------------------------------------------------------ profiles (ncu traffic)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gqaw_attend.cuh", "gqaw_internal.cuh", "gqaw_attend_bf16.cu", "gqaw_attend_f32.cu"):
+        with open(os.path.join(ROOT, "sliding_window_gqa_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary of this workload,
+    or None if there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "attend_%s.md" % workload)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not hm or hm.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+class Harness:
+    """Device buffers and per-step argument structs for one workload replica."""
+
+    def __init__(self, name, steps, warmup, seed, split_keys=0):
+        import torch
+
+        import workloads as wl
+        from sliding_window_gqa_02_gb300 import gqaw
+
+        self.torch, self.wl, self.gqaw = torch, wl, gqaw
+        spec = workload_spec(name)
+        self.name, self.spec = name, spec
+        sh = spec["shape"]
+        self.sh = sh
+        self.B = spec.get("B", sh.B)
+        self.S = spec["S"]
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        self.stream = torch.cuda.Stream()  # every launch and copy of this replica goes here
+        n = steps + warmup
+        self.n = n
+        B, S = self.B, self.S
+        pk, pv = wl.cache(sh, seed, B=self.B)
+        self.pk, self.pv = pk.to(self.dev), pv.to(self.dev)
+        del pk, pv
+        T0 = wl.lengths(B, spec["lo"], spec["hi"], seed)
+        # per-step pre-step lengths (decode: +1; verify: + accepted; prefill: +S)
+        Ts = [T0.copy()]
+        for t in range(n):
+            if spec["accept"]:
+                Ts.append(Ts[-1] + wl.accepted(B, S, seed * 1000 + t))
+            else:
+                Ts.append(Ts[-1] + S)
+        self.T = np.stack(Ts[:n])  # (n, B) lengths before each step
+        seq = (self.T + S - 1).astype(np.int32)
+        self.seq_host = torch.from_numpy(seq).pin_memory()
+        self.seq = self.seq_host.to(self.dev)
+        self.totals = [int(self.T[t].max()) + S for t in range(n)]
+        nin = 4
+        ins = [wl.step_inputs(sh, S, seed * 100 + i, B=B) for i in range(nin)]
+        self.q_host = [x[0].pin_memory() for x in ins]
+        self.k_host = [x[1].pin_memory() for x in ins]
+        self.v_host = [x[2].pin_memory() for x in ins]
+        self.q = [x.to(self.dev) for x in self.q_host]
+        self.k = [x.to(self.dev) for x in self.k_host]
+        self.v = [x.to(self.dev) for x in self.v_host]
+        self.out = torch.empty_like(self.q[0])
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.bias = None
+        self.bias_strides = None
+        if spec["bias"]:
+            TM = max(self.totals)
+            self.bias = wl.bias(B, sh.Nq, S, TM, seed).to(self.dev)
+            self.bias_strides = (sh.Nq * S * TM, S * TM, TM)
+        self.split_keys = split_keys
+        self.args = []
+        ws_bytes = 0
+        for t in range(n):
+            a = self._args(t, None)
+            ws_bytes = max(ws_bytes, gqaw.gqaw_workspace_bytes(a))
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.dev)
+        gqaw.check(gqaw.gqaw_workspace_init(int(self.ws.data_ptr()), ws_bytes, self.stream.cuda_stream))
+        self.args = [self._args(t, self.ws) for t in range(n)]
+
+    def _args(self, t, ws):
+        i = t % len(self.q)
+        sh = self.sh
+        return self.gqaw.make_args(
+            self.q[i], self.k[i], self.v[i], self.pk, self.pv, self.pk, self.pv, self.seq[t], self.totals[t],
+            sh.Nq, sh.Nkv, sh.W, self.out, workspace=ws, softcap=sh.softcap, attention_bias=self.bias,
+            bias_strides=self.bias_strides, split_keys=self.split_keys)
+
+    def step(self, t):
+        self.gqaw.check(self.gqaw.gqa_windowed_step(self.args[t], self.stream.cuda_stream))
+
+    def step_phases(self, t, ev_mid):
+        g = self.gqaw
+        g.check(g.gqaw_attend(self.args[t], self.stream.cuda_stream))
+        ev_mid.record(self.stream)
+        g.check(g.gqaw_update_cache(self.args[t], self.stream.cuda_stream))
+
+    def step_e2e(self, t):
+        """One step through the C ABI from pinned host buffers: copy the step's query,
+        key, value and seqlens_k in, run the step, copy the output back."""
+        i = t % len(self.q)
+        self.q[0].copy_(self.q_host[i], non_blocking=True)
+        self.k[0].copy_(self.k_host[i], non_blocking=True)
+        self.v[0].copy_(self.v_host[i], non_blocking=True)
+        self.seq[t].copy_(self.seq_host[t], non_blocking=True)
+        a = self.args_e2e[t]
+        self.gqaw.check(self.gqaw.gqa_windowed_step(a, self.stream.cuda_stream))
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def prepare_e2e(self):
+        # every e2e step reads its inputs from slot 0, refreshed from the host
+        sh = self.sh
+        self.args_e2e = [self.gqaw.make_args(
+            self.q[0], self.k[0], self.v[0], self.pk, self.pv, self.pk, self.pv, self.seq[t], self.totals[t],
+            sh.Nq, sh.Nkv, sh.W, self.out, workspace=self.ws, softcap=sh.softcap, attention_bias=self.bias,
+            bias_strides=self.bias_strides, split_keys=self.split_keys) for t in range(self.n)]
+        e = self.q_host[0].element_size()
+        self.h2d = (self.q_host[0].numel() + self.k_host[0].numel() + self.v_host[0].numel()) * e + self.B * 4
+        self.d2h = self.out.numel() * self.out.element_size()
+
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import workloads as wl  # noqa: F401
+    from sliding_window_gqa_02_gb300 import build, gqaw
+
+    build.build()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    name = args.workload
+    K, Wm = args.steps, args.warmup
+    h = Harness(name, K, Wm, seed=11 + rank, split_keys=args.split_keys)
+    stream = h.stream
+    torch.cuda.synchronize()
+    torch.cuda.set_stream(stream)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.5)
+
+    for t in range(Wm):
+        h.step(t)
+    torch.cuda.synchronize()
+    _barrier(world)
+
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_end = torch.cuda.Event(enable_timing=True)
+    launches0 = gqaw.gqaw_launch_count()
+    if h.spec["graph"]:
+        # small, launch-bound workloads: the K steps are captured once as a CUDA graph
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for t in range(Wm, Wm + K):
+                h.step(t)
+        torch.cuda.synchronize()
+        launches0 = gqaw.gqaw_launch_count()
+        launches_per_step = 2
+        t_wall0 = time.time()
+        ev_a[0].record(stream)
+        g.replay()
+        ev_end.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        total_ms = ev_a[0].elapsed_time(ev_end)
+        attend_ms = None
+        launches = launches_per_step * K
+    else:
+        t_wall0 = time.time()
+        for j, t in enumerate(range(Wm, Wm + K)):
+            ev_a[j].record(stream)
+            h.step_phases(t, ev_m[j])
+        ev_end.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        total_ms = ev_a[0].elapsed_time(ev_end)
+        attend_ms = [ev_a[j].elapsed_time(ev_m[j]) for j in range(K)]
+        launches = gqaw.gqaw_launch_count() - launches0
+    clocks.stop()
+    total_ms = _max_over_ranks(total_ms, world)
+
+    sh, B, S = h.sh, h.B, h.S
+    tokens = B * S * K * world
+    value = tokens / (total_ms / 1e3)
+    peak, peak_src = measured_peaks()
+    e = 2 if sh.dtype == "bf16" else 4
+    att_bytes = step_bytes = 0.0
+    bias_bytes = 0.0
+    for t in range(Wm, Wm + K):
+        a, s = algorithmic_bytes(sh, S, h.T[t], B)
+        att_bytes += a
+        step_bytes += s
+        if h.bias is not None:
+            bias_bytes += 4 * sh.Nq * visible_columns(S, h.T[t], sh.W)
+    att_bytes += bias_bytes
+    step_bytes += bias_bytes
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": sh.dtype, "data": "synthetic",
+        "config": {"workload": name, "B": B, "S": S, "num_heads": sh.Nq, "kv_num_heads": sh.Nkv,
+                   "head_size": sh.D, "local_window_size": sh.W, "capacity": sh.C, "softcap": sh.softcap,
+                   "contexts": "U[%d,%d]" % (h.spec["lo"], h.spec["hi"]),
+                   "l2": "no flush: K/V window per step %.0f MB > 129 MB L2" % (step_bytes / K / 1e6)
+                   if step_bytes / K > 129e6 else "CUDA-graph replay, working set L2-resident",
+                   "launch": "CUDA graph of K steps" if h.spec["graph"] else "stream launches",
+                   "parallelism": "replicas x%d" % world},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    step_gbs = step_bytes / (total_ms / 1e3) / 1e9 / world * world
+    result["step_hbm"] = {"achieved_gbs": step_gbs, "frac_of_peak": step_gbs / peak, "peak_gbs": peak,
+                          "peak_source": peak_src, "bytes_per_step": step_bytes / K}
+    if attend_ms is not None:
+        am = statistics.mean(attend_ms)
+        ach = att_bytes / K / (am / 1e3) / 1e9
+        traffic = profiled_traffic(name)
+        result["roofline"] = {"kernel": "attend_kernel", "bound": "hbm", "achieved": ach, "peak": peak,
+                              "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
+                              "algorithmic_bytes_per_launch": att_bytes / K, "avg_launch_ms": am,
+                              "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
+    # end-to-end through the C ABI with host buffers (the e2e pass re-runs the same
+    # step indices on the advanced cache: the step function is defined for any buffer)
+    h.prepare_e2e()
+    for t in range(min(Wm, 3)):
+        h.step_e2e(t)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(Wm, Wm + K):
+        h.step_e2e(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world)
+    result["e2e"] = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h.h2d,
+                     "d2h_bytes_per_step": h.d2h, "ms_per_step": e2e_ms / K}
+    torch.cuda.set_stream(torch.cuda.default_stream())
+    del h
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        result["cpu_baseline"] = cpu_baseline(name, budget_s=args.cpu_seconds)
+    if rank == 0 and not args.no_extra:
+        result["workloads"] = extra_workloads(name, args)
+    return result
+
+
+def extra_workloads(main, args):
+    """Short measurements of the other workloads (context; not the headline)."""
+    import torch
+
+    out = {}
+    for name in ("pages-decode", "slack-decode", "verify8", "longctx-prefill"):
+        if name == main:
+            continue
+        K = 64 if name != "longctx-prefill" else 8
+        Wm = 3
+        h = Harness(name, K, Wm, seed=5)
+        torch.cuda.synchronize()
+        torch.cuda.set_stream(h.stream)
+        for t in range(Wm):
+            h.step(t)
+        torch.cuda.synchronize()
+        if h.spec["graph"]:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=h.stream):
+                for t in range(Wm, Wm + K):
+                    h.step(t)
+            torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(h.stream)
+        if h.spec["graph"]:
+            g.replay()
+        else:
+            for t in range(Wm, Wm + K):
+                h.step(t)
+        e1.record(h.stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / K
+        _, sb = algorithmic_bytes(h.sh, h.S, h.T[Wm], h.B)
+        entry = {"ms_per_step": ms, "tokens_per_s": h.B * h.S / (ms / 1e3),
+                 "step_gbs": sb / (ms / 1e3) / 1e9, "B": h.B, "S": h.S, "dtype": h.sh.dtype,
+                 "launch": "CUDA graph" if h.spec["graph"] else "stream"}
+        if h.S > 1:
+            flops = 0
+            for P in h.T[Wm]:
+                for s in range(h.S):
+                    flops += h.sh.Nq * 4 * h.sh.D * min(int(P) + s + 1, h.sh.W)
+            entry["tflops"] = flops / (ms / 1e3) / 1e12
+        out[name] = entry
+        torch.cuda.synchronize()
+        torch.cuda.set_stream(torch.cuda.default_stream())
+        del h
+        torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+
+
+def oracle_item_step(name, seed, b_items, t_index=0):
+    """Run the oracle on items ``b_items`` of one step of ``name``; returns seconds."""
+    import oracle
+    import workloads as wl
+
+    spec = workload_spec(name)
+    sh = spec["shape"]
+    B = spec.get("B", sh.B)
+    S = spec["S"]
+    T0 = wl.lengths(B, spec["lo"], spec["hi"], seed) + t_index * S
+    q, k, v = wl.step_inputs(sh, S, seed * 100 + (t_index % 4), B=B)
+    nq, nk, nv = wl.to_numpy(q), wl.to_numpy(k), wl.to_numpy(v)
+    odt = oracle.F32 if sh.dtype == wl.F32 else oracle.BF16
+    el = 0.0
+    for b in b_items:
+        pk, pv = wl.cache(sh, seed * 7919 + b, B=1)
+        npk, npv = wl.to_numpy(pk), wl.to_numpy(pv)
+        seq = (T0[b:b + 1] + S - 1).astype(np.int32)
+        total = int(seq.max()) + 1
+        bias = None
+        if spec["bias"]:
+            bias = wl.to_numpy(wl.bias(1, sh.Nq, S, total, seed + b))
+        t0 = time.perf_counter()
+        oracle.step(nq[b:b + 1], nk[b:b + 1], nv[b:b + 1], npk, npv, seq, total, sh.Nq, sh.Nkv, sh.W,
+                    softcap=sh.softcap, attention_bias=bias, dtype=odt)
+        el += time.perf_counter() - t0
+    return el
+
+
+def cpu_baseline(name, budget_s=15.0):
+    """The oracle as it stands, single-threaded, on items of the same workload until
+    about ``budget_s`` seconds of oracle time; tokens/s = tokens computed / time."""
+    spec = workload_spec(name)
+    B = spec.get("B", spec["shape"].B)
+    S = spec["S"]
+    done, el, b = 0, 0.0, 0
+    while el < budget_s and done < B:
+        el += oracle_item_step(name, 11, [b])
+        done += 1
+        b += 1
+    return {"value": done * S / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d items of one %s step (%d token(s) each), fp64 C oracle, 1 thread, %.1f s"
+                      % (done, B, name, S, el)}
+
+
+def run_reference(args):
+    """The reference arm: the oracle on host cores, each step a bounded sample."""
+    spec = workload_spec(args.workload)
+    B = spec.get("B", spec["shape"].B)
+    S = spec["S"]
+    K, Wm = args.steps, args.warmup
+    t_item = oracle_item_step(args.workload, 11, [0])
+    per_step = max(1, min(B, int(120.0 / max(K + Wm, 1) / max(t_item, 1e-6))))
+    for t in range(Wm):
+        oracle_item_step(args.workload, 11, [(t * per_step + j) % B for j in range(per_step)], t)
+    el = 0.0
+    for t in range(K):
+        el += oracle_item_step(args.workload, 11, [((Wm + t) * per_step + j) % B for j in range(per_step)], Wm + t)
+    tokens = K * per_step * S
+    value = tokens / el
+    sample = "%d of %d items per step, %d steps, fp64 C oracle, 1 thread" % (per_step, B, K)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": K,
+            "warmup": Wm, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "S": S},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ distributed helpers
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        if not dist.is_initialized():
+            backend = os.environ.get("GQAW_DIST_BACKEND", "nccl")
+            if backend == "nccl":
+                import torch
+
+                torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            dist.init_process_group(backend)
+    return rank, world
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gqaw", choices=["gqaw", "reference"])
+    ap.add_argument("--workload", default="longctx-decode")
+    ap.add_argument("--split-keys", type=int, default=0)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, world = _dist()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

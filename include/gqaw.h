@@ -1,0 +1,172 @@
+/*
+ * gqaw.h -- C ABI of the windowed-KV-cache GroupQueryAttention step for GB300 (sm_103a).
+ *
+ * One call computes one com.microsoft::GroupQueryAttention step over a sliding-window
+ * ("windowed") KV cache, as specified by these pages:
+ *
+ *  [P1] onnxruntime PR #32419 "Specify GroupQueryAttention windowed KV cache layout
+ *       contract", Description: capacity C (dimension 2 of past_key), window
+ *       W = local_window_size, G = C - W + 1, resident count
+ *           L(T) = T                          if T <= C
+ *           L(T) = T - G * ceil((T - C) / G)  otherwise,
+ *       row i of present_key/present_value holds absolute position T - L + i for
+ *       i in [0, L) and rows [L, C) are unspecified; any S >= 1 is accepted, including
+ *       S > C; rejecting k draft tokens needs no cache edit and is exact iff
+ *       L(T - k) == L(T) - k; the attention_bias last dimension stays
+ *       total_sequence_length, indexed by absolute key position.  Review thread:
+ *       T is per batch item, T_b = seqlens_k[b] + 1.
+ *  [P2] onnxruntime PR #31142 "[CPU] Add windowed kv cache for GQA", Key design
+ *       decisions: drifting layout (a whole G-row block is reclaimed at once),
+ *       compaction skipped on drifting steps, staging for hazardous multi-token
+ *       steps; review thread: planner arithmetic in 64-bit, P = seqlens_k[b] + 1 - S.
+ *  [P3] onnxruntime/mobius issue #111 "GQA In-Place KV Cache: Investigation Report",
+ *       Part 1.1 (inputs and outputs, BNSH caches), 1.2 (past and present may be one
+ *       buffer), 1.3 (num_heads, kv_num_heads, scale = 1/sqrt(head_dim) by default,
+ *       local_window_size, softcap with 0 = disabled).
+ *  [P4] onnxruntime PR #34226 "Fix CPU Attention causal mask for q_len=1 with past_key
+ *       and kv_len > 1", Description: key j is visible to query i iff
+ *       j <= i + past_sequence_length.
+ *
+ * What a step computes, per batch item b (T = seqlens_k[b] + 1, P = T - S,
+ * Lp = L(P), Lt = L(T)):
+ *   - the query of new token s sits at absolute position i = P + s and attends the
+ *     keys j with i - W < j <= i (causal rule of [P4] plus the local window of W keys
+ *     including itself); query head h reads kv head h / (num_heads / kv_num_heads);
+ *     logit z_j = scale * q.k_j, then softcap * tanh(z_j / softcap) if softcap > 0,
+ *     then + attention_bias[b, h, s, j]; softmax over the visible keys; output is the
+ *     weighted sum of the values, rounded to the cache dtype;
+ *   - present rows [0, Lt) receive the Lt most recent positions of the past rows
+ *     [0, Lp) followed by the S new rows (bit copies).
+ *
+ * Memory.  The caller owns every buffer.  The library allocates nothing; all work is
+ * enqueued on the caller's stream and the call returns without synchronising.
+ *
+ * Errors.  Every function returning gqaw_status checks its arguments on the host first
+ * and, if they are wrong, returns an error code before enqueuing anything and leaves
+ * every output untouched; gqaw_last_error() then describes the problem.  Per-item
+ * problems only visible on the device (seqlens_k[b] + 1 - S < 0, or
+ * seqlens_k[b] + 1 > total_sequence_length) set a bit of the device status word kept in
+ * the workspace; that item's output and present rows are then unspecified and the
+ * other items are computed normally.  gqaw_device_status() reads the word.  No kernel
+ * traps; every wait inside a kernel is bounded and sets a status bit if it expires.
+ */
+#ifndef GQAW_H
+#define GQAW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gqaw_status {
+  GQAW_OK = 0,
+  GQAW_EINVAL = 1,      /* an argument is malformed (null, misaligned, out of range) */
+  GQAW_EUNSUPPORTED = 2, /* well formed but not implemented (e.g. head_size 96) */
+  GQAW_ECUDA = 3,       /* a CUDA runtime call failed; gqaw_last_error() has its message */
+  GQAW_EWORKSPACE = 4,  /* workspace missing, misaligned or smaller than gqaw_workspace_bytes() */
+  GQAW_EDEVICE = 5      /* gqaw_device_status(): the device status word is non-zero */
+} gqaw_status;
+
+typedef enum gqaw_dtype {
+  GQAW_F32 = 0, /* float32 query/key/value/cache/output */
+  GQAW_BF16 = 1 /* bfloat16 query/key/value/cache/output */
+} gqaw_dtype;
+
+/* Bits of the device status word. */
+#define GQAW_DEV_BAD_SEQLEN 1u /* some seqlens_k[b] + 1 - S < 0 or > total_sequence_length */
+#define GQAW_DEV_TIMEOUT 2u    /* a bounded in-kernel wait expired (an internal fault) */
+
+/* Arguments of one step.  All tensor pointers are DEVICE pointers.  Layouts are
+ * row-major with the shapes given; "BNSH" is (batch, kv head, row, head_size).
+ * Alignment: every tensor pointer except seqlens_k and attention_bias must be 16-byte
+ * aligned; seqlens_k and attention_bias 4-byte aligned; workspace 256-byte aligned. */
+typedef struct gqaw_step_args {
+  int32_t batch_size;            /* B >= 0; B == 0 is a valid empty step */
+  int32_t sequence_length;       /* S >= 1 new tokens per item (same S for every item) */
+  int32_t num_heads;             /* Nq >= 1 */
+  int32_t kv_num_heads;          /* Nkv >= 1, Nq % Nkv == 0 */
+  int32_t head_size;             /* D: one of 8, 16, 32, 64, 128, 256 */
+  int32_t capacity;              /* C >= 1: rows per (b, kv head) slice of the caches */
+  int32_t local_window_size;     /* W, 1 <= W <= C */
+  int32_t dtype;                 /* gqaw_dtype of query/key/value/caches/output */
+  float scale;                   /* > 0, or 0 for the default 1/sqrt(D) */
+  float softcap;                 /* >= 0; 0 disables soft-capping */
+  int32_t total_sequence_length; /* host scalar >= S: max_b T_b, the bias column count */
+  int32_t split_keys;            /* 0: automatic; > 0 overrides the keys per split-K chunk */
+  const void *query;             /* (B, S, Nq*D) */
+  const void *key;               /* (B, S, Nkv*D): the S new keys */
+  const void *value;             /* (B, S, Nkv*D): the S new values */
+  const void *past_key;          /* (B, Nkv, C, D) BNSH; rows [0, L(P_b)) are read */
+  const void *past_value;        /* (B, Nkv, C, D) BNSH */
+  void *present_key;             /* (B, Nkv, C, D): == past_key (in place) or disjoint */
+  void *present_value;           /* (B, Nkv, C, D): == past_value (in place) or disjoint */
+  const int32_t *seqlens_k;      /* (B,) int32: T_b - 1 */
+  const float *attention_bias;   /* NULL, or fp32 element [b*sb + h*sh + s*ss + j] with
+                                    j in [0, total_sequence_length) the absolute key
+                                    position; the last dimension is contiguous */
+  int64_t bias_stride_b;         /* sb >= 0 (elements; 0 broadcasts over the batch) */
+  int64_t bias_stride_h;         /* sh >= 0 (0 broadcasts over heads) */
+  int64_t bias_stride_s;         /* ss >= 0 */
+  void *output;                  /* (B, S, Nq*D) */
+  void *workspace;               /* device scratch of gqaw_workspace_bytes() bytes; its
+                                    first 256 bytes hold the device status word and must
+                                    be zeroed once (gqaw_workspace_init) before first use */
+  size_t workspace_bytes;
+  int32_t *resident_len_out;     /* NULL, or (B,) int32 receiving L(T_b) */
+} gqaw_step_args;
+
+/* L(T) of [P1] in 64-bit arithmetic.  Pure host function.  Returns -1 if T < 0,
+ * C < 1, W < 1 or W > C. */
+int64_t gqaw_resident_len(int64_t T, int64_t C, int64_t W);
+
+/* Rollback rule of [P1]: 1 if rejecting the last k tokens of a cache of length T is
+ * exact (L(T - k) == L(T) - k), 0 if not, -1 on invalid arguments (k < 0, k > T, or
+ * invalid T, C, W as for gqaw_resident_len).  Pure host function. */
+int gqaw_rollback_exact(int64_t T, int64_t k, int64_t C, int64_t W);
+
+/* Workspace bytes the step needs for these arguments (only the size fields, dtype and
+ * split_keys are read; pointers may be NULL).  Returns 0 if the sizes are invalid
+ * (gqaw_last_error() says why).  Always at least 256. */
+size_t gqaw_workspace_bytes(const gqaw_step_args *args);
+
+/* Zero the device status word at the start of `workspace` on `stream`. */
+gqaw_status gqaw_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/* One whole step, enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream): attention over the pre-step cache rows and the new rows, then the cache
+ * update (block compaction on eviction steps, append of the new rows).  Equivalent to
+ * gqaw_attend() followed by gqaw_update_cache() on the same stream. */
+gqaw_status gqa_windowed_step(const gqaw_step_args *args, void *stream);
+
+/* First phase only: attention.  Reads query, key, value, past rows and the bias; writes
+ * the output, or per-split partial results into the workspace when the keys are split.
+ * Does not write present_key/present_value. */
+gqaw_status gqaw_attend(const gqaw_step_args *args, void *stream);
+
+/* Second phase only: merges split partial results into the output (when the keys were
+ * split), moves the surviving rows and appends the new rows ([P2] block compaction and
+ * append), writes resident_len_out.  Must follow gqaw_attend() with the same arguments
+ * on the same stream (the in-place update overwrites rows the attention reads). */
+gqaw_status gqaw_update_cache(const gqaw_step_args *args, void *stream);
+
+/* Copy the device status word of `workspace` to *flags (synchronises `stream`); zero it
+ * afterwards if `reset` is non-zero.  Returns GQAW_EDEVICE if the word was non-zero. */
+gqaw_status gqaw_device_status(void *workspace, uint32_t *flags, int reset, void *stream);
+
+/* Message of the last error returned on the calling thread ("" if none). */
+const char *gqaw_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t gqaw_launch_count(void);
+
+/* sizeof(gqaw_step_args) as compiled into the library, so that a binding written in
+ * another language can check its copy of the struct layout. */
+size_t gqaw_step_args_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQAW_H */

@@ -20,13 +20,14 @@ from __future__ import annotations
 import ctypes
 import math
 import os
+import platform
 import subprocess
 
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gqaw_oracle.c")
-_LIB = os.path.join(_HERE, "liboracle_gqaw.so")
+_LIB = os.path.join(_HERE, "liboracle_gqaw.%s.so" % platform.machine())
 
 F32 = 0
 BF16 = 1
@@ -67,6 +68,8 @@ class _Args(ctypes.Structure):
         ("output", ctypes.c_void_p),
         ("output_f64", ctypes.c_void_p),
         ("resident_len", ctypes.c_void_p),
+        ("s_begin", ctypes.c_int64),
+        ("s_end", ctypes.c_int64),
     ]
 
 
@@ -121,7 +124,7 @@ def _elem_dtype(dtype: int):
 
 def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_length,
          num_heads, kv_num_heads, local_window_size, scale=0.0, softcap=0.0,
-         attention_bias=None, bias_strides=None, dtype=F32):
+         attention_bias=None, bias_strides=None, dtype=F32, rows=None):
     """One windowed GQA step on host arrays.
 
     Arrays are numpy: float32 for ``dtype=F32``; uint16 bfloat16 bit patterns for
@@ -133,7 +136,9 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
 
     Returns dict(output, output_f64, present_key, present_value, resident_len).
     The present arrays start as copies of the past arrays; rows [0, L) are written.
-    ``scale == 0`` selects 1/sqrt(head_size).
+    ``scale == 0`` selects 1/sqrt(head_size).  ``rows=(s0, s1)`` evaluates the attention
+    only for new tokens s0 <= s < s1 (other output rows stay zero); ``rows=(0, 0)``
+    gives the cache layout alone.
     """
     lib = _load()
     et = _elem_dtype(dtype)
@@ -177,6 +182,8 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
         attention_bias=_ptr(attention_bias), bias_stride_b=sb, bias_stride_h=sh,
         bias_stride_s=ss, output=_ptr(output), output_f64=_ptr(output_f64),
         resident_len=_ptr(resident),
+        s_begin=0 if rows is None else int(rows[0]),
+        s_end=S if rows is None else int(rows[1]),
     )
     rc = lib.oracle_step(ctypes.byref(a))
     if rc != 0:

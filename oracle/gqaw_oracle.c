@@ -76,6 +76,9 @@ typedef struct oracle_args {
   void *output;              /* (B, S, Nq*D) in dtype */
   double *output_f64;        /* NULL or (B, S, Nq*D), before the final rounding */
   int32_t *resident_len;     /* NULL or (B,), L(T_b) after the step */
+  int64_t s_begin, s_end;    /* attention is evaluated for new tokens s in [s_begin, s_end)
+                                only (outputs of other rows are left as they are); the
+                                present rows are always written */
 } oracle_args;
 
 /* [P1] Description, resident-count formula:
@@ -168,7 +171,7 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc) {
 
   /* Attention ([P4] causal rule, local window of W keys, [P3] scale/softcap,
    * [P1] absolute-column attention_bias). */
-  for (s = 0; s < S; ++s) {
+  for (s = a->s_begin; s < a->s_end && s < S; ++s) {
     const int64_t i = P + s; /* absolute position of query s */
     int64_t jlo = i - W + 1;
     if (jlo < 0) jlo = 0;

@@ -1,0 +1,350 @@
+// gqaw_host.cu -- the C ABI of include/gqaw.h: argument checks, launch planning and
+// kernel launches.  No allocation, no synchronisation (except gqaw_device_status).
+//
+// A step is two kernels on the caller's stream:
+//   1. attention (attend_kernel): reads the pre-step cache rows and the new rows, so a
+//      multi-token step that evicts rows its own queries need is handled without any
+//      staging copy (onnxruntime PR #31142 "[CPU] Add windowed kv cache for GQA",
+//      Key design decisions, "Staging for hazardous steps": the CPU copies into a
+//      temporary cache; here the order of the two kernels makes that unnecessary);
+//   2. finish (finish_kernel): split combine, block compaction, append.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "gqaw_internal.cuh"
+
+namespace gqaw {
+cudaError_t launch_attend_f32(const Params &p, int gb, int blocks, cudaStream_t stream);
+cudaError_t launch_attend_bf16(const Params &p, int gb, int blocks, cudaStream_t stream);
+int attend_tile_f32(int D);
+int attend_tile_bf16(int D);
+cudaError_t launch_finish(const Params &p, int dtype, int blocks, cudaStream_t stream);
+}  // namespace gqaw
+
+namespace {
+
+thread_local std::string t_error;
+std::atomic<unsigned long long> g_launches{0ull};
+
+// Split-K sizing aims at about this many attention CTAs per step (152 SMs x 16).
+constexpr long long kTargetCtas = 2432;
+// Largest cache bytes one column-group block of the finish kernel moves.
+constexpr long long kCopyChainBytes = 64 * 1024;
+
+gqaw_status fail(gqaw_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_error = buf;
+  return s;
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Launch {
+  int esize, rowbytes, group, gb, headblocks, tile, nsplit, chunk, ncg;
+  long long units, attend_blocks, ncombine, ncopy;
+  size_t off_m, off_l, off_acc, ws_bytes;
+};
+
+bool head_size_ok(int D) { return D == 8 || D == 16 || D == 32 || D == 64 || D == 128 || D == 256; }
+
+// Sizes only: everything gqaw_workspace_bytes needs.
+gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
+  if (!a) return fail(GQAW_EINVAL, "args is NULL");
+  if (a->batch_size < 0) return fail(GQAW_EINVAL, "batch_size %d < 0", a->batch_size);
+  if (a->sequence_length < 1) return fail(GQAW_EINVAL, "sequence_length %d < 1", a->sequence_length);
+  if (a->num_heads < 1 || a->kv_num_heads < 1)
+    return fail(GQAW_EINVAL, "num_heads %d and kv_num_heads %d must be >= 1", a->num_heads, a->kv_num_heads);
+  if (a->num_heads % a->kv_num_heads != 0)
+    return fail(GQAW_EINVAL, "num_heads %d is not a multiple of kv_num_heads %d", a->num_heads, a->kv_num_heads);
+  if (a->dtype != GQAW_F32 && a->dtype != GQAW_BF16) return fail(GQAW_EINVAL, "unknown dtype %d", a->dtype);
+  if (a->head_size < 1) return fail(GQAW_EINVAL, "head_size %d < 1", a->head_size);
+  if (!head_size_ok(a->head_size))
+    return fail(GQAW_EUNSUPPORTED, "head_size %d: supported are 8, 16, 32, 64, 128, 256", a->head_size);
+  if (a->capacity < 1) return fail(GQAW_EINVAL, "capacity %d < 1", a->capacity);
+  if (a->local_window_size < 1 || a->local_window_size > a->capacity)
+    return fail(GQAW_EINVAL, "local_window_size %d must be in [1, capacity=%d]", a->local_window_size,
+                a->capacity);
+  if (a->total_sequence_length < a->sequence_length)
+    return fail(GQAW_EINVAL, "total_sequence_length %d < sequence_length %d", a->total_sequence_length,
+                a->sequence_length);
+  if (!(a->scale >= 0.f) || !std::isfinite(a->scale)) return fail(GQAW_EINVAL, "scale must be finite and >= 0");
+  if (!(a->softcap >= 0.f) || !std::isfinite(a->softcap))
+    return fail(GQAW_EINVAL, "softcap must be finite and >= 0");
+  if (a->split_keys < 0) return fail(GQAW_EINVAL, "split_keys %d < 0", a->split_keys);
+
+  L->esize = a->dtype == GQAW_F32 ? 4 : 2;
+  L->rowbytes = a->head_size * L->esize;
+  L->group = a->num_heads / a->kv_num_heads;
+  L->gb = 1;  // query heads per CTA: the next power of two >= group, at most 8
+  while (L->gb < L->group && L->gb < 8) L->gb *= 2;
+  L->headblocks = (int)ceil_div(L->group, L->gb);
+  L->tile = a->dtype == GQAW_F32 ? gqaw::attend_tile_f32(a->head_size) : gqaw::attend_tile_bf16(a->head_size);
+  L->units = (long long)a->batch_size * a->sequence_length * a->kv_num_heads * L->headblocks;
+
+  const long long keys_max =
+      a->local_window_size < a->total_sequence_length ? a->local_window_size : a->total_sequence_length;
+  long long chunk;
+  if (a->split_keys > 0) {
+    chunk = ceil_div(a->split_keys, L->tile) * L->tile;
+  } else {
+    long long want = L->units > 0 ? ceil_div(kTargetCtas, L->units) : 1;
+    const long long most = ceil_div(keys_max, 2LL * L->tile);
+    if (want > most) want = most;
+    if (want < 1) want = 1;
+    chunk = ceil_div(ceil_div(keys_max, want), L->tile) * L->tile;
+  }
+  if (chunk > keys_max) chunk = ceil_div(keys_max, L->tile) * L->tile;
+  L->chunk = (int)chunk;
+  L->nsplit = (int)ceil_div(keys_max, chunk);
+  L->attend_blocks = L->units * L->nsplit;
+  if (L->attend_blocks > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many attention blocks");
+
+  const int nv = L->rowbytes / 16;
+  L->ncg = 1;
+  while (L->ncg * 2 <= nv / 2 && (long long)a->capacity * L->rowbytes / L->ncg > kCopyChainBytes) L->ncg *= 2;
+
+  const long long nrows = (long long)a->batch_size * a->sequence_length * a->num_heads;
+  L->off_m = L->off_l = L->off_acc = 0;
+  L->ws_bytes = 256;  // device status word
+  if (L->nsplit > 1) {
+    L->off_m = 256;
+    L->off_l = L->off_m + align256((size_t)nrows * L->nsplit * 4);
+    L->off_acc = L->off_l + align256((size_t)nrows * L->nsplit * 4);
+    L->ws_bytes = L->off_acc + align256((size_t)nrows * L->nsplit * a->head_size * 4);
+  }
+  L->ncombine = L->nsplit > 1 ? ceil_div(nrows * a->head_size, 256) : 0;
+  L->ncopy = (long long)a->batch_size * a->kv_num_heads * 2 * L->ncg;
+  if (L->ncombine + L->ncopy > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many finish blocks");
+  return GQAW_OK;
+}
+
+bool aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+struct Range {
+  const char *lo, *hi;
+  const char *name;
+};
+
+bool overlap(const Range &x, const Range &y) { return x.lo < y.hi && y.lo < x.hi; }
+
+gqaw_status check_pointers(const gqaw_step_args *a, const Launch &L) {
+  struct {
+    const void *p;
+    const char *name;
+  } req[] = {{a->query, "query"},           {a->key, "key"},
+             {a->value, "value"},           {a->past_key, "past_key"},
+             {a->past_value, "past_value"}, {a->present_key, "present_key"},
+             {a->present_value, "present_value"}, {a->seqlens_k, "seqlens_k"},
+             {a->output, "output"}};
+  for (auto &r : req) {
+    if (!r.p) return fail(GQAW_EINVAL, "%s is NULL", r.name);
+    const size_t al = r.p == (const void *)a->seqlens_k ? 4 : 16;
+    if (!aligned(r.p, al)) return fail(GQAW_EINVAL, "%s is not %zu-byte aligned", r.name, al);
+  }
+  if (a->attention_bias) {
+    if (!aligned(a->attention_bias, 4)) return fail(GQAW_EINVAL, "attention_bias is not 4-byte aligned");
+    if (a->bias_stride_b < 0 || a->bias_stride_h < 0 || a->bias_stride_s < 0)
+      return fail(GQAW_EINVAL, "attention_bias strides must be >= 0");
+  }
+  if (!a->workspace) return fail(GQAW_EWORKSPACE, "workspace is NULL");
+  if (!aligned(a->workspace, 256)) return fail(GQAW_EWORKSPACE, "workspace is not 256-byte aligned");
+  if (a->workspace_bytes < L.ws_bytes)
+    return fail(GQAW_EWORKSPACE, "workspace_bytes %zu < required %zu", a->workspace_bytes, L.ws_bytes);
+
+  const size_t B = (size_t)a->batch_size, S = (size_t)a->sequence_length, D = (size_t)a->head_size;
+  const size_t cache = B * a->kv_num_heads * (size_t)a->capacity * D * L.esize;
+  const size_t qo = B * S * a->num_heads * D * L.esize, kv = B * S * a->kv_num_heads * D * L.esize;
+  auto rng = [](const void *p, size_t n, const char *name) {
+    return Range{static_cast<const char *>(p), static_cast<const char *>(p) + n, name};
+  };
+  const Range pk = rng(a->past_key, cache, "past_key"), pv = rng(a->past_value, cache, "past_value");
+  const Range rk = rng(a->present_key, cache, "present_key"), rv = rng(a->present_value, cache, "present_value");
+  const Range q = rng(a->query, qo, "query"), k = rng(a->key, kv, "key"), v = rng(a->value, kv, "value");
+  const Range o = rng(a->output, qo, "output"), ws = rng(a->workspace, L.ws_bytes, "workspace");
+  // present_key is past_key (in place) or disjoint from it; the same for values.
+  if (a->present_key != a->past_key && overlap(rk, pk))
+    return fail(GQAW_EINVAL, "present_key partially overlaps past_key");
+  if (a->present_value != a->past_value && overlap(rv, pv))
+    return fail(GQAW_EINVAL, "present_value partially overlaps past_value");
+  const Range *written[] = {&rk, &rv, &o, &ws};
+  const Range *all[] = {&pk, &pv, &rk, &rv, &q, &k, &v, &o, &ws};
+  for (const Range *w : written)
+    for (const Range *x : all) {
+      if (w == x) continue;
+      if ((w == &rk && x == &pk && a->present_key == a->past_key) ||
+          (w == &rv && x == &pv && a->present_value == a->past_value))
+        continue;
+      if (overlap(*w, *x)) return fail(GQAW_EINVAL, "%s overlaps %s", w->name, x->name);
+    }
+  return GQAW_OK;
+}
+
+void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
+  std::memset(p, 0, sizeof(*p));
+  p->q = a->query;
+  p->k = a->key;
+  p->v = a->value;
+  p->pk = a->past_key;
+  p->pv = a->past_value;
+  p->prk = a->present_key;
+  p->prv = a->present_value;
+  p->seqlens = a->seqlens_k;
+  p->bias = a->attention_bias;
+  p->bsb = a->bias_stride_b;
+  p->bsh = a->bias_stride_h;
+  p->bss = a->bias_stride_s;
+  p->out = a->output;
+  char *ws = static_cast<char *>(a->workspace);
+  p->status = reinterpret_cast<uint32_t *>(ws);
+  if (L.nsplit > 1) {
+    p->ws_m = reinterpret_cast<float *>(ws + L.off_m);
+    p->ws_l = reinterpret_cast<float *>(ws + L.off_l);
+    p->ws_acc = reinterpret_cast<float *>(ws + L.off_acc);
+  }
+  p->resident_out = a->resident_len_out;
+  p->B = a->batch_size;
+  p->S = a->sequence_length;
+  p->Nq = a->num_heads;
+  p->Nkv = a->kv_num_heads;
+  p->D = a->head_size;
+  p->C = a->capacity;
+  p->W = a->local_window_size;
+  p->total = a->total_sequence_length;
+  p->group = L.group;
+  p->headblocks = L.headblocks;
+  p->nsplit = L.nsplit;
+  p->chunk = L.chunk;
+  const float scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt((float)a->head_size);
+  if (a->softcap > 0.f) {
+    p->qscale = scale / a->softcap;
+    p->capmul = a->softcap * gqaw::kLog2e;
+  } else {
+    p->qscale = scale * gqaw::kLog2e;
+    p->capmul = 0.f;
+  }
+  p->biasmul = gqaw::kLog2e;
+  p->ncg = L.ncg;
+  p->ncombine = (int)L.ncombine;
+  p->rowbytes = L.rowbytes;
+}
+
+gqaw_status prepare(const gqaw_step_args *a, Launch *L, gqaw::Params *p) {
+  gqaw_status s = plan_launch(a, L);
+  if (s != GQAW_OK) return s;
+  if (a->batch_size == 0) return GQAW_OK;
+  s = check_pointers(a, *L);
+  if (s != GQAW_OK) return s;
+  fill_params(a, *L, p);
+  return GQAW_OK;
+}
+
+gqaw_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(GQAW_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+gqaw_status run_attend(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
+  const cudaError_t e = a->dtype == GQAW_F32 ? gqaw::launch_attend_f32(p, L.gb, (int)L.attend_blocks, st)
+                                             : gqaw::launch_attend_bf16(p, L.gb, (int)L.attend_blocks, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+  g_launches.fetch_add(1);
+  return GQAW_OK;
+}
+
+gqaw_status run_finish(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
+  const cudaError_t e = gqaw::launch_finish(p, a->dtype, (int)(L.ncombine + L.ncopy), st);
+  if (e != cudaSuccess) return cuda_fail(e, "finish kernel launch");
+  g_launches.fetch_add(1);
+  return GQAW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t gqaw_resident_len(int64_t T, int64_t C, int64_t W) {
+  if (T < 0 || C < 1 || W < 1 || W > C) return -1;
+  if (T <= C) return T;
+  const int64_t G = C - W + 1;
+  return T - G * ((T - C + G - 1) / G);
+}
+
+int gqaw_rollback_exact(int64_t T, int64_t k, int64_t C, int64_t W) {
+  if (k < 0 || k > T) return -1;
+  const int64_t a = gqaw_resident_len(T - k, C, W), b = gqaw_resident_len(T, C, W);
+  if (a < 0 || b < 0) return -1;
+  return a == b - k ? 1 : 0;
+}
+
+size_t gqaw_workspace_bytes(const gqaw_step_args *args) {
+  Launch L;
+  if (plan_launch(args, &L) != GQAW_OK) return 0;
+  return L.ws_bytes;
+}
+
+gqaw_status gqaw_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+  if (!workspace) return fail(GQAW_EWORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(GQAW_EWORKSPACE, "workspace is not 256-byte aligned");
+  if (workspace_bytes < 256) return fail(GQAW_EWORKSPACE, "workspace_bytes %zu < 256", workspace_bytes);
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return GQAW_OK;
+}
+
+gqaw_status gqa_windowed_step(const gqaw_step_args *args, void *stream) {
+  Launch L;
+  gqaw::Params p;
+  gqaw_status s = prepare(args, &L, &p);
+  if (s != GQAW_OK || args->batch_size == 0) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = run_attend(args, L, p, st);
+  if (s != GQAW_OK) return s;
+  return run_finish(args, L, p, st);
+}
+
+gqaw_status gqaw_attend(const gqaw_step_args *args, void *stream) {
+  Launch L;
+  gqaw::Params p;
+  gqaw_status s = prepare(args, &L, &p);
+  if (s != GQAW_OK || args->batch_size == 0) return s;
+  return run_attend(args, L, p, static_cast<cudaStream_t>(stream));
+}
+
+gqaw_status gqaw_update_cache(const gqaw_step_args *args, void *stream) {
+  Launch L;
+  gqaw::Params p;
+  gqaw_status s = prepare(args, &L, &p);
+  if (s != GQAW_OK || args->batch_size == 0) return s;
+  return run_finish(args, L, p, static_cast<cudaStream_t>(stream));
+}
+
+gqaw_status gqaw_device_status(void *workspace, uint32_t *flags, int reset, void *stream) {
+  if (!workspace) return fail(GQAW_EWORKSPACE, "workspace is NULL");
+  if (!flags) return fail(GQAW_EINVAL, "flags is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (reset) {
+    e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  }
+  if (*flags) return fail(GQAW_EDEVICE, "device status 0x%x", *flags);
+  return GQAW_OK;
+}
+
+const char *gqaw_last_error(void) { return t_error.c_str(); }
+
+uint64_t gqaw_launch_count(void) { return g_launches.load(); }
+
+size_t gqaw_step_args_size(void) { return sizeof(gqaw_step_args); }
+
+}  // extern "C"

@@ -1,0 +1,165 @@
+// gqaw_internal.cuh -- device-side building blocks shared by the step's kernels.
+//
+// The per-item plan follows onnxruntime PR #32419 "Specify GroupQueryAttention
+// windowed KV cache layout contract" (Description: L(T), row layout) and PR #31142
+// "[CPU] Add windowed kv cache for GQA" (review thread: 64-bit planner arithmetic,
+// past length P = seqlens_k[b] + 1 - S).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gqaw.h"
+
+namespace gqaw {
+
+// Everything a kernel needs, passed by value.
+struct Params {
+  const void *q, *k, *v;     // (B,S,Nq*D), (B,S,Nkv*D), (B,S,Nkv*D)
+  const void *pk, *pv;       // past (B,Nkv,C,D)
+  void *prk, *prv;           // present (B,Nkv,C,D)
+  const int32_t *seqlens;    // (B,)
+  const float *bias;         // NULL or [b*bsb + h*bsh + s*bss + j]
+  long long bsb, bsh, bss;
+  void *out;                 // (B,S,Nq*D)
+  float *ws_m, *ws_l;        // split partials: running max (log2 units) and sum
+  float *ws_acc;             // split partials: unnormalised weighted values
+  uint32_t *status;          // device status word
+  int32_t *resident_out;     // NULL or (B,)
+  int B, S, Nq, Nkv, D, C, W, total, group;
+  int headblocks;            // query-head blocks per kv head
+  int nsplit;                // key chunks per query row
+  int chunk;                 // keys per chunk (multiple of the tile)
+  float qscale;              // q multiplier: scale*log2(e), or scale/softcap with softcap
+  float capmul;              // softcap*log2(e), or 0 without softcap
+  float biasmul;             // log2(e)
+  int ncg;                   // column groups per cache row in the copy jobs
+  int ncombine;              // blocks of the finish kernel that merge split partials
+  int rowbytes;              // D * element size
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// L(T) in 64-bit integers.
+__device__ __forceinline__ long long resident_len(long long T, long long C, long long W) {
+  if (T <= C) return T;
+  const long long G = C - W + 1;
+  return T - G * ((T - C + G - 1) / G);
+}
+
+struct Plan {
+  long long T, P, Lp, Lt;
+};
+
+// Per-item plan.  Returns false (and the caller flags the item) when the item's
+// seqlens_k is out of range.
+__device__ __forceinline__ bool plan_item(const Params &p, int b, Plan &pl) {
+  const long long T = (long long)p.seqlens[b] + 1;
+  const long long P = T - p.S;
+  if (P < 0 || T > (long long)p.total) return false;
+  pl.T = T;
+  pl.P = P;
+  pl.Lp = resident_len(P, p.C, p.W);
+  pl.Lt = resident_len(T, p.C, p.W);
+  return true;
+}
+
+__device__ __forceinline__ void flag(const Params &p, uint32_t bits) { atomicOr(p.status, bits); }
+
+// ---------------------------------------------------------------- conversions
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kPerVec = 4;
+  __device__ __forceinline__ static void unpack(const uint4 &u, float *f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+  __device__ __forceinline__ static float store(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kPerVec = 8;
+  // A bfloat16 is the high half of a float32: widening is a shift (exact).
+  __device__ __forceinline__ static void unpack(const uint4 &u, float *f) {
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xffff0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xffff0000u);
+    f[4] = __uint_as_float(u.z << 16);
+    f[5] = __uint_as_float(u.z & 0xffff0000u);
+    f[6] = __uint_as_float(u.w << 16);
+    f[7] = __uint_as_float(u.w & 0xffff0000u);
+  }
+  __device__ __forceinline__ static __nv_bfloat16 store(float x) { return __float2bfloat16_rn(x); }
+};
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete; give up after about
+// two seconds of SM clock (4e9 cycles) (returns false: the caller flags GQAW_DEV_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > 4000000000ll) return false;
+  }
+  return true;
+}
+
+// Bulk (non-tensor) TMA copy global -> shared, completing on `bar` with tx bytes.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read once (K/V rows of the window).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace gqaw

@@ -1,0 +1,234 @@
+"""ctypes binding of ``libgqaw.so`` (include/gqaw.h), with the same function names.
+
+This module only marshals arguments: every step of the computation runs in the CUDA
+kernels of the library.  If the library has not been built the first call raises;
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libgqaw.so")
+
+GQAW_OK = 0
+GQAW_EINVAL = 1
+GQAW_EUNSUPPORTED = 2
+GQAW_ECUDA = 3
+GQAW_EWORKSPACE = 4
+GQAW_EDEVICE = 5
+
+GQAW_F32 = 0
+GQAW_BF16 = 1
+
+GQAW_DEV_BAD_SEQLEN = 1
+GQAW_DEV_TIMEOUT = 2
+
+STATUS_NAMES = {0: "GQAW_OK", 1: "GQAW_EINVAL", 2: "GQAW_EUNSUPPORTED", 3: "GQAW_ECUDA",
+                4: "GQAW_EWORKSPACE", 5: "GQAW_EDEVICE"}
+
+EXPORTED = ["gqaw_resident_len", "gqaw_rollback_exact", "gqaw_workspace_bytes", "gqaw_workspace_init",
+            "gqa_windowed_step", "gqaw_attend", "gqaw_update_cache", "gqaw_device_status",
+            "gqaw_last_error", "gqaw_launch_count", "gqaw_step_args_size"]
+
+
+class gqaw_step_args(ctypes.Structure):
+    """Mirror of ``gqaw_step_args`` in include/gqaw.h (same field order and types)."""
+
+    _fields_ = [
+        ("batch_size", ctypes.c_int32),
+        ("sequence_length", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("kv_num_heads", ctypes.c_int32),
+        ("head_size", ctypes.c_int32),
+        ("capacity", ctypes.c_int32),
+        ("local_window_size", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("softcap", ctypes.c_float),
+        ("total_sequence_length", ctypes.c_int32),
+        ("split_keys", ctypes.c_int32),
+        ("query", ctypes.c_void_p),
+        ("key", ctypes.c_void_p),
+        ("value", ctypes.c_void_p),
+        ("past_key", ctypes.c_void_p),
+        ("past_value", ctypes.c_void_p),
+        ("present_key", ctypes.c_void_p),
+        ("present_value", ctypes.c_void_p),
+        ("seqlens_k", ctypes.c_void_p),
+        ("attention_bias", ctypes.c_void_p),
+        ("bias_stride_b", ctypes.c_int64),
+        ("bias_stride_h", ctypes.c_int64),
+        ("bias_stride_s", ctypes.c_int64),
+        ("output", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("resident_len_out", ctypes.c_void_p),
+    ]
+
+
+class GqawError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once).  Raises if it is missing: there is no CPU path."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libgqaw.so is not built (%s); run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(gqaw_step_args)
+    lib.gqaw_resident_len.restype = ctypes.c_int64
+    lib.gqaw_resident_len.argtypes = [ctypes.c_int64] * 3
+    lib.gqaw_rollback_exact.restype = ctypes.c_int
+    lib.gqaw_rollback_exact.argtypes = [ctypes.c_int64] * 4
+    lib.gqaw_workspace_bytes.restype = ctypes.c_size_t
+    lib.gqaw_workspace_bytes.argtypes = [P]
+    lib.gqaw_workspace_init.restype = ctypes.c_int
+    lib.gqaw_workspace_init.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    for name in ("gqa_windowed_step", "gqaw_attend", "gqaw_update_cache"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [P, ctypes.c_void_p]
+    lib.gqaw_device_status.restype = ctypes.c_int
+    lib.gqaw_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int,
+                                       ctypes.c_void_p]
+    lib.gqaw_last_error.restype = ctypes.c_char_p
+    lib.gqaw_last_error.argtypes = []
+    lib.gqaw_launch_count.restype = ctypes.c_uint64
+    lib.gqaw_launch_count.argtypes = []
+    lib.gqaw_step_args_size.restype = ctypes.c_size_t
+    lib.gqaw_step_args_size.argtypes = []
+    if lib.gqaw_step_args_size() != ctypes.sizeof(gqaw_step_args):
+        raise RuntimeError("gqaw_step_args layout mismatch: library %d bytes, binding %d bytes"
+                           % (lib.gqaw_step_args_size(), ctypes.sizeof(gqaw_step_args)))
+    _lib = lib
+    return lib
+
+
+# ----------------------------------------------------------------- same-name wrappers
+
+
+def gqaw_resident_len(T: int, C: int, W: int) -> int:
+    return int(load().gqaw_resident_len(T, C, W))
+
+
+def gqaw_rollback_exact(T: int, k: int, C: int, W: int) -> int:
+    return int(load().gqaw_rollback_exact(T, k, C, W))
+
+
+def gqaw_workspace_bytes(args: gqaw_step_args) -> int:
+    return int(load().gqaw_workspace_bytes(ctypes.byref(args)))
+
+
+def gqaw_workspace_init(workspace: int, nbytes: int, stream: int = 0) -> int:
+    return int(load().gqaw_workspace_init(workspace, nbytes, stream))
+
+
+def gqa_windowed_step(args: gqaw_step_args, stream: int = 0) -> int:
+    return int(load().gqa_windowed_step(ctypes.byref(args), stream))
+
+
+def gqaw_attend(args: gqaw_step_args, stream: int = 0) -> int:
+    return int(load().gqaw_attend(ctypes.byref(args), stream))
+
+
+def gqaw_update_cache(args: gqaw_step_args, stream: int = 0) -> int:
+    return int(load().gqaw_update_cache(ctypes.byref(args), stream))
+
+
+def gqaw_device_status(workspace: int, reset: bool = False, stream: int = 0):
+    """Returns (status, flags)."""
+    flags = ctypes.c_uint32(0)
+    st = int(load().gqaw_device_status(workspace, ctypes.byref(flags), int(bool(reset)), stream))
+    return st, int(flags.value)
+
+
+def gqaw_last_error() -> str:
+    return load().gqaw_last_error().decode()
+
+
+def gqaw_launch_count() -> int:
+    return int(load().gqaw_launch_count())
+
+
+def check(status: int) -> None:
+    if status != GQAW_OK:
+        raise GqawError(status, gqaw_last_error())
+
+
+# ----------------------------------------------------------------- torch marshalling
+
+
+def _ptr(t):
+    return None if t is None else int(t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return GQAW_F32
+    if t.dtype == torch.bfloat16:
+        return GQAW_BF16
+    raise TypeError("query/key/value/caches must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def make_args(query, key, value, past_key, past_value, present_key, present_value, seqlens_k,
+              total_sequence_length: int, num_heads: int, kv_num_heads: int, local_window_size: int,
+              output, workspace=None, scale: float = 0.0, softcap: float = 0.0, attention_bias=None,
+              bias_strides=None, resident_len_out=None, split_keys: int = 0) -> gqaw_step_args:
+    """Fill a ``gqaw_step_args`` from CUDA tensors (shapes as in include/gqaw.h).
+
+    ``attention_bias``: fp32 tensor whose last dimension is contiguous; its (b, h, s)
+    strides are taken from the tensor (a size-1 dimension broadcasts with stride 0)
+    unless ``bias_strides`` gives them in elements.  ``workspace``: a uint8 CUDA
+    tensor, or None when only the size is wanted.
+    """
+    B, Nkv, C, D = past_key.shape
+    S = query.shape[1]
+    a = gqaw_step_args()
+    a.batch_size, a.sequence_length = int(B), int(S)
+    a.num_heads, a.kv_num_heads, a.head_size = int(num_heads), int(kv_num_heads), int(D)
+    a.capacity, a.local_window_size = int(C), int(local_window_size)
+    a.dtype = _dtype_code(past_key)
+    a.scale, a.softcap = float(scale), float(softcap)
+    a.total_sequence_length, a.split_keys = int(total_sequence_length), int(split_keys)
+    a.query, a.key, a.value = _ptr(query), _ptr(key), _ptr(value)
+    a.past_key, a.past_value = _ptr(past_key), _ptr(past_value)
+    a.present_key, a.present_value = _ptr(present_key), _ptr(present_value)
+    a.seqlens_k = _ptr(seqlens_k)
+    if attention_bias is not None:
+        if attention_bias.stride(-1) != 1:
+            raise ValueError("attention_bias: last dimension must be contiguous")
+        if bias_strides is None:
+            bb, bh, bs, _ = attention_bias.shape
+            st = attention_bias.stride()
+            bias_strides = (0 if bb == 1 else st[0], 0 if bh == 1 else st[1], 0 if bs == 1 else st[2])
+        a.attention_bias = _ptr(attention_bias)
+        a.bias_stride_b, a.bias_stride_h, a.bias_stride_s = (int(x) for x in bias_strides)
+    a.output = _ptr(output)
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = _ptr(workspace), int(workspace.numel() * workspace.element_size())
+    a.resident_len_out = _ptr(resident_len_out)
+    return a
+
+
+def new_workspace(args: gqaw_step_args, device, stream: int = 0):
+    """Allocate (torch) and zero-initialise a workspace large enough for ``args``."""
+    import torch
+
+    n = gqaw_workspace_bytes(args)
+    if n == 0:
+        check(GQAW_EINVAL)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    check(gqaw_workspace_init(int(ws.data_ptr()), n, stream))
+    return ws

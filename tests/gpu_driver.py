@@ -1,0 +1,97 @@
+"""Test helper: drive the CUDA library across steps, and compare with the oracle.
+
+The CUDA side is called only through the C ABI (``sliding_window_gqa_02_gb300.gqaw``);
+torch supplies device memory and the stream.  Nothing here computes any part of the
+step.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads as wl
+from sliding_window_gqa_02_gb300 import gqaw
+
+TOL = {wl.F32: 1e-5, wl.BF16: 2e-2}
+
+
+class GpuCache:
+    def __init__(self, B, Nq, Nkv, D, C, W, dtype, scale=0.0, softcap=0.0, past_key=None, past_value=None,
+                 inplace=True, split_keys=0):
+        self.dev = torch.device("cuda:0")
+        self.B, self.Nq, self.Nkv, self.D, self.C, self.W = B, Nq, Nkv, D, C, W
+        self.dtype, self.scale, self.softcap = dtype, scale, softcap
+        self.inplace, self.split_keys = inplace, split_keys
+        td = wl.TORCH_DTYPE[dtype]
+        z = torch.zeros((B, Nkv, C, D), dtype=td)
+        self.pk = (z if past_key is None else past_key).to(self.dev).contiguous()
+        self.pv = (z if past_value is None else past_value).to(self.dev).contiguous()
+        if not inplace:
+            self.rk = torch.full_like(self.pk, 7)  # stale rows: must never be read
+            self.rv = torch.full_like(self.pv, 7)
+
+    def step(self, q, k, v, seqlens, total=None, bias=None, bias_strides=None, phases=False):
+        seqlens = np.asarray(seqlens, np.int64)
+        if total is None:
+            total = int(seqlens.max()) + 1
+        dq, dk, dv = (t.to(self.dev).contiguous() for t in (q, k, v))
+        seq = torch.tensor(seqlens.astype(np.int32), device=self.dev)
+        out = torch.full_like(dq, float("nan"))
+        res = torch.full((self.B,), -1, dtype=torch.int32, device=self.dev)
+        dbias = None if bias is None else bias.to(self.dev)
+        rk, rv = (self.pk, self.pv) if self.inplace else (self.rk, self.rv)
+        kw = dict(scale=self.scale, softcap=self.softcap, attention_bias=dbias, bias_strides=bias_strides,
+                  resident_len_out=res, split_keys=self.split_keys)
+        args = gqaw.make_args(dq, dk, dv, self.pk, self.pv, rk, rv, seq, total, self.Nq, self.Nkv, self.W,
+                              out, **kw)
+        stream = torch.cuda.current_stream().cuda_stream
+        ws = gqaw.new_workspace(args, self.dev, stream)
+        args = gqaw.make_args(dq, dk, dv, self.pk, self.pv, rk, rv, seq, total, self.Nq, self.Nkv, self.W,
+                              out, workspace=ws, **kw)
+        if phases:
+            gqaw.check(gqaw.gqaw_attend(args, stream))
+            gqaw.check(gqaw.gqaw_update_cache(args, stream))
+        else:
+            gqaw.check(gqaw.gqa_windowed_step(args, stream))
+        torch.cuda.synchronize()
+        st, flags = gqaw.gqaw_device_status(int(ws.data_ptr()), stream=stream)
+        if not self.inplace:
+            self.pk, self.rk = self.rk, self.pk
+            self.pv, self.rv = self.rv, self.pv
+        return {
+            "output": out.cpu(),
+            "resident_len": res.cpu().numpy(),
+            "present_key": wl.to_numpy(self.pk.cpu()),
+            "present_value": wl.to_numpy(self.pv.cpu()),
+            "device_flags": flags,
+        }
+
+
+def oracle_dtype(dtype):
+    import oracle
+
+    return oracle.F32 if dtype == wl.F32 else oracle.BF16
+
+
+def compare(gpu, ref, dtype, items=None, rows=None, check_layout=True):
+    """Assert parity: resident lengths equal, present rows [0, L_b) bit-exact for the
+    given items (all by default), output within TOL relative to the output's scale
+    (max |oracle|) over the given items and token rows.  Returns the output error."""
+    B = len(ref["resident_len"])
+    items = list(range(B)) if items is None else list(items)
+    assert gpu["device_flags"] == 0, "device status 0x%x" % gpu["device_flags"]
+    for b in items:
+        assert gpu["resident_len"][b] == ref["resident_len"][b], (b, gpu["resident_len"][b], ref["resident_len"][b])
+        if check_layout:
+            n = int(ref["resident_len"][b])
+            assert np.array_equal(gpu["present_key"][b, :, :n], ref["present_key"][b, :, :n]), "present_key item %d" % b
+            assert np.array_equal(gpu["present_value"][b, :, :n], ref["present_value"][b, :, :n]), "present_value item %d" % b
+    got = gpu["output"].float().numpy()[items]
+    exp = ref["output_f64"][items]
+    if rows is not None:
+        got, exp = got[:, rows[0]:rows[1]], exp[:, rows[0]:rows[1]]
+    assert np.all(np.isfinite(got)), "non-finite output"
+    scale = float(np.abs(exp).max())
+    err = float(np.abs(got - exp).max()) / (scale if scale > 0 else 1.0)
+    assert err <= TOL[dtype], "output error %.3g > %.3g" % (err, TOL[dtype])
+    return err
