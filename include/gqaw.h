@@ -165,6 +165,35 @@ uint64_t gqaw_launch_count(void);
  * another language can check its copy of the struct layout. */
 size_t gqaw_step_args_size(void);
 
+/* Size of the static scratch used by gqa_windowed_step_noalloc (8 MiB). */
+#define GQAW_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/* The same step as gqa_windowed_step, for callers that cannot allocate device memory
+ * (for example a plugin inside an inference runtime that owns all device memory and
+ * gives the plugin no allocator, or a serving loop that allows no allocation after
+ * start-up).  The pages have no counterpart: this is a deployment variant only.
+ *
+ * The split-K scratch normally taken from args->workspace comes instead from a
+ * fixed-size array compiled into the library (GQAW_NOALLOC_SCRATCH_BYTES; every GPU
+ * that loads the library holds it until the process exits).  args->workspace and
+ * args->workspace_bytes are ignored; all other fields mean what they mean for
+ * gqa_windowed_step.  Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
+ * library call.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current) and zeroes its status word with cudaMemsetAsync on
+ * `stream`; make that first call before any stream capture.  Later calls reuse the
+ * address.  Every call on a device shares the one array, which keeps the previous
+ * call's contents (each step overwrites every partial it reads, so nothing else needs
+ * clearing); calls that overlap on the GPU (several streams at once) race on it and
+ * must be ordered by the caller.  The device status word lives in the array and is not
+ * reported by this entry point.
+ *
+ * Returns GQAW_EWORKSPACE, before enqueuing anything, when the step needs more scratch
+ * than the array holds (gqaw_workspace_bytes(args) > GQAW_NOALLOC_SCRATCH_BYTES); the
+ * other errors are those of gqa_windowed_step. */
+gqaw_status gqa_windowed_step_noalloc(const gqaw_step_args *args, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -268,6 +268,11 @@ gqaw_status run_finish(const gqaw_step_args *a, const Launch &L, const gqaw::Par
 
 }  // namespace
 
+namespace gqaw {
+// Lets other translation units of the library report an error through gqaw_last_error().
+void set_error(const char *msg) { t_error = msg; }
+}  // namespace gqaw
+
 extern "C" {
 
 int64_t gqaw_resident_len(int64_t T, int64_t C, int64_t W) {

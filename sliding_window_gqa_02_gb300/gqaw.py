@@ -30,7 +30,9 @@ STATUS_NAMES = {0: "GQAW_OK", 1: "GQAW_EINVAL", 2: "GQAW_EUNSUPPORTED", 3: "GQAW
 
 EXPORTED = ["gqaw_resident_len", "gqaw_rollback_exact", "gqaw_workspace_bytes", "gqaw_workspace_init",
             "gqa_windowed_step", "gqaw_attend", "gqaw_update_cache", "gqaw_device_status",
-            "gqaw_last_error", "gqaw_launch_count", "gqaw_step_args_size"]
+            "gqaw_last_error", "gqaw_launch_count", "gqaw_step_args_size", "gqa_windowed_step_noalloc"]
+
+GQAW_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
 class gqaw_step_args(ctypes.Structure):
@@ -94,7 +96,7 @@ def load(path: str = LIB_PATH):
     lib.gqaw_workspace_bytes.argtypes = [P]
     lib.gqaw_workspace_init.restype = ctypes.c_int
     lib.gqaw_workspace_init.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
-    for name in ("gqa_windowed_step", "gqaw_attend", "gqaw_update_cache"):
+    for name in ("gqa_windowed_step", "gqaw_attend", "gqaw_update_cache", "gqa_windowed_step_noalloc"):
         f = getattr(lib, name)
         f.restype = ctypes.c_int
         f.argtypes = [P, ctypes.c_void_p]
@@ -135,6 +137,12 @@ def gqaw_workspace_init(workspace: int, nbytes: int, stream: int = 0) -> int:
 
 def gqa_windowed_step(args: gqaw_step_args, stream: int = 0) -> int:
     return int(load().gqa_windowed_step(ctypes.byref(args), stream))
+
+
+def gqa_windowed_step_noalloc(args: gqaw_step_args, stream: int = 0) -> int:
+    """The step with its scratch taken from the library's static array (for callers
+    that cannot allocate); ``args.workspace`` is ignored."""
+    return int(load().gqa_windowed_step_noalloc(ctypes.byref(args), stream))
 
 
 def gqaw_attend(args: gqaw_step_args, stream: int = 0) -> int:
