@@ -110,9 +110,13 @@ typedef struct gqaw_step_args {
   int64_t bias_stride_h;         /* sh >= 0 (0 broadcasts over heads) */
   int64_t bias_stride_s;         /* ss >= 0 */
   void *output;                  /* (B, S, Nq*D) */
-  void *workspace;               /* device scratch of gqaw_workspace_bytes() bytes; its
-                                    first 256 bytes hold the device status word and must
-                                    be zeroed once (gqaw_workspace_init) before first use */
+  void *workspace;               /* device scratch of gqaw_workspace_bytes() bytes, zeroed
+                                    once with gqaw_workspace_init() before first use (and
+                                    again after a device error); it holds the device
+                                    status word, the list of items whose rows move, the
+                                    split-K tickets and partial results.  Every completed
+                                    step leaves it ready for the next one.  Steps that
+                                    share a workspace must not overlap on the GPU. */
   size_t workspace_bytes;
   int32_t *resident_len_out;     /* NULL, or (B,) int32 receiving L(T_b) */
 } gqaw_step_args;
@@ -131,7 +135,7 @@ int gqaw_rollback_exact(int64_t T, int64_t k, int64_t C, int64_t W);
  * (gqaw_last_error() says why).  Always at least 256. */
 size_t gqaw_workspace_bytes(const gqaw_step_args *args);
 
-/* Zero the device status word at the start of `workspace` on `stream`. */
+/* Zero all `workspace_bytes` bytes of `workspace` on `stream` (cudaMemsetAsync). */
 gqaw_status gqaw_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /* One whole step, enqueued on `stream` (a cudaStream_t; NULL = the legacy default
@@ -140,15 +144,18 @@ gqaw_status gqaw_workspace_init(void *workspace, size_t workspace_bytes, void *s
  * gqaw_attend() followed by gqaw_update_cache() on the same stream. */
 gqaw_status gqa_windowed_step(const gqaw_step_args *args, void *stream);
 
-/* First phase only: attention.  Reads query, key, value, past rows and the bias; writes
- * the output, or per-split partial results into the workspace when the keys are split.
- * Does not write present_key/present_value. */
+/* First phase only (one kernel): the attention over the pre-step rows and the new rows,
+ * including the merge of split key chunks, so the output is complete when it ends;
+ * resident_len_out; the append of the new rows of every item that reclaims no block
+ * with past == present (rows [L(P), L(P) + S), which no query reads).  Items that
+ * reclaim a block ([P2] block compaction), and all items when present is a separate
+ * buffer, are recorded in the workspace for gqaw_update_cache(). */
 gqaw_status gqaw_attend(const gqaw_step_args *args, void *stream);
 
-/* Second phase only: merges split partial results into the output (when the keys were
- * split), moves the surviving rows and appends the new rows ([P2] block compaction and
- * append), writes resident_len_out.  Must follow gqaw_attend() with the same arguments
- * on the same stream (the in-place update overwrites rows the attention reads). */
+/* Second phase only (one kernel): for the items gqaw_attend() recorded, moves the
+ * surviving rows and appends the new rows; then clears the record.  Must follow
+ * gqaw_attend() with the same arguments on the same stream (the in-place update
+ * overwrites rows the attention reads). */
 gqaw_status gqaw_update_cache(const gqaw_step_args *args, void *stream);
 
 /* Copy the device status word of `workspace` to *flags (synchronises `stream`); zero it

@@ -8,6 +8,7 @@
 //      Key design decisions, "Staging for hazardous steps": the CPU copies into a
 //      temporary cache; here the order of the two kernels makes that unnecessary);
 //   2. finish (finish_kernel): split combine, block compaction, append.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -22,7 +23,7 @@ cudaError_t launch_attend_f32(const Params &p, int gb, int blocks, cudaStream_t 
 cudaError_t launch_attend_bf16(const Params &p, int gb, int blocks, cudaStream_t stream);
 int attend_tile_f32(int D);
 int attend_tile_bf16(int D);
-cudaError_t launch_finish(const Params &p, int dtype, int blocks, cudaStream_t stream);
+cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream);
 }  // namespace gqaw
 
 namespace {
@@ -30,10 +31,12 @@ namespace {
 thread_local std::string t_error;
 std::atomic<unsigned long long> g_launches{0ull};
 
-// Split-K sizing aims at about this many attention CTAs per step (152 SMs x 16).
-constexpr long long kTargetCtas = 2432;
-// Largest cache bytes one column-group block of the finish kernel moves.
+// Most attention CTAs of a step: GB300's 152 SMs x 2 resident CTAs per SM.
+constexpr long long kMaxCtas = 152 * 2;
+// Largest cache bytes one column-group job of the finish kernel moves.
 constexpr long long kCopyChainBytes = 64 * 1024;
+// Upper bound on the cache-update kernel's blocks (152 SMs x 2).
+constexpr long long kFinishBlocks = 152 * 2;
 
 gqaw_status fail(gqaw_status s, const char *fmt, ...) {
   char buf[512];
@@ -49,9 +52,9 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Launch {
-  int esize, rowbytes, group, gb, headblocks, tile, nsplit, chunk, ncg;
-  long long units, attend_blocks, ncombine, ncopy;
-  size_t off_m, off_l, off_acc, ws_bytes;
+  int esize, rowbytes, group, gb, headblocks, tile, tpu, ncg;
+  long long units, ctas, ncopy;
+  size_t off_list, off_tickets, off_partials, ws_bytes;
 };
 
 bool head_size_ok(int D) { return D == 8 || D == 16 || D == 32 || D == 64 || D == 128 || D == 256; }
@@ -90,40 +93,48 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   L->tile = a->dtype == GQAW_F32 ? gqaw::attend_tile_f32(a->head_size) : gqaw::attend_tile_bf16(a->head_size);
   L->units = (long long)a->batch_size * a->sequence_length * a->kv_num_heads * L->headblocks;
 
+  // Persistent stream-K attention: the step's work is units x tpu key tiles; the
+  // grid has at most kMaxCtas CTAs (the launch lowers it to the resident count), each
+  // taking a contiguous range of tiles.  split_keys > 0 asks for ranges of about that
+  // many keys instead.
   const long long keys_max =
       a->local_window_size < a->total_sequence_length ? a->local_window_size : a->total_sequence_length;
-  long long chunk;
-  if (a->split_keys > 0) {
-    chunk = ceil_div(a->split_keys, L->tile) * L->tile;
-  } else {
-    long long want = L->units > 0 ? ceil_div(kTargetCtas, L->units) : 1;
-    const long long most = ceil_div(keys_max, 2LL * L->tile);
-    if (want > most) want = most;
-    if (want < 1) want = 1;
-    chunk = ceil_div(ceil_div(keys_max, want), L->tile) * L->tile;
+  L->tpu = (int)ceil_div(keys_max, L->tile);
+  const long long vtiles = L->units * L->tpu;
+  long long ctas = std::min(vtiles, kMaxCtas);
+  if (vtiles < kMaxCtas && L->units > 0) {
+    // Less than one wave of tiles: latency decides.  Split each unit into k ranges
+    // (k CTAs per unit), trading tiles per CTA against the merge a split unit needs
+    // (about four tiles' worth of latency).
+    long long best_k = 1, best_cost = L->tpu;
+    for (long long k = 2; k <= L->tpu && L->units * k <= kMaxCtas; ++k) {
+      const long long cost = ceil_div(L->tpu, k) + 4;
+      if (cost < best_cost) {
+        best_cost = cost;
+        best_k = k;
+      }
+    }
+    ctas = L->units * best_k;
   }
-  if (chunk > keys_max) chunk = ceil_div(keys_max, L->tile) * L->tile;
-  L->chunk = (int)chunk;
-  L->nsplit = (int)ceil_div(keys_max, chunk);
-  L->attend_blocks = L->units * L->nsplit;
-  if (L->attend_blocks > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many attention blocks");
+  if (a->split_keys > 0) ctas = std::max(1LL, std::min(ctas, ceil_div(vtiles * L->tile, a->split_keys)));
+  L->ctas = ctas;
 
   const int nv = L->rowbytes / 16;
   L->ncg = 1;
   while (L->ncg * 2 <= nv / 2 && (long long)a->capacity * L->rowbytes / L->ncg > kCopyChainBytes) L->ncg *= 2;
 
-  const long long nrows = (long long)a->batch_size * a->sequence_length * a->num_heads;
-  L->off_m = L->off_l = L->off_acc = 0;
-  L->ws_bytes = 256;  // device status word
-  if (L->nsplit > 1) {
-    L->off_m = 256;
-    L->off_l = L->off_m + align256((size_t)nrows * L->nsplit * 4);
-    L->off_acc = L->off_l + align256((size_t)nrows * L->nsplit * 4);
-    L->ws_bytes = L->off_acc + align256((size_t)nrows * L->nsplit * a->head_size * 4);
-  }
-  L->ncombine = L->nsplit > 1 ? ceil_div(nrows * a->head_size, 256) : 0;
-  L->ncopy = (long long)a->batch_size * a->kv_num_heads * 2 * L->ncg;
-  if (L->ncombine + L->ncopy > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many finish blocks");
+  // Workspace: [0, 256) status word and the two counters of the cache-update list;
+  // the list itself (B items); per-unit tickets; two partial-result slots per
+  // attention CTA.  Everything must start at zero (gqaw_workspace_init); every step
+  // leaves the counters and tickets at zero again.
+  L->off_list = 256;
+  L->off_tickets = L->off_list + align256((size_t)a->batch_size * 4);
+  L->off_partials = L->off_tickets + align256((size_t)L->units * 4);
+  L->ws_bytes = L->off_partials + align256((size_t)L->ctas * 2 * L->gb * (a->head_size + 2) * 4);
+  // Cache-update kernel: grid-stride over the jobs of the registered items.
+  const long long jobs = (long long)a->batch_size * a->kv_num_heads * 2 * L->ncg;
+  if (jobs > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many cache-update jobs");
+  L->ncopy = std::min(jobs, kFinishBlocks);
   return GQAW_OK;
 }
 
@@ -205,11 +216,11 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
   p->out = a->output;
   char *ws = static_cast<char *>(a->workspace);
   p->status = reinterpret_cast<uint32_t *>(ws);
-  if (L.nsplit > 1) {
-    p->ws_m = reinterpret_cast<float *>(ws + L.off_m);
-    p->ws_l = reinterpret_cast<float *>(ws + L.off_l);
-    p->ws_acc = reinterpret_cast<float *>(ws + L.off_acc);
-  }
+  p->move_count = reinterpret_cast<uint32_t *>(ws + 4);
+  p->done_count = reinterpret_cast<uint32_t *>(ws + 8);
+  p->move_list = reinterpret_cast<int32_t *>(ws + L.off_list);
+  p->tickets = reinterpret_cast<uint32_t *>(ws + L.off_tickets);
+  p->partials = reinterpret_cast<float *>(ws + L.off_partials);
   p->resident_out = a->resident_len_out;
   p->B = a->batch_size;
   p->S = a->sequence_length;
@@ -221,8 +232,8 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
   p->total = a->total_sequence_length;
   p->group = L.group;
   p->headblocks = L.headblocks;
-  p->nsplit = L.nsplit;
-  p->chunk = L.chunk;
+  p->nunits = L.units;
+  p->tpu = L.tpu;
   const float scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt((float)a->head_size);
   if (a->softcap > 0.f) {
     p->qscale = scale / a->softcap;
@@ -233,7 +244,6 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
   }
   p->biasmul = gqaw::kLog2e;
   p->ncg = L.ncg;
-  p->ncombine = (int)L.ncombine;
   p->rowbytes = L.rowbytes;
 }
 
@@ -252,15 +262,15 @@ gqaw_status cuda_fail(cudaError_t e, const char *what) {
 }
 
 gqaw_status run_attend(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
-  const cudaError_t e = a->dtype == GQAW_F32 ? gqaw::launch_attend_f32(p, L.gb, (int)L.attend_blocks, st)
-                                             : gqaw::launch_attend_bf16(p, L.gb, (int)L.attend_blocks, st);
+  const cudaError_t e = a->dtype == GQAW_F32 ? gqaw::launch_attend_f32(p, L.gb, (int)L.ctas, st)
+                                             : gqaw::launch_attend_bf16(p, L.gb, (int)L.ctas, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   g_launches.fetch_add(1);
   return GQAW_OK;
 }
 
 gqaw_status run_finish(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
-  const cudaError_t e = gqaw::launch_finish(p, a->dtype, (int)(L.ncombine + L.ncopy), st);
+  const cudaError_t e = gqaw::launch_finish(p, (int)L.ncopy, st);
   if (e != cudaSuccess) return cuda_fail(e, "finish kernel launch");
   g_launches.fetch_add(1);
   return GQAW_OK;
@@ -299,7 +309,7 @@ gqaw_status gqaw_workspace_init(void *workspace, size_t workspace_bytes, void *s
   if (!workspace) return fail(GQAW_EWORKSPACE, "workspace is NULL");
   if (!aligned(workspace, 256)) return fail(GQAW_EWORKSPACE, "workspace is not 256-byte aligned");
   if (workspace_bytes < 256) return fail(GQAW_EWORKSPACE, "workspace_bytes %zu < 256", workspace_bytes);
-  const cudaError_t e = cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   return GQAW_OK;
 }

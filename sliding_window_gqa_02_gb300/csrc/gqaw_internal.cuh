@@ -23,19 +23,21 @@ struct Params {
   const float *bias;         // NULL or [b*bsb + h*bsh + s*bss + j]
   long long bsb, bsh, bss;
   void *out;                 // (B,S,Nq*D)
-  float *ws_m, *ws_l;        // split partials: running max (log2 units) and sum
-  float *ws_acc;             // split partials: unnormalised weighted values
+  float *partials;           // per attention CTA, 2 slots of GB x (D accumulators, max, sum)
   uint32_t *status;          // device status word
+  uint32_t *move_count;      // items registered for the cache-update kernel this step
+  uint32_t *done_count;      // cache-update blocks finished this step
+  int32_t *move_list;        // (B,) the registered items
+  uint32_t *tickets;         // per attention unit: contributors finished
   int32_t *resident_out;     // NULL or (B,)
   int B, S, Nq, Nkv, D, C, W, total, group;
   int headblocks;            // query-head blocks per kv head
-  int nsplit;                // key chunks per query row
-  int chunk;                 // keys per chunk (multiple of the tile)
+  long long nunits;          // attention units: B * S * Nkv * headblocks
+  int tpu;                   // key tiles per unit: ceil(min(W, total) / tile)
   float qscale;              // q multiplier: scale*log2(e), or scale/softcap with softcap
   float capmul;              // softcap*log2(e), or 0 without softcap
   float biasmul;             // log2(e)
   int ncg;                   // column groups per cache row in the copy jobs
-  int ncombine;              // blocks of the finish kernel that merge split partials
   int rowbytes;              // D * element size
 };
 
@@ -66,6 +68,15 @@ __device__ __forceinline__ bool plan_item(const Params &p, int b, Plan &pl) {
 }
 
 __device__ __forceinline__ void flag(const Params &p, uint32_t bits) { atomicOr(p.status, bits); }
+
+// Does item b need the cache-update kernel?  Yes when a block of rows is reclaimed
+// (seed = L(P) + S - L(T) > 0: rows move, and the new rows land on rows the attention
+// may still read) or when present is a separate buffer (every surviving row is
+// copied).  Otherwise the new rows go to rows [L(P), L(P) + S), which no query of the
+// step reads, and the attention kernel appends them itself.
+__device__ __forceinline__ bool item_moves(const Params &p, const Plan &pl) {
+  return pl.Lp + p.S - pl.Lt > 0 || p.pk != p.prk || p.pv != p.prv;
+}
 
 // ---------------------------------------------------------------- conversions
 
@@ -156,6 +167,17 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
+}
+
+// Programmatic dependent launch: the kernels of a step are launched with
+// programmatic stream serialisation, so a kernel may start while the previous one in
+// the stream drains.  pdl_wait() blocks until that previous kernel has completed and
+// its memory is visible; nothing produced upstream may be read before it.
+// pdl_launch_dependents() lets the next kernel in the stream be launched early (its
+// CTAs then wait in their own pdl_wait()).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {

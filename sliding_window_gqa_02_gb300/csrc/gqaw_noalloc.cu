@@ -30,7 +30,8 @@ std::mutex g_mutex;
 void *g_scratch_dev[kMaxDevices] = {nullptr};
 
 // Device address of g_scratch on the current device; the first call for a device
-// looks it up and zeroes the status word at its start (on `stream`).
+// looks it up and zeroes the whole array (on `stream`): the step's counters and
+// tickets must start at zero, and every step leaves them at zero again.
 gqaw_status scratch_for_current_device(void **out, cudaStream_t stream) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -50,7 +51,7 @@ gqaw_status scratch_for_current_device(void **out, cudaStream_t stream) {
       gqaw::set_error(e != cudaSuccess ? cudaGetErrorString(e) : "cudaGetSymbolAddress returned NULL");
       return GQAW_ECUDA;
     }
-    e = cudaMemsetAsync(p, 0, 256, stream);  // device status word
+    e = cudaMemsetAsync(p, 0, GQAW_NOALLOC_SCRATCH_BYTES, stream);
     if (e != cudaSuccess) {
       gqaw::set_error(cudaGetErrorString(e));
       return GQAW_ECUDA;

@@ -83,8 +83,10 @@ def test_workspace_bytes(lib):
     assert n >= 256 and n % 256 == 0
     assert lib.gqaw_workspace_bytes(_args(lib, head_size=96)) == 0
     assert "head_size 96" in lib.gqaw_last_error()
-    # forcing a single chunk needs only the status word
-    assert lib.gqaw_workspace_bytes(_args(lib, split_keys=4096)) == 256
+    # fewer, longer attention ranges need fewer partial-result slots
+    big = _args(lib, batch_size=64, local_window_size=40, total_sequence_length=5000)
+    assert lib.gqaw_workspace_bytes(_args(lib, batch_size=64, local_window_size=40, total_sequence_length=5000,
+                                          split_keys=100000)) < lib.gqaw_workspace_bytes(big)
 
 
 @pytest.mark.parametrize("over,status,msg", [
