@@ -16,7 +16,9 @@
 #include <cstring>
 #include <string>
 
-#include "gqaw_internal.cuh"
+#include <cudaTypedefs.h>
+
+#include "gqaw_tc.cuh"
 
 namespace gqaw {
 cudaError_t launch_attend_f32(const Params &p, int gb, int blocks, cudaStream_t stream);
@@ -24,6 +26,7 @@ cudaError_t launch_attend_bf16(const Params &p, int gb, int blocks, cudaStream_t
 int attend_tile_f32(int D);
 int attend_tile_bf16(int D);
 cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream);
+cudaError_t launch_mma(const Params &p, const TcArgs &ta, const TcMaps &maps, int grid, cudaStream_t stream);
 }  // namespace gqaw
 
 namespace {
@@ -33,6 +36,7 @@ std::atomic<unsigned long long> g_launches{0ull};
 
 // Most attention CTAs of a step: GB300's 152 SMs x 2 resident CTAs per SM.
 constexpr long long kMaxCtas = 152 * 2;
+constexpr long long kSms = 152;
 // Largest cache bytes one column-group job of the finish kernel moves.
 constexpr long long kCopyChainBytes = 64 * 1024;
 // Upper bound on the cache-update kernel's blocks (152 SMs x 2).
@@ -55,6 +59,9 @@ struct Launch {
   int esize, rowbytes, group, gb, headblocks, tile, tpu, ncg;
   long long units, ctas, ncopy;
   size_t off_list, off_tickets, off_partials, ws_bytes;
+  bool tc;                // multi-token step on the tensor-core kernel
+  gqaw::TcArgs ta;
+  long long tc_grid;
 };
 
 bool head_size_ok(int D) { return D == 8 || D == 16 || D == 32 || D == 64 || D == 128 || D == 256; }
@@ -135,6 +142,29 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   const long long jobs = (long long)a->batch_size * a->kv_num_heads * 2 * L->ncg;
   if (jobs > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many cache-update jobs");
   L->ncopy = std::min(jobs, kFinishBlocks);
+
+  // Multi-token steps with bf16 caches and head size 128 run on the tensor-core
+  // kernel when the query-head group tiles 128 rows exactly.
+  L->tc = a->dtype == GQAW_BF16 && a->head_size == 128 && a->sequence_length >= 2 && L->group <= 128 &&
+          128 % L->group == 0;
+  if (L->tc) {
+    L->ta.tokens_per_tile = 128 / L->group;
+    L->ta.rowtiles = (int)ceil_div(a->sequence_length, L->ta.tokens_per_tile);
+    const long long base = (long long)a->batch_size * a->kv_num_heads * L->ta.rowtiles;
+    // key tiles of one query tile: the window before it plus its own tokens
+    const long long nt = ceil_div(std::min<long long>(a->local_window_size, a->total_sequence_length), 128) +
+                         ceil_div(L->ta.tokens_per_tile, 128) + 1;
+    long long ns = 1;  // split keys only when the query tiles fill less than 3/4 of the SMs
+    if (base > 0 && base * 4 < kSms * 3) ns = std::max(1LL, std::min({kSms / base, nt / 4, 16LL}));
+    if (a->split_keys > 0) ns = std::max(1LL, std::min(16LL, ceil_div(nt * 128, a->split_keys)));
+    L->ta.nsplit = (int)ns;
+    L->tc_grid = base * ns;
+    if (L->tc_grid > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many attention blocks");
+    L->off_tickets = L->off_list + align256((size_t)a->batch_size * 4);
+    L->off_partials = L->off_tickets + align256((size_t)base * 4);
+    L->ws_bytes = L->off_partials;
+    if (ns > 1) L->ws_bytes += align256((size_t)L->tc_grid * 128 * gqaw::kTcPartialStride * 4);
+  }
   return GQAW_OK;
 }
 
@@ -261,7 +291,58 @@ gqaw_status cuda_fail(cudaError_t e, const char *what) {
   return fail(GQAW_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link-time libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// A bf16 tensor map with 128-byte swizzle; dims/box innermost first, strides in bytes.
+bool encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                const cuuint32_t *box) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+gqaw_status run_mma(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
+  gqaw::TcMaps maps;
+  const cuuint64_t D = 128, BS = (cuuint64_t)a->batch_size * a->sequence_length;
+  const cuuint64_t rows = (cuuint64_t)a->batch_size * a->kv_num_heads * a->capacity;
+  const cuuint64_t q_dims[3] = {D, (cuuint64_t)a->num_heads, BS};
+  const cuuint64_t q_str[2] = {D * 2, (cuuint64_t)a->num_heads * D * 2};
+  const cuuint32_t q_box[3] = {64, (cuuint32_t)L.group, (cuuint32_t)(128 / L.group)};
+  const cuuint64_t c_dims[2] = {D, rows};
+  const cuuint64_t c_str[1] = {D * 2};
+  const cuuint32_t c_box[2] = {64, 128};
+  const cuuint64_t n_dims[3] = {D, (cuuint64_t)a->kv_num_heads, BS};
+  const cuuint64_t n_str[2] = {D * 2, (cuuint64_t)a->kv_num_heads * D * 2};
+  const cuuint32_t n_box[3] = {64, 1, 128};
+  if (!encode_map(&maps.q, a->query, 3, q_dims, q_str, q_box) ||
+      !encode_map(&maps.kc, a->past_key, 2, c_dims, c_str, c_box) ||
+      !encode_map(&maps.vc, a->past_value, 2, c_dims, c_str, c_box) ||
+      !encode_map(&maps.kn, a->key, 3, n_dims, n_str, n_box) ||
+      !encode_map(&maps.vn, a->value, 3, n_dims, n_str, n_box))
+    return fail(GQAW_ECUDA, "cuTensorMapEncodeTiled failed for the multi-token kernel");
+  const cudaError_t e = gqaw::launch_mma(p, L.ta, maps, (int)L.tc_grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "multi-token kernel launch");
+  g_launches.fetch_add(1);
+  return GQAW_OK;
+}
+
 gqaw_status run_attend(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
+  if (L.tc) return run_mma(a, L, p, st);
   const cudaError_t e = a->dtype == GQAW_F32 ? gqaw::launch_attend_f32(p, L.gb, (int)L.ctas, st)
                                              : gqaw::launch_attend_bf16(p, L.gb, (int)L.ctas, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");

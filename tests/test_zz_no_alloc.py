@@ -85,10 +85,10 @@ def test_noalloc_rejects_steps_needing_more_scratch():
 
     sh = wl.SHAPES["longctx"]
     a = gqaw.gqaw_step_args()
-    # 4096 items x 512 tokens x 8 kv heads: one 4-byte ticket per attention unit is
-    # already 64 MiB of scratch
+    # fp32, 4096 items x 512 tokens x 8 kv heads: one 4-byte ticket per attention unit
+    # is already 64 MiB of scratch
     a.batch_size, a.sequence_length, a.num_heads, a.kv_num_heads = 4096, 512, sh.Nq, sh.Nkv
-    a.head_size, a.capacity, a.local_window_size, a.dtype = sh.D, sh.C, sh.W, gqaw.GQAW_BF16
+    a.head_size, a.capacity, a.local_window_size, a.dtype = sh.D, sh.C, sh.W, gqaw.GQAW_F32
     a.total_sequence_length = 40000
     assert gqaw.gqaw_workspace_bytes(a) > gqaw.GQAW_NOALLOC_SCRATCH_BYTES
     assert gqaw.gqa_windowed_step_noalloc(a, 0) == gqaw.GQAW_EWORKSPACE
