@@ -317,6 +317,8 @@ def run_gpu(args, rank, world):
     name = args.workload
     K, Wm = args.steps, args.warmup
     h = Harness(name, K, Wm, seed=11 + rank, split_keys=args.split_keys, batch=args.batch)
+    if args.no_graph:
+        h.spec["graph"] = False
     stream = h.stream
     torch.cuda.synchronize()
     torch.cuda.set_stream(stream)
@@ -612,6 +614,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="longctx-decode")
     ap.add_argument("--split-keys", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (profiling)")
+    ap.add_argument("--no-graph", action="store_true", help="launch every step from the host (no CUDA graph)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

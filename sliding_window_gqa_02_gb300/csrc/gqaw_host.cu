@@ -144,9 +144,9 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   L->ncopy = std::min(jobs, kFinishBlocks);
 
   // Multi-token steps with bf16 caches and head size 128 run on the tensor-core
-  // kernel when the query-head group tiles 128 rows exactly.
-  L->tc = a->dtype == GQAW_BF16 && a->head_size == 128 && a->sequence_length >= 2 && L->group <= 128 &&
-          128 % L->group == 0;
+  // kernel when the query-head group tiles a 32-row lane quarter exactly.
+  L->tc = a->dtype == GQAW_BF16 && a->head_size == 128 && a->sequence_length >= 2 && L->group <= 32 &&
+          32 % L->group == 0;
   if (L->tc) {
     L->ta.tokens_per_tile = 128 / L->group;
     L->ta.rowtiles = (int)ceil_div(a->sequence_length, L->ta.tokens_per_tile);
@@ -322,7 +322,7 @@ gqaw_status run_mma(const gqaw_step_args *a, const Launch &L, const gqaw::Params
   const cuuint64_t rows = (cuuint64_t)a->batch_size * a->kv_num_heads * a->capacity;
   const cuuint64_t q_dims[3] = {D, (cuuint64_t)a->num_heads, BS};
   const cuuint64_t q_str[2] = {D * 2, (cuuint64_t)a->num_heads * D * 2};
-  const cuuint32_t q_box[3] = {64, (cuuint32_t)L.group, (cuuint32_t)(128 / L.group)};
+  const cuuint32_t q_box[3] = {64, (cuuint32_t)L.group, (cuuint32_t)(32 / L.group)};
   const cuuint64_t c_dims[2] = {D, rows};
   const cuuint64_t c_str[1] = {D * 2};
   const cuuint32_t c_box[2] = {64, 128};

@@ -38,27 +38,35 @@ constexpr int kRows = 128;       // query rows per CTA (M)
 constexpr int kKeys = 128;       // keys per tile (N of Q.K^T, K of P.V)
 constexpr int kD = 128;          // head size
 constexpr int kHalf = 16384;     // bytes of a [128 rows][64 bf16] swizzled block
-constexpr int kStages = 2;
 constexpr int kThreads = 128;
-// shared memory: Q (2 halves), per stage K (2 halves) and V (2 halves), P (2 halves)
+// shared memory: Q, two K buffers, two V buffers, P -- each two 64-column halves
 constexpr int kSmemQ = 0;
-constexpr int kSmemStage0 = 2 * kHalf;
-constexpr int kStageBytes = 4 * kHalf;
-constexpr int kSmemP = kSmemStage0 + kStages * kStageBytes;
+constexpr int kSmemK = 2 * kHalf;
+constexpr int kSmemV = kSmemK + 4 * kHalf;
+constexpr int kSmemP = kSmemV + 4 * kHalf;
 constexpr int kSmemBars = kSmemP + 2 * kHalf;
 constexpr int kSmemTotal = kSmemBars + 256;
 constexpr int kSmemAlloc = kSmemTotal + 1024;  // room to align the base to 1024 bytes
-constexpr uint32_t kTmemCols = 256;            // S: columns [0,128); O: [128,256)
+constexpr uint32_t kTmemCols = 512;            // S: two buffers, columns [0,256); O: [256,384)
 constexpr float kRescaleLog2 = 8.0f;           // lazy rescale threshold (log2 units)
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kRows, kKeys, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kRows, kD, 0, 1);
 
-__device__ __forceinline__ float masked_logit(float acc, const Params &p, bool ok, const float *bias_row, long long j) {
-  float z = acc * p.qscale;
-  if (p.capmul != 0.f) z = p.capmul * tanhf(z);
-  if (bias_row) z += p.biasmul * bias_row[j];
-  return ok ? z : -INFINITY;
+// 2^x, approximate (ex2.approx, relative error ~2^-22; -inf gives +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh from its exponential form, tanh(x) = 1 - 2 / (e^(2x) + 1): absolute error about
+// 1e-7 (it saturates to +-1 correctly), which is what a logit cap multiplies.
+__device__ __forceinline__ float fast_tanh(float x) {
+  const float e = fast_exp2(2.8853900817779268f * fminf(fmaxf(x, -15.f), 15.f));  // 2 log2(e) x
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return fmaf(-2.f, r, 1.f);
 }
 
 }  // namespace
@@ -67,10 +75,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_attend_kernel(const Params p, const TcArgs ta, const __grid_constant__ TcMaps maps) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kSmemBars);  // [kStages]
-  uint64_t *bar_q = full + kStages;
-  uint64_t *bar_s = bar_q + 1;
-  uint64_t *bar_o = bar_s + 1;
+  uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + kSmemBars);  // [2]: K tile landed
+  uint64_t *vfull = kfull + 2;                                        // [2]: V tile landed
+  uint64_t *bar_q = vfull + 2;
+  uint64_t *bar_s = bar_q + 1;  // [2]: S = Q K^T done, per tensor-memory buffer
+  uint64_t *bar_o = bar_s + 2;  // O += P V done
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_o + 1);
   __shared__ int s_last, s_abort;
 
@@ -84,9 +93,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = x / p.Nkv;
 
   if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&full[st], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&bar_s[i], 1);
+    }
     mbar_init(bar_q, 1);
-    mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
     mbar_fence_init();
     s_abort = 0;
@@ -96,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + kKeys;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 2 * kKeys;
   pdl_wait();
   pdl_launch_dependents();
 
@@ -141,11 +153,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     flag(p, GQAW_DEV_BAD_SEQLEN);
   }
 
-  // this thread's query row
+  // This thread's query row.  The tile's tokens are spread evenly over the four TMEM
+  // lane quarters (one warp each), tpq tokens per quarter, so a short step (S x g < 128
+  // rows) still gives every warp real rows.
   const int r = tid;
-  const int tok = s0 + r / g;
+  const int tpq = (s_end - s0 + 3) / 4;
+  const int tl = (r % 32) / g;  // token within the quarter
+  const int tok = s0 + (r / 32) * tpq + tl;
   const int hh = r % g;
-  const bool row_ok = ok && tok < s_end;
+  const bool row_ok = ok && tl < tpq && tok < s_end;
   const long long qi = P + tok;  // absolute position of the row's token
   const long long rlo = qi - p.W + 1 > 0 ? qi - p.W + 1 : 0;
   const int h = kvh * g + hh;
@@ -155,35 +171,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint64_t pol = 0;
   const int row0_cache = (int)(((long long)b * p.Nkv + kvh) * p.C);
-  // Thread 0: load key tile t of the list into stage st.
-  auto load_tile = [&](int t, int st) {
-    unsigned char *kb = smem + kSmemStage0 + st * kStageBytes;
-    unsigned char *vb = kb + 2 * kHalf;
-    mbar_arrive_expect_tx(&full[st], 4 * kHalf);
+  // Thread 0: load the K (or V) half-tiles of key tile t into buffer `dst`.
+  auto load_kv = [&](int t, unsigned char *dst, uint64_t *bar, bool value) {
+    mbar_arrive_expect_tx(bar, 2 * kHalf);
     if (t < nc) {
+      const CUtensorMap *m = value ? &maps.vc : &maps.kc;
       const int row = row0_cache + (int)(klo + (long long)t * kKeys - P + pl.Lp);
-      tc::tma_load_2d(kb, &maps.kc, 0, row, &full[st], pol);
-      tc::tma_load_2d(kb + kHalf, &maps.kc, 64, row, &full[st], pol);
-      tc::tma_load_2d(vb, &maps.vc, 0, row, &full[st], pol);
-      tc::tma_load_2d(vb + kHalf, &maps.vc, 64, row, &full[st], pol);
+      tc::tma_load_2d(dst, m, 0, row, bar, pol);
+      tc::tma_load_2d(dst + kHalf, m, 64, row, bar, pol);
     } else {
+      const CUtensorMap *m = value ? &maps.vn : &maps.kn;
       const int tokrow = b * p.S + (t - nc) * kKeys;
-      tc::tma_load_3d(kb, &maps.kn, 0, kvh, tokrow, &full[st], pol);
-      tc::tma_load_3d(kb + kHalf, &maps.kn, 64, kvh, tokrow, &full[st], pol);
-      tc::tma_load_3d(vb, &maps.vn, 0, kvh, tokrow, &full[st], pol);
-      tc::tma_load_3d(vb + kHalf, &maps.vn, 64, kvh, tokrow, &full[st], pol);
+      tc::tma_load_3d(dst, m, 0, kvh, tokrow, bar, pol);
+      tc::tma_load_3d(dst + kHalf, m, 64, kvh, tokrow, bar, pol);
     }
   };
-  if (tid == 0 && t_begin < t_end) {
+  auto kbuf = [&](int k) { return smem + kSmemK + (k % 2) * 2 * kHalf; };
+  auto vbuf = [&](int k) { return smem + kSmemV + (k % 2) * 2 * kHalf; };
+  const int ntl = t_end - t_begin;  // key tiles of this CTA
+  // S = Q K^T of local tile k into tensor-memory buffer k % 2 (thread 0).
+  auto issue_qk = [&](int k) {
+    if (!mbar_wait(&kfull[k % 2], (k / 2) & 1)) flag(p, GQAW_DEV_TIMEOUT);
+    tc::fence_after_sync();
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      const int half = kk / 4, off = (kk % 4) * 32;
+      const uint64_t a = tc::smem_desc_sw128(smem + kSmemQ + half * kHalf + off, 16, 1024);
+      const uint64_t bd = tc::smem_desc_sw128(kbuf(k) + half * kHalf + off, 16, 1024);
+      tc::mma_bf16_ss(tmem_s + (k % 2) * kKeys, a, bd, kIdescQK, kk > 0);
+    }
+    tc::mma_commit(&bar_s[k % 2]);
+  };
+  if (tid == 0 && ntl > 0) {
     pol = policy_evict_first();
     mbar_arrive_expect_tx(bar_q, 2 * kHalf);
-    const int qtok = b * p.S + s0;
-    tc::tma_load_3d(smem + kSmemQ, &maps.q, 0, kvh * g, qtok, bar_q, tc::policy_evict_last());
-    tc::tma_load_3d(smem + kSmemQ + kHalf, &maps.q, 64, kvh * g, qtok, bar_q, tc::policy_evict_last());
-    for (int t = t_begin; t < t_end && t < t_begin + kStages; ++t) load_tile(t, (t - t_begin) % kStages);
+    for (int q = 0; q < 4; ++q) {  // quarter q: tokens s0 + q * tpq ..., rows [32q, 32q + 32)
+      const int qtok = b * p.S + s0 + q * tpq;
+      tc::tma_load_3d(smem + kSmemQ + q * 4096, &maps.q, 0, kvh * g, qtok, bar_q, tc::policy_evict_last());
+      tc::tma_load_3d(smem + kSmemQ + kHalf + q * 4096, &maps.q, 64, kvh * g, qtok, bar_q,
+                      tc::policy_evict_last());
+    }
+    for (int k = 0; k < 2 && k < ntl; ++k) {
+      load_kv(t_begin + k, kbuf(k), &kfull[k % 2], false);
+      load_kv(t_begin + k, vbuf(k), &vfull[k % 2], true);
+    }
+    if (!mbar_wait(bar_q, 0)) flag(p, GQAW_DEV_TIMEOUT);
+    issue_qk(0);
   }
 
   float m_run = -INFINITY, l_run = 0.f;
+  const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
   // A bounded wait that expires sets s_abort; every thread reads it after the tile's
   // barrier, so the whole CTA leaves the loop together.
   auto bail = [&]() {
@@ -191,60 +228,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 1;
   };
   int done_tiles = 0;
-  for (int t = t_begin; t < t_end; ++t) {
-    const int k = t - t_begin;  // local tile counter
-    const int st = k % kStages;
+  for (int k = 0; k < ntl; ++k) {
+    const int t = t_begin + k;
     const long long j0 = t < nc ? klo + (long long)t * kKeys : P + (long long)(t - nc) * kKeys;
     const long long jhi_src = t < nc ? P : P + s_end;  // keys of this source
     const int nvalid = (int)(jhi_src - j0 < kKeys ? jhi_src - j0 : kKeys);
-    unsigned char *kb = smem + kSmemStage0 + st * kStageBytes;
-    unsigned char *vb = kb + 2 * kHalf;
-
-    // ---- S = Q K^T
-    if (tid == 0) {
-      if (k == 0 && !mbar_wait(bar_q, 0)) bail();
-      if (!mbar_wait(&full[st], (k / kStages) & 1)) bail();
-      tc::fence_after_sync();
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const int half = kk / 4, off = (kk % 4) * 32;
-        const uint64_t a = tc::smem_desc_sw128(smem + kSmemQ + half * kHalf + off, 16, 1024);
-        const uint64_t bd = tc::smem_desc_sw128(kb + half * kHalf + off, 16, 1024);
-        tc::mma_bf16_ss(tmem_s, a, bd, kIdescQK, kk > 0);
-      }
-      tc::mma_commit(bar_s);
+    // visible columns of this row in this tile: [c_lo, c_hi)
+    int c_lo = 0, c_hi = 0;
+    if (row_ok) {
+      const long long lo = rlo - j0, hi = qi - j0 + 1;
+      c_lo = (int)(lo < 0 ? 0 : (lo > kKeys ? kKeys : lo));
+      c_hi = (int)(hi < 0 ? 0 : (hi > nvalid ? nvalid : hi));
     }
-    if (!mbar_wait(bar_s, k & 1)) bail();
+
+    // ---- tensor core: S of the next tile while this one is in softmax
+    if (tid == 0 && k + 1 < ntl) issue_qk(k + 1);
+    if (!mbar_wait(&bar_s[k % 2], (k / 2) & 1)) bail();
     tc::fence_after_sync();
+    // K buffer k % 2 is free again (Q.K^T of tile k is done): fetch K of tile k + 2
+    if (tid == 0 && k + 2 < ntl) load_kv(t + 2, kbuf(k), &kfull[k % 2], false);
 
-    // ---- logits of this row
+    // ---- logits of this row (log2 units), row maximum
     float z[kKeys];
+    const uint32_t ts = tmem_s + (k % 2) * kKeys + ((uint32_t)(warp * 32) << 16);
+    float mt = -INFINITY;
+    if (plain) {
 #pragma unroll
-    for (int c32 = 0; c32 < kKeys / 32; ++c32) {
-      float v[32];
-      tc::tmem_ld32(tmem_s + ((uint32_t)(warp * 32) << 16) + c32 * 32, v);
+      for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+        float v[32];
+        tc::tmem_ld32(ts + c32 * 32, v);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int col = c32 * 32 + c;
-        const long long j = j0 + col;
-        const bool vis = row_ok && col < nvalid && j >= rlo && j <= qi;
-        z[col] = masked_logit(v[c], p, vis, vis ? bias_row : nullptr, j);
+        for (int c = 0; c < 32; ++c) {
+          const int col = c32 * 32 + c;
+          z[col] = (col >= c_lo && col < c_hi) ? v[c] : -INFINITY;
+          mt = fmaxf(mt, z[col]);
+        }
+      }
+      mt *= p.qscale;  // qscale > 0: max commutes with the scale
+    } else {
+      const float *brow = bias_row ? bias_row + j0 : nullptr;  // this tile's bias columns
+#pragma unroll
+      for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+        float v[32];
+        tc::tmem_ld32(ts + c32 * 32, v);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int col = c32 * 32 + c;
+          const bool vis = col >= c_lo && col < c_hi;
+          float x = v[c] * p.qscale;
+          if (p.capmul != 0.f) x = p.capmul * fast_tanh(x);
+          if (vis && brow) x = fmaf(p.biasmul, brow[col], x);
+          z[col] = vis ? x : -INFINITY;
+          mt = fmaxf(mt, z[col]);
+        }
       }
     }
-    float mt = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kKeys; ++c) mt = fmaxf(mt, z[c]);
 
-    // ---- the previous P.V has finished: P buffer and O are ours again
+    // ---- the previous P.V has finished: P buffer, V buffer (k-1) % 2 and O are free
     if (k > 0 && !mbar_wait(bar_o, (k - 1) & 1)) bail();
-    if (tid == 0 && t + 1 < t_end && k + 1 >= kStages) load_tile(t + 1, (k + 1) % kStages);
+    if (tid == 0 && k >= 1 && k + 1 < ntl) load_kv(t + 1, vbuf(k + 1), &vfull[(k + 1) % 2], true);
     tc::fence_after_sync();
 
     // lazy rescale: the reference max moves only when exceeded by more than 2^8
     const bool need = mt > m_run + kRescaleLog2;
     float alpha = 1.f;
     if (need) {
-      alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - mt);
+      alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mt);
       m_run = mt;
       l_run *= alpha;
     }
@@ -261,12 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- P (bf16) into shared memory, K-major with 128-byte swizzle
     const float base = m_run == -INFINITY ? 0.f : m_run;
+    const float zs = plain ? p.qscale : 1.f;  // plain logits are still unscaled
 #pragma unroll
     for (int q = 0; q < kKeys / 8; ++q) {
       float pv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        pv[e] = exp2f(z[q * 8 + e] - base);
+        pv[e] = fast_exp2(fmaf(z[q * 8 + e], zs, -base));
         l_run += pv[e];
       }
       uint4 w;
@@ -278,8 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4 *>(smem + kSmemP + half * kHalf + r * 128 + ((chunk ^ (r & 7)) * 16)) = w;
     }
     // keys past this source's range: their V rows must be finite (0 * NaN is NaN)
+    unsigned char *vb = vbuf(k);
     if (nvalid < kKeys) {
-      if (!mbar_wait(&full[st], (k / kStages) & 1)) bail();
+      if (!mbar_wait(&vfull[k % 2], (k / 2) & 1)) bail();
       for (int e = tid; e < (kKeys - nvalid) * 16; e += kThreads) {
         const int row = nvalid + e / 16, part = e % 16;  // 16 chunks of 16 B per key (two halves)
         *reinterpret_cast<uint4 *>(vb + (part / 8) * kHalf + row * 128 + (part % 8) * 16) = make_uint4(0, 0, 0, 0);
@@ -291,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- O += P V
     if (tid == 0) {
+      if (!mbar_wait(&vfull[k % 2], (k / 2) & 1)) bail();
       tc::fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < kKeys / 16; ++kk) {
@@ -305,8 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ++done_tiles;
     if (s_abort) break;  // uniform: read by all threads after the barrier above
   }
-  const int ntl = done_tiles;
-  if (ntl > 0 && !mbar_wait(bar_o, (ntl - 1) & 1)) flag(p, GQAW_DEV_TIMEOUT);
+  if (done_tiles > 0 && !mbar_wait(bar_o, (done_tiles - 1) & 1)) flag(p, GQAW_DEV_TIMEOUT);
+  // an S = Q K^T issued ahead for a tile the loop did not reach must land before exit
+  if (tid == 0 && done_tiles < ntl && done_tiles + 1 <= ntl)
+    mbar_wait(&bar_s[done_tiles % 2], (done_tiles / 2) & 1);
   tc::fence_after_sync();
 
   // ---- epilogue: this CTA's (O, m, l) for its row
