@@ -413,3 +413,44 @@ def test_multi_token_equals_single_tokens_gpu():
         n = int(ra["resident_len"][i])
         assert np.array_equal(ra["present_key"][i, :, :n], rb["present_key"][i, :, :n])
         assert np.array_equal(ra["present_value"][i, :, :n], rb["present_value"][i, :, :n])
+
+
+# ------------------------------------------------------------------ tensor-core path shapes
+
+
+@pytest.mark.parametrize("heads", [(1, 1), (2, 1), (8, 1), (16, 2), (32, 1), (32, 8)])
+@pytest.mark.parametrize("S", [2, 3, 9, 33, 130])
+def test_tensor_core_path_shapes(heads, S):
+    """Multi-token bf16 steps with head size 128 run on the tcgen05 kernel for every
+    query-head group that tiles a 32-row lane quarter (1, 2, 4, 8, 16, 32); token counts
+    leave lane quarters partly filled and cross 128-row query tiles; W=100 puts window
+    edges inside key tiles; a ragged batch, one item starting from an empty cache."""
+    Nq, Nkv = heads
+    if Nq // Nkv >= 16 and S > 33:
+        S = 33  # keep the oracle's work bounded
+    B, C, W = 2, 110, 100
+    sh = wl.Shape("tc", B=B, Nq=Nq, Nkv=Nkv, D=128, W=W, C=C, dtype=wl.BF16)
+    pk, pv = wl.cache(sh, 15)
+    p = _shape_pair(sh, past_key=pk, past_value=pv)
+    T = np.array([0, 77], np.int64)
+    for t in range(2):
+        q, k, v = wl.step_inputs(sh, S, 1500 + 10 * S + t)
+        p.step(q, k, v, T + S - 1)
+        T = T + S
+
+
+@pytest.mark.parametrize("split_keys", [128, 512])
+@pytest.mark.parametrize("inplace", [True, False])
+def test_tensor_core_path_splits_and_buffers(split_keys, inplace):
+    """Forced key splits (merged by the last contributor) and a separate present
+    buffer on the tensor-core kernel, with softcap and a bias."""
+    sh = wl.Shape("tcs", B=3, Nq=16, Nkv=4, D=128, W=300, C=311, dtype=wl.BF16, softcap=20.0)
+    pk, pv = wl.cache(sh, 16)
+    p = _shape_pair(sh, past_key=pk, past_value=pv, inplace=inplace, split_keys=split_keys)
+    T = np.array([5, 290, 600], np.int64)
+    for t, S in enumerate([12, 12, 40]):
+        q, k, v = wl.step_inputs(sh, S, 1600 + t)
+        total = int(T.max()) + S
+        bias = wl.bias(sh.B, sh.Nq, S, total, 1600 + t, std=1.0)
+        p.step(q, k, v, T + S - 1, total=total, bias=bias)
+        T = T + S
