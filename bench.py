@@ -59,6 +59,17 @@ def workload_spec(name):
     raise SystemExit("unknown workload " + name)
 
 
+def workload_config(name, B=None):
+    """The `config` object of the JSON line (shared by the GPU and reference arms).
+    The step computes in fp32 (accumulation) over caches of `cache_dtype`."""
+    spec = workload_spec(name)
+    sh = spec["shape"]
+    return {"workload": name, "B": B if B else spec.get("B", sh.B), "S": spec["S"], "num_heads": sh.Nq,
+            "kv_num_heads": sh.Nkv, "head_size": sh.D, "local_window_size": sh.W, "capacity": sh.C,
+            "cache_dtype": sh.dtype, "softcap": sh.softcap, "bias": spec["bias"],
+            "contexts": "U[%d,%d]" % (spec["lo"], spec["hi"])}
+
+
 def resident_len(T, C, W):
     """L(T) through the C ABI (host function of the library)."""
     from sliding_window_gqa_02_gb300 import gqaw
@@ -396,14 +407,12 @@ def run_gpu(args, rank, world):
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": sh.dtype, "data": "synthetic",
-        "config": {"workload": name, "B": B, "S": S, "num_heads": sh.Nq, "kv_num_heads": sh.Nkv,
-                   "head_size": sh.D, "local_window_size": sh.W, "capacity": sh.C, "softcap": sh.softcap,
-                   "contexts": "U[%d,%d]" % (h.spec["lo"], h.spec["hi"]),
-                   "l2": "no flush: K/V window per step %.0f MB > 129 MB L2" % (step_bytes / K / 1e6)
-                   if step_bytes / K > 129e6 else "CUDA-graph replay, working set L2-resident",
-                   "launch": "CUDA graph of K steps" if h.spec["graph"] else "stream launches",
-                   "parallelism": "replicas x%d" % world},
+        "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(name, B),
+                       l2="no flush: K/V window per step %.0f MB > 129 MB L2" % (step_bytes / K / 1e6)
+                       if step_bytes / K > 129e6 else "CUDA-graph replay, working set L2-resident",
+                       launch="CUDA graph of K steps" if h.spec["graph"] else "stream launches",
+                       parallelism="replicas x%d" % world),
         "gpu_launches": launches,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
@@ -498,6 +507,9 @@ def extra_workloads(main, args):
 # ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
 
 
+_ORACLE_INPUTS = {}
+
+
 def oracle_item_step(name, seed, b_items, t_index=0):
     """Run the oracle on items ``b_items`` of one step of ``name``; returns seconds."""
     import oracle
@@ -508,13 +520,19 @@ def oracle_item_step(name, seed, b_items, t_index=0):
     B = spec.get("B", sh.B)
     S = spec["S"]
     T0 = wl.lengths(B, spec["lo"], spec["hi"], seed) + t_index * S
-    q, k, v = wl.step_inputs(sh, S, seed * 100 + (t_index % 4), B=B)
-    nq, nk, nv = wl.to_numpy(q), wl.to_numpy(k), wl.to_numpy(v)
+    key = ("inputs", name, seed, t_index % 4)
+    if key not in _ORACLE_INPUTS:
+        q, k, v = wl.step_inputs(sh, S, seed * 100 + (t_index % 4), B=B)
+        _ORACLE_INPUTS[key] = (wl.to_numpy(q), wl.to_numpy(k), wl.to_numpy(v))
+    nq, nk, nv = _ORACLE_INPUTS[key]
     odt = oracle.F32 if sh.dtype == wl.F32 else oracle.BF16
     el = 0.0
     for b in b_items:
-        pk, pv = wl.cache(sh, seed * 7919 + b, B=1)
-        npk, npv = wl.to_numpy(pk), wl.to_numpy(pv)
+        ckey = ("cache", name, seed, b % 8)  # eight distinct caches serve every item: timing only
+        if ckey not in _ORACLE_INPUTS:
+            pk, pv = wl.cache(sh, seed * 7919 + b % 8, B=1)
+            _ORACLE_INPUTS[ckey] = (wl.to_numpy(pk), wl.to_numpy(pv))
+        npk, npv = _ORACLE_INPUTS[ckey]
         seq = (T0[b:b + 1] + S - 1).astype(np.int32)
         total = int(seq.max()) + 1
         bias = None
@@ -533,14 +551,13 @@ def cpu_baseline(name, budget_s=15.0):
     spec = workload_spec(name)
     B = spec.get("B", spec["shape"].B)
     S = spec["S"]
-    done, el, b = 0, 0.0, 0
-    while el < budget_s and done < B:
-        el += oracle_item_step(name, 11, [b])
+    done, el = 0, 0.0
+    while el < budget_s and done < 64 * B:  # item after item, step after step
+        el += oracle_item_step(name, 11, [done % B], done // B)
         done += 1
-        b += 1
     return {"value": done * S / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d items of one %s step (%d token(s) each), fp64 C oracle, 1 thread, %.1f s"
-                      % (done, B, name, S, el)}
+            "sample": "%d item-steps of %s (%d items per step, %d token(s) each), fp64 C oracle, 1 thread, %.1f s"
+                      % (done, name, B, S, el)}
 
 
 def run_reference(args):
@@ -562,7 +579,7 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": K,
             "warmup": Wm, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "B": B, "S": S},
+            "config": workload_config(args.workload, B),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -608,7 +625,7 @@ def _max_over_ranks(x, world):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gqaw", choices=["gqaw", "reference"])
     ap.add_argument("--workload", default="longctx-decode")
