@@ -200,6 +200,16 @@ def profiled_traffic(workload):
     return float(m.group(1))
 
 
+def bf16_peak_tflops():
+    """Dense bf16 tensor peak: the burst cuBLAS figure of MEASURED_PEAKS.json, else the
+    fallback of 1900 TFLOP/s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -487,8 +497,12 @@ def extra_workloads(main, args):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / K
         _, sb = algorithmic_bytes(h.sh, h.S, h.T[Wm], h.B)
+        if h.bias is not None:
+            sb += 4 * h.sh.Nq * visible_columns(h.S, h.T[Wm], h.sh.W)
+        hbm, _ = measured_peaks()
         entry = {"ms_per_step": ms, "tokens_per_s": h.B * h.S / (ms / 1e3),
-                 "step_gbs": sb / (ms / 1e3) / 1e9, "B": h.B, "S": h.S, "dtype": h.sh.dtype,
+                 "step_gbs": sb / (ms / 1e3) / 1e9, "hbm_frac": sb / (ms / 1e3) / 1e9 / hbm,
+                 "B": h.B, "S": h.S, "cache_dtype": h.sh.dtype,
                  "launch": "CUDA graph" if h.spec["graph"] else "stream"}
         if h.S > 1:
             flops = 0
@@ -496,6 +510,8 @@ def extra_workloads(main, args):
                 for s in range(h.S):
                     flops += h.sh.Nq * 4 * h.sh.D * min(int(P) + s + 1, h.sh.W)
             entry["tflops"] = flops / (ms / 1e3) / 1e12
+            entry["tensor_frac"] = entry["tflops"] / bf16_peak_tflops()
+            entry["kernel"] = "mma_attend_kernel (tcgen05)" if h.sh.dtype == "bf16" and h.sh.D == 128 else "attend_kernel"
         out[name] = entry
         torch.cuda.synchronize()
         torch.cuda.set_stream(torch.cuda.default_stream())
