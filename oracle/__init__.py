@@ -70,6 +70,8 @@ class _Args(ctypes.Structure):
         ("resident_len", ctypes.c_void_p),
         ("s_begin", ctypes.c_int64),
         ("s_end", ctypes.c_int64),
+        ("head_sink", ctypes.c_void_p),
+        ("smooth_softmax", ctypes.c_int64),
     ]
 
 
@@ -124,7 +126,7 @@ def _elem_dtype(dtype: int):
 
 def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_length,
          num_heads, kv_num_heads, local_window_size, scale=0.0, softcap=0.0,
-         attention_bias=None, bias_strides=None, dtype=F32, rows=None):
+         attention_bias=None, bias_strides=None, dtype=F32, rows=None, head_sink=None, smooth_softmax=0):
     """One windowed GQA step on host arrays.
 
     Arrays are numpy: float32 for ``dtype=F32``; uint16 bfloat16 bit patterns for
@@ -138,7 +140,8 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
     The present arrays start as copies of the past arrays; rows [0, L) are written.
     ``scale == 0`` selects 1/sqrt(head_size).  ``rows=(s0, s1)`` evaluates the attention
     only for new tokens s0 <= s < s1 (other output rows stay zero); ``rows=(0, 0)``
-    gives the cache layout alone.
+    gives the cache layout alone.  ``head_sink`` (float32 (Nq,)) adds a sink logit per
+    head to the softmax denominator; ``smooth_softmax`` adds a sink of 0 to every head.
     """
     lib = _load()
     et = _elem_dtype(dtype)
@@ -148,6 +151,10 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
     past_key = np.ascontiguousarray(past_key, dtype=et)
     past_value = np.ascontiguousarray(past_value, dtype=et)
     seqlens_k = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    if head_sink is not None:
+        head_sink = np.ascontiguousarray(head_sink, dtype=np.float32)
+        if head_sink.shape != (num_heads,):
+            raise ValueError("oracle.step: head_sink must be (num_heads,)")
     B, Nkv, C, D = past_key.shape
     S = query.shape[1]
     if query.shape != (B, S, num_heads * D) or key.shape != (B, S, kv_num_heads * D):
@@ -184,6 +191,7 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
         resident_len=_ptr(resident),
         s_begin=0 if rows is None else int(rows[0]),
         s_end=S if rows is None else int(rows[1]),
+        head_sink=_ptr(head_sink), smooth_softmax=int(bool(smooth_softmax)),
     )
     rc = lib.oracle_step(ctypes.byref(a))
     if rc != 0:

@@ -30,7 +30,11 @@
  *  - multi-token steps with batch > 1 are allowed; every item uses the same S and
  *    its own P_b = T_b - S; P_b < 0 is an error;
  *  - the output is rounded once, from fp64, to the cache dtype (round to nearest
- *    even).
+ *    even);
+ *  - head_sink / smooth_softmax ([P3] Part 1.1 input 11 and Part 1.3, named only):
+ *    a sink is one more logit per head that joins the softmax denominator and has no
+ *    value row; it is taken as given (not scaled, capped or biased); smooth_softmax is
+ *    a sink of 0 for every head; head_sink wins when both are given.
  *
  * Precision: every input element is widened exactly to double; dot products,
  * softcap, softmax and the weighted sum are evaluated in double in ascending key
@@ -79,6 +83,8 @@ typedef struct oracle_args {
   int64_t s_begin, s_end;    /* attention is evaluated for new tokens s in [s_begin, s_end)
                                 only (outputs of other rows are left as they are); the
                                 present rows are always written */
+  const float *head_sink;    /* NULL or (Nq,): a sink logit per query head */
+  int64_t smooth_softmax;    /* non-zero: a sink logit of 0 for every head (if no head_sink) */
 } oracle_args;
 
 /* [P1] Description, resident-count formula:
@@ -194,6 +200,12 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc) {
                                           s * a->bias_stride_s + j];
         z[j - jlo] = zj;
         if (zj > zmax) zmax = zj;
+      }
+      /* the sink logit, if any, joins the maximum and the denominator */
+      if (a->head_sink || a->smooth_softmax) {
+        const double sink = a->head_sink ? (double)a->head_sink[h] : 0.0;
+        if (sink > zmax) zmax = sink;
+        denom += exp(sink - zmax);
       }
       for (d = 0; d < D; ++d) acc[d] = 0.0;
       for (j = jlo; j <= i; ++j) {

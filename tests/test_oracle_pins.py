@@ -451,3 +451,48 @@ def test_round_bf16_matches_torch_on_float_inputs():
     assert np.array_equal(got, ref)
     assert oracle.round_bf16(1.0 + 2**-8) == 0x3F80  # tie -> even (1.0)
     assert oracle.round_bf16(1.0 + 2**-8 + 2**-30) == 0x3F81  # above the tie: one fp64 rounding
+
+
+# ---------------------------------------------------------------- sinks
+
+
+def test_sink_closed_forms():
+    """head_sink / smooth_softmax (mobius issue #111, Part 1.1 input 11 and Part 1.3,
+    named only; reading: one more logit per head in the softmax denominator, with no
+    value row).  With Q = 0 every visible logit is 0, so each of the n visible keys gets
+    weight 1 / (e^sink + n) and the output is the mean of the visible values times
+    n / (e^sink + n); smooth_softmax is a sink of 0; a sink of -inf is no sink."""
+    D, Nq, Nkv, C, W = 8, 3, 1, 9, 5
+    sinks = np.array([0.7, -2.0, 3.0], np.float32)
+    for smooth in (False, True):
+        oc_ref = OracleCache(1, Nq, Nkv, D, C, W)
+        T = 0
+        for step, S in enumerate([4, 1, 3, 1]):
+            pos = np.arange(T, T + S, dtype=np.float32)
+            v = np.repeat(pos[:, None], D, axis=1)[None] + 1.0
+            k = _u(_rng(40 + step), (1, S, D))
+            q = np.zeros((1, S, Nq * D), np.float32)
+            r = oracle.step(q, k, v, oc_ref.pk, oc_ref.pv, np.array([T + S - 1], np.int32), T + S, Nq, Nkv, W,
+                            head_sink=None if smooth else sinks, smooth_softmax=smooth)
+            oc_ref.step(q, k, v, [T + S - 1])
+            for s in range(S):
+                i = T + s
+                lo = max(0, i - W + 1)
+                n = i - lo + 1
+                mean = (lo + i) / 2.0 + 1.0
+                for h in range(Nq):
+                    e_s = 1.0 if smooth else math.exp(float(sinks[h]))
+                    np.testing.assert_allclose(r["output_f64"][0, s, h * D:(h + 1) * D], mean * n / (e_s + n),
+                                               rtol=1e-13, atol=0)
+            T += S
+    rng = _rng(41)
+    q, k, v = _u(rng, (1, 4, Nq * D)), _u(rng, (1, 4, D)), _u(rng, (1, 4, D))
+    pk = np.zeros((1, 1, C, D), np.float32)
+    plain = oracle.step(q, k, v, pk, pk, np.array([3], np.int32), 4, Nq, Nkv, W)
+    none = oracle.step(q, k, v, pk, pk, np.array([3], np.int32), 4, Nq, Nkv, W,
+                       head_sink=np.full(Nq, -np.inf, np.float32))
+    zero = oracle.step(q, k, v, pk, pk, np.array([3], np.int32), 4, Nq, Nkv, W, head_sink=np.zeros(Nq, np.float32))
+    smooth = oracle.step(q, k, v, pk, pk, np.array([3], np.int32), 4, Nq, Nkv, W, smooth_softmax=True)
+    assert np.array_equal(plain["output_f64"], none["output_f64"])
+    assert np.array_equal(zero["output_f64"], smooth["output_f64"])
+    assert not np.array_equal(plain["output_f64"], smooth["output_f64"])
