@@ -22,7 +22,8 @@
  *  [P3] onnxruntime/mobius issue #111 "GQA In-Place KV Cache: Investigation Report",
  *       Part 1.1 (inputs and outputs, BNSH caches), 1.2 (past and present may be one
  *       buffer), 1.3 (num_heads, kv_num_heads, scale = 1/sqrt(head_dim) by default,
- *       local_window_size, softcap with 0 = disabled).
+ *       local_window_size, softcap with 0 = disabled, smooth_softmax), and the
+ *       optional head_sink input of Part 1.1.
  *  [P4] onnxruntime PR #34226 "Fix CPU Attention causal mask for q_len=1 with past_key
  *       and kv_len > 1", Description: key j is visible to query i iff
  *       j <= i + past_sequence_length.
@@ -33,8 +34,10 @@
  *     keys j with i - W < j <= i (causal rule of [P4] plus the local window of W keys
  *     including itself); query head h reads kv head h / (num_heads / kv_num_heads);
  *     logit z_j = scale * q.k_j, then softcap * tanh(z_j / softcap) if softcap > 0,
- *     then + attention_bias[b, h, s, j]; softmax over the visible keys; output is the
- *     weighted sum of the values, rounded to the cache dtype;
+ *     then + attention_bias[b, h, s, j]; softmax over the visible keys, its
+ *     denominator joined by exp(head_sink[h]) (or exp(0) with smooth_softmax) when a
+ *     sink is given; output is the weighted sum of the values, rounded to the cache
+ *     dtype;
  *   - present rows [0, Lt) receive the Lt most recent positions of the past rows
  *     [0, Lp) followed by the S new rows (bit copies).
  *
@@ -80,8 +83,8 @@ typedef enum gqaw_dtype {
 
 /* Arguments of one step.  All tensor pointers are DEVICE pointers.  Layouts are
  * row-major with the shapes given; "BNSH" is (batch, kv head, row, head_size).
- * Alignment: every tensor pointer except seqlens_k and attention_bias must be 16-byte
- * aligned; seqlens_k and attention_bias 4-byte aligned; workspace 256-byte aligned. */
+ * Alignment: every tensor pointer except seqlens_k, attention_bias and head_sink must be
+ * 16-byte aligned; those three 4-byte aligned; workspace 256-byte aligned. */
 typedef struct gqaw_step_args {
   int32_t batch_size;            /* B >= 0; B == 0 is a valid empty step */
   int32_t sequence_length;       /* S >= 1 new tokens per item (same S for every item) */
@@ -119,6 +122,10 @@ typedef struct gqaw_step_args {
                                     share a workspace must not overlap on the GPU. */
   size_t workspace_bytes;
   int32_t *resident_len_out;     /* NULL, or (B,) int32 receiving L(T_b) */
+  const float *head_sink;        /* NULL, or (Nq,) fp32: one sink logit per query head
+                                    ([P3] Part 1.1, input 11); 4-byte aligned */
+  int32_t smooth_softmax;        /* non-zero: a sink logit of 0 for every head ([P3]
+                                    Part 1.3); ignored when head_sink is given */
 } gqaw_step_args;
 
 /* L(T) of [P1] in 64-bit arithmetic.  Pure host function.  Returns -1 if T < 0,

@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
         A = fmaf(f, row[d], A);
       }
       if (cf == cl) {
-        out[(orow0 + h) * D + d] = Elem<T>::store(A / L);
+        out[(orow0 + h) * D + d] = Elem<T>::store(sink_divide(A, L, base, sink_log2(p, hq0 + h)));
       } else {
         float *part = p.partials + ((cta * 2 + slot) * GB + h) * (D + 2);
         part[d] = A;
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
             L = fmaf(f, __ldcg(part + D + 1), L);
             A = fmaf(f, __ldcg(part + d), A);
           }
-          out[(orow0 + h) * D + d] = Elem<T>::store(A / L);
+          out[(orow0 + h) * D + d] = Elem<T>::store(sink_divide(A, L, base, sink_log2(p, hq0 + h)));
         }
         if (threadIdx.x == 0) p.tickets[u] = 0u;  // ready for the next step
       }

@@ -196,6 +196,7 @@ gqaw_status check_pointers(const gqaw_step_args *a, const Launch &L) {
     if (a->bias_stride_b < 0 || a->bias_stride_h < 0 || a->bias_stride_s < 0)
       return fail(GQAW_EINVAL, "attention_bias strides must be >= 0");
   }
+  if (a->head_sink && !aligned(a->head_sink, 4)) return fail(GQAW_EINVAL, "head_sink is not 4-byte aligned");
   if (!a->workspace) return fail(GQAW_EWORKSPACE, "workspace is NULL");
   if (!aligned(a->workspace, 256)) return fail(GQAW_EWORKSPACE, "workspace is not 256-byte aligned");
   if (a->workspace_bytes < L.ws_bytes)
@@ -275,6 +276,8 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
   p->biasmul = gqaw::kLog2e;
   p->ncg = L.ncg;
   p->rowbytes = L.rowbytes;
+  p->sink = a->head_sink;
+  p->sink_mode = a->head_sink ? 1 : (a->smooth_softmax ? 2 : 0);
 }
 
 gqaw_status prepare(const gqaw_step_args *a, Launch *L, gqaw::Params *p) {

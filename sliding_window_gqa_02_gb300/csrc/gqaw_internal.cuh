@@ -39,9 +39,36 @@ struct Params {
   float biasmul;             // log2(e)
   int ncg;                   // column groups per cache row in the copy jobs
   int rowbytes;              // D * element size
+  const float *sink;         // NULL or (Nq,): sink logit per query head (natural-log units)
+  int sink_mode;             // 0: no sink; 1: sink[h]; 2: a sink of 0 for every head
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// The sink logit of query head h in log2 units, -inf when there is none (mobius
+// issue #111, Part 1.1 input head_sink and Part 1.3 smooth_softmax).
+__device__ __forceinline__ float sink_log2(const Params &p, int h) {
+  if (p.sink_mode == 1) return p.sink[h] * kLog2e;
+  return p.sink_mode == 2 ? 0.f : -INFINITY;
+}
+
+// Output of a softmax row from its accumulator A and denominator l, both taken
+// against the reference maximum m (log2 units), with the sink logit s2 joining the
+// denominator: A / (l + 2^(s2 - m)), scaled by 2^(m - s2) when the sink is the larger
+// so that nothing overflows.  Without a sink (s2 = -inf) this is A / l exactly.
+__device__ __forceinline__ float sink_divide(float A, float l, float m, float s2) {
+  if (s2 <= m) return A / (l + exp2f(s2 - m));
+  const float f = exp2f(m - s2);
+  return (A * f) / fmaf(l, f, 1.f);
+}
+
+// The factor 1 / (l + 2^(s2 - m)) that turns accumulators into outputs, in the same
+// overflow-safe form; 1 / l exactly without a sink.
+__device__ __forceinline__ float sink_reciprocal(float l, float m, float s2) {
+  if (s2 <= m) return 1.f / (l + exp2f(s2 - m));
+  const float f = exp2f(m - s2);
+  return f / fmaf(l, f, 1.f);
+}
 
 // L(T) in 64-bit integers.
 __device__ __forceinline__ long long resident_len(long long T, long long C, long long W) {

@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (ok) {
     if (ta.nsplit == 1) {
       if (row_ok) {
-        const float inv = 1.f / l_run;
+        const float inv = sink_reciprocal(l_run, m_run, sink_log2(p, h));
 #pragma unroll
         for (int c = 0; c < kD; c += 8) {
           uint4 w;
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             f[q] = mq == -INFINITY ? 0.f : exp2f(mq - mb);
             L += f[q] * __ldcg(p.partials + ((first + q) * kRows + r) * kTcPartialStride + kD + 1);
           }
-          const float inv = 1.f / L;
+          const float inv = sink_reciprocal(L, mb, sink_log2(p, h));
           for (int c = 0; c < kD; c += 2) {
             float a0 = 0.f, a1 = 0.f;
             for (int q = 0; q < ta.nsplit && q < 16; ++q) {

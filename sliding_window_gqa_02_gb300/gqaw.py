@@ -67,6 +67,8 @@ class gqaw_step_args(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("resident_len_out", ctypes.c_void_p),
+        ("head_sink", ctypes.c_void_p),
+        ("smooth_softmax", ctypes.c_int32),
     ]
 
 
@@ -193,13 +195,15 @@ def _dtype_code(t) -> int:
 def make_args(query, key, value, past_key, past_value, present_key, present_value, seqlens_k,
               total_sequence_length: int, num_heads: int, kv_num_heads: int, local_window_size: int,
               output, workspace=None, scale: float = 0.0, softcap: float = 0.0, attention_bias=None,
-              bias_strides=None, resident_len_out=None, split_keys: int = 0) -> gqaw_step_args:
+              bias_strides=None, resident_len_out=None, split_keys: int = 0, head_sink=None,
+              smooth_softmax: bool = False) -> gqaw_step_args:
     """Fill a ``gqaw_step_args`` from CUDA tensors (shapes as in include/gqaw.h).
 
     ``attention_bias``: fp32 tensor whose last dimension is contiguous; its (b, h, s)
     strides are taken from the tensor (a size-1 dimension broadcasts with stride 0)
     unless ``bias_strides`` gives them in elements.  ``workspace``: a uint8 CUDA
-    tensor, or None when only the size is wanted.
+    tensor, or None when only the size is wanted.  ``head_sink``: None or a contiguous
+    fp32 (num_heads,) CUDA tensor of sink logits; ``smooth_softmax``: a sink of 0.
     """
     B, Nkv, C, D = past_key.shape
     S = query.shape[1]
@@ -227,6 +231,12 @@ def make_args(query, key, value, past_key, past_value, present_key, present_valu
     if workspace is not None:
         a.workspace, a.workspace_bytes = _ptr(workspace), int(workspace.numel() * workspace.element_size())
     a.resident_len_out = _ptr(resident_len_out)
+    if head_sink is not None:
+        if str(head_sink.dtype) != "torch.float32" or tuple(head_sink.shape) != (int(num_heads),) \
+                or not head_sink.is_contiguous():
+            raise ValueError("head_sink: contiguous float32 tensor of shape (num_heads,)")
+        a.head_sink = _ptr(head_sink)
+    a.smooth_softmax = int(bool(smooth_softmax))
     return a
 
 

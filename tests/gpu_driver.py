@@ -17,8 +17,10 @@ TOL = {wl.F32: 1e-5, wl.BF16: 2e-2}
 
 class GpuCache:
     def __init__(self, B, Nq, Nkv, D, C, W, dtype, scale=0.0, softcap=0.0, past_key=None, past_value=None,
-                 inplace=True, split_keys=0):
+                 inplace=True, split_keys=0, head_sink=None, smooth_softmax=False):
         self.dev = torch.device("cuda:0")
+        self.head_sink = None if head_sink is None else head_sink.to(self.dev).contiguous()
+        self.smooth_softmax = smooth_softmax
         self.B, self.Nq, self.Nkv, self.D, self.C, self.W = B, Nq, Nkv, D, C, W
         self.dtype, self.scale, self.softcap = dtype, scale, softcap
         self.inplace, self.split_keys = inplace, split_keys
@@ -41,7 +43,8 @@ class GpuCache:
         dbias = None if bias is None else bias.to(self.dev)
         rk, rv = (self.pk, self.pv) if self.inplace else (self.rk, self.rv)
         kw = dict(scale=self.scale, softcap=self.softcap, attention_bias=dbias, bias_strides=bias_strides,
-                  resident_len_out=res, split_keys=self.split_keys)
+                  resident_len_out=res, split_keys=self.split_keys, head_sink=self.head_sink,
+                  smooth_softmax=self.smooth_softmax)
         args = gqaw.make_args(dq, dk, dv, self.pk, self.pv, rk, rv, seq, total, self.Nq, self.Nkv, self.W,
                               out, **kw)
         stream = torch.cuda.current_stream().cuda_stream

@@ -12,7 +12,8 @@ import oracle
 
 class OracleCache:
     def __init__(self, B, Nq, Nkv, D, C, W, dtype=oracle.F32, scale=0.0, softcap=0.0,
-                 past_key=None, past_value=None):
+                 past_key=None, past_value=None, head_sink=None, smooth_softmax=False):
+        self.head_sink, self.smooth_softmax = head_sink, smooth_softmax
         self.B, self.Nq, self.Nkv, self.D, self.C, self.W = B, Nq, Nkv, D, C, W
         self.dtype, self.scale, self.softcap = dtype, scale, softcap
         et = np.float32 if dtype == oracle.F32 else np.uint16
@@ -25,6 +26,7 @@ class OracleCache:
             total = int(seqlens.max()) + 1
         r = oracle.step(q, k, v, self.pk, self.pv, seqlens, total, self.Nq, self.Nkv, self.W,
                         scale=self.scale, softcap=self.softcap, attention_bias=bias,
-                        bias_strides=bias_strides, dtype=self.dtype)
+                        bias_strides=bias_strides, dtype=self.dtype, head_sink=self.head_sink,
+                        smooth_softmax=self.smooth_softmax)
         self.pk, self.pv = r["present_key"], r["present_value"]
         return r

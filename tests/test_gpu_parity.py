@@ -33,12 +33,14 @@ class Pair:
     """The same cache driven by the CUDA library and by the oracle."""
 
     def __init__(self, B, Nq, Nkv, D, C, W, dtype, scale=0.0, softcap=0.0, past_key=None, past_value=None,
-                 inplace=True, split_keys=0):
+                 inplace=True, split_keys=0, head_sink=None, smooth_softmax=False):
         self.dtype = dtype
-        self.g = GpuCache(B, Nq, Nkv, D, C, W, dtype, scale, softcap, past_key, past_value, inplace, split_keys)
+        self.g = GpuCache(B, Nq, Nkv, D, C, W, dtype, scale, softcap, past_key, past_value, inplace, split_keys,
+                          head_sink, smooth_softmax)
         self.o = OracleCache(B, Nq, Nkv, D, C, W, oracle_dtype(dtype), scale, softcap,
                              None if past_key is None else wl.to_numpy(past_key),
-                             None if past_value is None else wl.to_numpy(past_value))
+                             None if past_value is None else wl.to_numpy(past_value),
+                             None if head_sink is None else wl.to_numpy(head_sink), smooth_softmax)
         self.errs = []
 
     def step(self, q, k, v, seqlens, total=None, bias=None, bias_strides=None, phases=False):

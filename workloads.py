@@ -106,6 +106,11 @@ def bias(B: int, Nq: int, S: int, total: int, seed: int, std: float = 0.5) -> to
     return draw((B, Nq, S, total), F32, seed + 200003, "normal", std)
 
 
+def head_sink(Nq: int, seed: int, mean: float = 0.0, std: float = 2.0) -> torch.Tensor:
+    """fp32 sink logits (Nq,) ~ N(mean, std^2), one per query head."""
+    return draw((Nq,), F32, seed + 400009, "normal", std) + mean
+
+
 def lengths(B: int, lo: int, hi: int, seed: int) -> np.ndarray:
     """Per-item token counts T_b ~ U{lo..hi} (inclusive), int64."""
     rng = np.random.Generator(np.random.Philox(seed + 300007))
