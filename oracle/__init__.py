@@ -37,6 +37,7 @@ _ERRORS = {
     2: "seqlens_k[b] + 1 - S < 0 for some item",
     3: "T_b > total_sequence_length for some item",
     4: "out of memory",
+    5: "rotary position outside the cos/sin caches",
 }
 
 
@@ -72,6 +73,13 @@ class _Args(ctypes.Structure):
         ("s_end", ctypes.c_int64),
         ("head_sink", ctypes.c_void_p),
         ("smooth_softmax", ctypes.c_int64),
+        ("do_rotary", ctypes.c_int64),
+        ("rotary_interleaved", ctypes.c_int64),
+        ("rotary_dim", ctypes.c_int64),
+        ("rotary_cache_len", ctypes.c_int64),
+        ("cos_cache", ctypes.c_void_p),
+        ("sin_cache", ctypes.c_void_p),
+        ("position_ids", ctypes.c_void_p),
     ]
 
 
@@ -126,7 +134,8 @@ def _elem_dtype(dtype: int):
 
 def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_length,
          num_heads, kv_num_heads, local_window_size, scale=0.0, softcap=0.0,
-         attention_bias=None, bias_strides=None, dtype=F32, rows=None, head_sink=None, smooth_softmax=0):
+         attention_bias=None, bias_strides=None, dtype=F32, rows=None, head_sink=None, smooth_softmax=0,
+         cos_cache=None, sin_cache=None, position_ids=None, rotary_interleaved=False):
     """One windowed GQA step on host arrays.
 
     Arrays are numpy: float32 for ``dtype=F32``; uint16 bfloat16 bit patterns for
@@ -142,6 +151,9 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
     only for new tokens s0 <= s < s1 (other output rows stay zero); ``rows=(0, 0)``
     gives the cache layout alone.  ``head_sink`` (float32 (Nq,)) adds a sink logit per
     head to the softmax denominator; ``smooth_softmax`` adds a sink of 0 to every head.
+    ``cos_cache``/``sin_cache`` ((max_pos, rd/2) in the step's dtype) turn on the rotary
+    embedding of the new query and key rows; ``position_ids`` (int64 (B, S)) overrides
+    the positions P_b + s; ``rotary_interleaved`` pairs dimensions (2i, 2i+1).
     """
     lib = _load()
     et = _elem_dtype(dtype)
@@ -155,7 +167,17 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
         head_sink = np.ascontiguousarray(head_sink, dtype=np.float32)
         if head_sink.shape != (num_heads,):
             raise ValueError("oracle.step: head_sink must be (num_heads,)")
+    do_rotary = cos_cache is not None
+    if do_rotary:
+        cos_cache = np.ascontiguousarray(cos_cache, dtype=et)
+        sin_cache = np.ascontiguousarray(sin_cache, dtype=et)
+        if cos_cache.ndim != 2 or sin_cache.shape != cos_cache.shape:
+            raise ValueError("oracle.step: cos_cache and sin_cache must be equal (max_pos, rd/2) arrays")
     B, Nkv, C, D = past_key.shape
+    if do_rotary and position_ids is not None:
+        position_ids = np.ascontiguousarray(position_ids, dtype=np.int64)
+        if position_ids.shape != (B, query.shape[1]):
+            raise ValueError("oracle.step: position_ids must be (B, S)")
     S = query.shape[1]
     if query.shape != (B, S, num_heads * D) or key.shape != (B, S, kv_num_heads * D):
         raise ValueError("oracle.step: shape mismatch")
@@ -192,6 +214,11 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
         s_begin=0 if rows is None else int(rows[0]),
         s_end=S if rows is None else int(rows[1]),
         head_sink=_ptr(head_sink), smooth_softmax=int(bool(smooth_softmax)),
+        do_rotary=int(do_rotary), rotary_interleaved=int(bool(rotary_interleaved)),
+        rotary_dim=2 * cos_cache.shape[1] if do_rotary else 0,
+        rotary_cache_len=cos_cache.shape[0] if do_rotary else 0,
+        cos_cache=_ptr(cos_cache), sin_cache=_ptr(sin_cache),
+        position_ids=_ptr(position_ids) if do_rotary else None,
     )
     rc = lib.oracle_step(ctypes.byref(a))
     if rc != 0:

@@ -34,7 +34,18 @@
  *  - head_sink / smooth_softmax ([P3] Part 1.1 input 11 and Part 1.3, named only):
  *    a sink is one more logit per head that joins the softmax denominator and has no
  *    value row; it is taken as given (not scaled, capped or biased); smooth_softmax is
- *    a sink of 0 for every head; head_sink wins when both are given.
+ *    a sink of 0 for every head; head_sink wins when both are given;
+ *  - rotary embedding ([P3] Part 1.1 inputs cos_cache, sin_cache, position_ids and
+ *    Part 1.3 attributes do_rotary, rotary_interleaved; named only): the rotary
+ *    position embedding of RoFormer (Su et al.), each pair of dimensions (x1, x2)
+ *    turned by the angle of its position, y1 = x1 cos - x2 sin, y2 = x2 cos + x1 sin,
+ *    with cos/sin read from row `pos` of the caches at column i for the i-th pair.
+ *    Pairs are (i, i + rd/2) by default and (2i, 2i + 1) when interleaved; rd is
+ *    twice the cache width (head_size unless given), dimensions from rd on pass
+ *    through.  pos = position_ids[b, s] if given, else the absolute position P_b + s.
+ *    The new query and key rows of the step are turned before use; the turned key
+ *    rows are what the cache stores (rounded once to the cache dtype), the turned
+ *    query stays in double.  Values are not turned.
  *
  * Precision: every input element is widened exactly to double; dot products,
  * softcap, softmax and the weighted sum are evaluated in double in ascending key
@@ -52,7 +63,8 @@ enum {
   ORACLE_EARGS = 1,     /* malformed sizes */
   ORACLE_EPAST = 2,     /* seqlens_k[b] + 1 - S < 0 for some item */
   ORACLE_ETOTAL = 3,    /* T_b > total_sequence_length for some item */
-  ORACLE_ENOMEM = 4
+  ORACLE_ENOMEM = 4,
+  ORACLE_EPOS = 5       /* a rotary position outside [0, rotary_cache_len) */
 };
 
 typedef struct oracle_args {
@@ -85,6 +97,13 @@ typedef struct oracle_args {
                                 present rows are always written */
   const float *head_sink;    /* NULL or (Nq,): a sink logit per query head */
   int64_t smooth_softmax;    /* non-zero: a sink logit of 0 for every head (if no head_sink) */
+  int64_t do_rotary;         /* non-zero: turn the new query and key rows (rotary embedding) */
+  int64_t rotary_interleaved; /* non-zero: pairs (2i, 2i+1); else (i, i + rd/2) */
+  int64_t rotary_dim;        /* rd, even, 0 < rd <= D */
+  int64_t rotary_cache_len;  /* rows of cos_cache / sin_cache */
+  const void *cos_cache;     /* (rotary_cache_len, rd/2) in dtype */
+  const void *sin_cache;     /* (rotary_cache_len, rd/2) in dtype */
+  const int64_t *position_ids; /* NULL or (B, S) */
 } oracle_args;
 
 /* [P1] Description, resident-count formula:
@@ -157,10 +176,50 @@ static int64_t input_row(const oracle_args *a, int64_t b, int64_t s, int64_t kvh
   return ((b * a->sequence_length + s) * a->kv_num_heads + kvh) * a->head_size;
 }
 
+/* The rotary embedding of one row of D elements at element offset `off` of `src`,
+ * turned by the angles of position `pos` (reading above), into y[0..D) in double. */
+static void rotate_row(const oracle_args *a, const void *src, int64_t off, int64_t pos, double *y) {
+  const int64_t D = a->head_size, half = a->rotary_dim / 2;
+  int64_t i;
+  for (i = 0; i < D; ++i) y[i] = load_elem(src, off + i, a->dtype);
+  for (i = 0; i < half; ++i) {
+    const double c = load_elem(a->cos_cache, pos * half + i, a->dtype);
+    const double sn = load_elem(a->sin_cache, pos * half + i, a->dtype);
+    const int64_t i1 = a->rotary_interleaved ? 2 * i : i;
+    const int64_t i2 = a->rotary_interleaved ? 2 * i + 1 : i + half;
+    const double x1 = y[i1], x2 = y[i2];
+    y[i1] = x1 * c - x2 * sn;
+    y[i2] = x2 * c + x1 * sn;
+  }
+}
+
+/* Turns the S new query and key rows of item b (reading above): the query rows into
+ * qrot (B, S, Nq*D) doubles, the key rows into krot (B, S, Nkv*D) in the cache dtype. */
+static int rotate_item(const oracle_args *a, int64_t b, double *qrot, void *krot, double *y) {
+  const int64_t S = a->sequence_length, D = a->head_size;
+  const int64_t P = (int64_t)a->seqlens_k[b] + 1 - S;
+  int64_t s, h, d;
+  for (s = 0; s < S; ++s) {
+    const int64_t pos = a->position_ids ? a->position_ids[b * S + s] : P + s;
+    if (pos < 0 || pos >= a->rotary_cache_len) return ORACLE_EPOS;
+    for (h = 0; h < a->num_heads; ++h) {
+      const int64_t off = ((b * S + s) * a->num_heads + h) * D;
+      rotate_row(a, a->query, off, pos, qrot + off);
+    }
+    for (h = 0; h < a->kv_num_heads; ++h) {
+      const int64_t off = input_row(a, b, s, h);
+      rotate_row(a, a->key, off, pos, y);
+      for (d = 0; d < D; ++d) store_elem(krot, off + d, a->dtype, y[d]);
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* One step for one batch item.  The virtual sequence X of item b has Lp + S rows:
  * X[r] = past row r for r < Lp, else new token r - Lp.  X[r] holds absolute
  * position P - Lp + r ([P1] row layout applied to the past length P). */
-static int step_item(const oracle_args *a, int64_t b, double *z, double *acc) {
+static int step_item(const oracle_args *a, int64_t b, double *z, double *acc, const double *qrot,
+                     const void *krot) {
   const int64_t S = a->sequence_length, D = a->head_size, W = a->local_window_size;
   const int64_t Nq = a->num_heads, Nkv = a->kv_num_heads, C = a->capacity;
   const int64_t group = Nq / Nkv;
@@ -168,6 +227,8 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc) {
   const int64_t T = (int64_t)a->seqlens_k[b] + 1; /* [P1] review: T_b = seqlens_k[b] + 1 */
   const int64_t P = T - S;                         /* [P2] review: past length */
   int64_t Lp, Lt, first_pos, s, h, kvh, r, d, j;
+
+  const void *key = krot ? krot : a->key; /* the new key rows, turned if do_rotary */
 
   if (P < 0) return ORACLE_EPAST;
   if (T > a->total_sequence_length) return ORACLE_ETOTAL;
@@ -188,11 +249,11 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc) {
       kvh = h / group;
       for (j = jlo; j <= i; ++j) {
         const int64_t xr = j - first_pos;
-        const void *kb = xr < Lp ? a->past_key : a->key;
+        const void *kb = xr < Lp ? a->past_key : key;
         const int64_t koff = xr < Lp ? cache_row(a, b, kvh, xr) : input_row(a, b, xr - Lp, kvh);
         double dot = 0.0, zj;
         for (d = 0; d < D; ++d)
-          dot += load_elem(a->query, qoff + d, a->dtype) * load_elem(kb, koff + d, a->dtype);
+          dot += (qrot ? qrot[qoff + d] : load_elem(a->query, qoff + d, a->dtype)) * load_elem(kb, koff + d, a->dtype);
         zj = a->scale * dot;
         if (a->softcap > 0.0) zj = a->softcap * tanh(zj / a->softcap);
         if (a->attention_bias)
@@ -230,7 +291,7 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc) {
     for (r = 0; r < Lt; ++r) {
       const int64_t xr = Lp + S - Lt + r;
       const int64_t src = xr < Lp ? cache_row(a, b, kvh, xr) : input_row(a, b, xr - Lp, kvh);
-      const void *ksrc = xr < Lp ? a->past_key : a->key;
+      const void *ksrc = xr < Lp ? a->past_key : key;
       const void *vsrc = xr < Lp ? a->past_value : a->value;
       const int64_t dst = cache_row(a, b, kvh, r);
       memcpy((char *)a->present_key + dst * esize, (const char *)ksrc + src * esize, D * esize);
@@ -245,23 +306,39 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc) {
  * error met (items before it are already written). */
 int oracle_step(const oracle_args *a) {
   int64_t b, nz;
-  double *z, *acc;
+  double *z, *acc, *qrot = NULL;
+  void *krot = NULL;
   int rc = ORACLE_OK;
   if (a->batch_size < 0 || a->sequence_length < 1 || a->num_heads < 1 || a->kv_num_heads < 1 ||
       a->num_heads % a->kv_num_heads != 0 || a->head_size < 1 || a->capacity < 1 ||
       a->local_window_size < 1 || a->local_window_size > a->capacity ||
       (a->dtype != ORACLE_F32 && a->dtype != ORACLE_BF16))
     return ORACLE_EARGS;
+  if (a->do_rotary && (a->rotary_dim < 2 || a->rotary_dim % 2 != 0 || a->rotary_dim > a->head_size ||
+                       a->rotary_cache_len < 0 || !a->cos_cache || !a->sin_cache))
+    return ORACLE_EARGS;
   nz = a->local_window_size;
   z = (double *)malloc(sizeof(double) * (size_t)nz);
   acc = (double *)malloc(sizeof(double) * (size_t)a->head_size);
-  if (!z || !acc) {
+  if (a->do_rotary) {
+    const size_t rows = (size_t)(a->batch_size * a->sequence_length);
+    qrot = (double *)malloc(sizeof(double) * rows * (size_t)(a->num_heads * a->head_size) + 8);
+    krot = malloc(8 * rows * (size_t)(a->kv_num_heads * a->head_size) + 8);
+  }
+  if (!z || !acc || (a->do_rotary && (!qrot || !krot))) {
     free(z);
     free(acc);
+    free(qrot);
+    free(krot);
     return ORACLE_ENOMEM;
   }
-  for (b = 0; b < a->batch_size && rc == ORACLE_OK; ++b) rc = step_item(a, b, z, acc);
+  for (b = 0; b < a->batch_size && rc == ORACLE_OK; ++b) {
+    if (a->do_rotary) rc = rotate_item(a, b, qrot, krot, acc);
+    if (rc == ORACLE_OK) rc = step_item(a, b, z, acc, qrot, krot);
+  }
   free(z);
   free(acc);
+  free(qrot);
+  free(krot);
   return rc;
 }

@@ -496,3 +496,188 @@ def test_sink_closed_forms():
     assert np.array_equal(plain["output_f64"], none["output_f64"])
     assert np.array_equal(zero["output_f64"], smooth["output_f64"])
     assert not np.array_equal(plain["output_f64"], smooth["output_f64"])
+
+
+# ---------------------------------------------------------------- rotary embedding
+# mobius issue #111, Part 1.1 (cos_cache, sin_cache, position_ids) and Part 1.3
+# (do_rotary, rotary_interleaved) name the fused rotary embedding; the reading is the
+# RoFormer rotation of dimension pairs by the angle of the token's position.  The pins
+# below use the complex-number form of that rotation (pair (x1, x2) as x1 + i x2,
+# multiplied by e^(i theta)), a worked quarter turn, and the relative-position property.
+
+
+def _rope_tables(npos, half, base=10000.0, dtype=np.float32):
+    """cos/sin caches of the usual RoPE angles pos * base^(-i/half)."""
+    ang = np.arange(npos)[:, None] * base ** (-np.arange(half)[None, :] / half)
+    return np.cos(ang).astype(dtype), np.sin(ang).astype(dtype)
+
+
+def _pairs(D, rd, interleaved):
+    half = rd // 2
+    return [(2 * i, 2 * i + 1) if interleaved else (i, i + half) for i in range(half)]
+
+
+def _turn_complex(x, pos, cos, sin, rd, interleaved):
+    """x (D,) turned by the angles of row pos, in complex arithmetic."""
+    y = x.astype(np.float64).copy()
+    for i, (a, b) in enumerate(_pairs(len(x), rd, interleaved)):
+        z = complex(x[a], x[b]) * complex(float(cos[pos, i]), float(sin[pos, i]))
+        y[a], y[b] = z.real, z.imag
+    return y
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_rotary_quarter_turn(interleaved):
+    """A quarter turn (cos 0, sin 1) of the first pair sends its first unit vector to
+    its second and the second to minus the first; other pairs (cos 1, sin 0) stay."""
+    D, C, W = 8, 8, 8
+    half = D // 2
+    cos = np.ones((4, half), np.float32)
+    sin = np.zeros((4, half), np.float32)
+    cos[2, 0], sin[2, 0] = 0.0, 1.0  # position 2: quarter turn of pair 0
+    a, b = _pairs(D, D, interleaved)[0]
+    k = np.zeros((1, 3, D), np.float32)
+    k[0, 2, a] = 1.0  # token at position 2: unit vector on the pair's first dimension
+    k[0, 1, a] = 1.0  # position 1: identity
+    r = oracle.step(np.zeros((1, 3, D), np.float32), k, k, np.zeros((1, 1, C, D), np.float32),
+                    np.zeros((1, 1, C, D), np.float32), np.array([2], np.int32), 3, 1, 1, W,
+                    cos_cache=cos, sin_cache=sin, rotary_interleaved=interleaved)
+    pk = r["present_key"][0, 0]
+    assert pk[2, b] == 1.0 and pk[2, a] == 0.0 and np.count_nonzero(pk[2]) == 1
+    assert pk[1, a] == 1.0 and np.count_nonzero(pk[1]) == 1
+    k[0, 2, a], k[0, 2, b] = 0.0, 1.0
+    r = oracle.step(np.zeros((1, 3, D), np.float32), k, k, np.zeros((1, 1, C, D), np.float32),
+                    np.zeros((1, 1, C, D), np.float32), np.array([2], np.int32), 3, 1, 1, W,
+                    cos_cache=cos, sin_cache=sin, rotary_interleaved=interleaved)
+    pk = r["present_key"][0, 0]
+    assert pk[2, a] == -1.0 and np.count_nonzero(pk[2]) == 1
+    # values are not turned
+    assert np.array_equal(r["present_value"][0, 0, :3], k[0])
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+@pytest.mark.parametrize("rd", [8, 4])
+def test_rotary_cache_rows_are_turned_keys(interleaved, rd):
+    """Across compactions and a ragged batch, resident row r holds the key of absolute
+    position p = T - L + r turned by the angles of p (complex form); dimensions from
+    rd on are the input's bits."""
+    D, Nq, Nkv, C, W = 8, 2, 1, 7, 4
+    cos, sin = _rope_tables(64, rd // 2)
+    rng = _rng(50)
+    total = 40
+    keys = _u(rng, (2, total, Nkv * D))
+    oc = OracleCache(2, Nq, Nkv, D, C, W, cos_cache=cos, sin_cache=sin, rotary_interleaved=interleaved)
+    T0 = np.array([0, 5])  # item 1 starts from a zero past of 5 tokens: only rows written here are checked
+    T = T0.copy()
+    for S in [6, 1, 3, 1, 1, 4, 2]:
+        q = _u(rng, (2, S, Nq * D))
+        k = np.stack([keys[b, T[b]:T[b] + S] for b in range(2)])
+        r = oc.step(q, k, k, T + S - 1)
+        T = T + S
+        for b in range(2):
+            L = int(r["resident_len"][b])
+            for row in range(L):
+                pos = T[b] - L + row
+                if pos < T0[b]:
+                    continue
+                want = _turn_complex(keys[b, pos], pos, cos, sin, rd, interleaved)
+                got = r["present_key"][b, 0, row]
+                np.testing.assert_allclose(got[:rd], want[:rd], rtol=0, atol=2e-7)
+                assert np.array_equal(got[rd:], keys[b, pos, rd:])
+
+
+def test_rotary_position_ids_override():
+    """position_ids replace the absolute positions: turning by ids equal to P + s gives
+    the default's bits, and a shifted id turns the key by the shifted angle."""
+    D, C, W = 8, 8, 8
+    cos, sin = _rope_tables(32, D // 2)
+    rng = _rng(51)
+    q, k = _u(rng, (1, 3, D)), _u(rng, (1, 3, D))
+    z = np.zeros((1, 1, C, D), np.float32)
+    base = oracle.step(q, k, k, z, z, np.array([4], np.int32), 5, 1, 1, W, cos_cache=cos, sin_cache=sin)
+    same = oracle.step(q, k, k, z, z, np.array([4], np.int32), 5, 1, 1, W, cos_cache=cos, sin_cache=sin,
+                       position_ids=np.array([[2, 3, 4]]))
+    assert np.array_equal(base["output_f64"], same["output_f64"])
+    assert np.array_equal(base["present_key"], same["present_key"])
+    moved = oracle.step(q, k, k, z, z, np.array([4], np.int32), 5, 1, 1, W, cos_cache=cos, sin_cache=sin,
+                        position_ids=np.array([[2, 3, 20]]))
+    np.testing.assert_allclose(moved["present_key"][0, 0, 4], _turn_complex(k[0, 2], 20, cos, sin, D, False),
+                               rtol=0, atol=2e-7)
+    with pytest.raises(ValueError):
+        oracle.step(q, k, k, z, z, np.array([4], np.int32), 5, 1, 1, W, cos_cache=cos, sin_cache=sin,
+                    position_ids=np.array([[2, 3, 32]]))
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_rotary_relative_position_invariance(interleaved):
+    """RoFormer's property: turned q.k depends on the positions' difference only, so
+    one prefill step from an empty cache gives the same outputs (to fp64 rounding) at
+    positions 0..S-1 and at 1000..1000+S-1.  Fails if the query and keys are turned
+    with different positions or conventions."""
+    D, Nq, Nkv, S = 16, 4, 2, 9
+    cos, sin = _rope_tables(1100, D // 2, dtype=np.float64)
+    rng = _rng(52)
+    q, k, v = _u(rng, (1, S, Nq * D)), _u(rng, (1, S, Nkv * D)), _u(rng, (1, S, Nkv * D))
+    z = np.zeros((1, Nkv, S, D), np.float32)
+    outs = []
+    for shift in (0, 1000):
+        r = oracle.step(q, k, v, z, z, np.array([S - 1], np.int32), S, Nq, Nkv, 6, cos_cache=cos.astype(np.float32),
+                        sin_cache=sin.astype(np.float32), position_ids=np.arange(S)[None] + shift,
+                        rotary_interleaved=interleaved)
+        outs.append(r["output_f64"])
+    # the stored keys are rounded to fp32, and the fp32 tables are not exact rotations:
+    # agreement to about 1e-6 is all the property promises here
+    np.testing.assert_allclose(outs[0], outs[1], rtol=0, atol=5e-6)
+    plain = oracle.step(q, k, v, z, z, np.array([S - 1], np.int32), S, Nq, Nkv, 6)["output_f64"]
+    assert np.abs(plain - outs[0]).max() > 1e-3  # the rotation does change the outputs
+
+
+def test_rotary_matches_sdpa_full_history():
+    """Multi-step windowed run with rotary embedding == torch float64
+    scaled-dot-product attention over the full history of turned queries and keys
+    (turned here with torch complex multiplication, non-interleaved pairs)."""
+    D, Nq, Nkv, C, W = 8, 4, 2, 7, 5
+    cos, sin = _rope_tables(64, D // 2)
+    rng = _rng(53)
+    total = 30
+    q, k, v = _u(rng, (1, total, Nq * D)), _u(rng, (1, total, Nkv * D)), _u(rng, (1, total, Nkv * D))
+
+    def turn(x, heads):
+        t = torch.from_numpy(x.astype(np.float64)).view(total, heads, 2, D // 2)
+        zc = torch.complex(t[:, :, 0], t[:, :, 1])
+        e = torch.complex(torch.from_numpy(cos[:total].astype(np.float64)),
+                          torch.from_numpy(sin[:total].astype(np.float64)))[:, None, :]
+        y = zc * e
+        return torch.stack([y.real, y.imag], dim=2).reshape(1, total, heads * D)
+
+    qt = turn(q[0], Nq).numpy()
+    # keys are stored rounded to the cache dtype (fp32) before attention reads them
+    kt = turn(k[0], Nkv).numpy().astype(np.float32).astype(np.float64)
+    oc = OracleCache(1, Nq, Nkv, D, C, W, cos_cache=cos, sin_cache=sin)
+    T = 0
+    for S in [3, 1, 4, 1, 6, 1, 2, 5, 1]:
+        r = oc.step(q[:, T:T + S], k[:, T:T + S], v[:, T:T + S], [T + S - 1])
+        ref = _sdpa_reference(qt[:, T:T + S], kt[:, :T + S], v[:, :T + S], Nq, Nkv, D, W, T, 1.0 / math.sqrt(D),
+                              None)
+        np.testing.assert_allclose(r["output_f64"], ref, rtol=0, atol=1e-12)
+        T += S
+
+
+def test_rotary_chunk_invariance():
+    """With rotary embedding, a 5-token step equals five 1-token steps bit for bit:
+    every token is turned by its own absolute position however the stream is split."""
+    D, Nq, Nkv, C, W = 8, 2, 1, 6, 4
+    cos, sin = _rope_tables(40, D // 2)
+    rng = _rng(54)
+    qp, kp, vp = _u(rng, (1, 7, Nq * D)), _u(rng, (1, 7, D)), _u(rng, (1, 7, D))
+    q5, k5, v5 = _u(rng, (1, 5, Nq * D)), _u(rng, (1, 5, D)), _u(rng, (1, 5, D))
+    a = OracleCache(1, Nq, Nkv, D, C, W, cos_cache=cos, sin_cache=sin, rotary_interleaved=True)
+    b = OracleCache(1, Nq, Nkv, D, C, W, cos_cache=cos, sin_cache=sin, rotary_interleaved=True)
+    a.step(qp, kp, vp, [6])
+    b.step(qp, kp, vp, [6])
+    ra = a.step(q5, k5, v5, [11])
+    for s in range(5):
+        rb = b.step(q5[:, s:s + 1], k5[:, s:s + 1], v5[:, s:s + 1], [7 + s])
+        assert np.array_equal(ra["output_f64"][:, s], rb["output_f64"][:, 0])
+    L = int(ra["resident_len"][0])
+    assert np.array_equal(a.pk[:, :, :L], b.pk[:, :, :L])
