@@ -6,7 +6,8 @@ decode token for all 64 items through the C ABI.  The K/V window read per step
 (about 1.07 GB) is larger than the 129 MB L2, so no flush is needed between steps.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl gqaw|reference]
-                    [--workload longctx-decode|longctx-decode-sink|pages-decode|slack-decode|verify8|longctx-prefill]
+                    [--workload longctx-decode|longctx-decode-sink|longctx-decode-rope|pages-decode|slack-decode|verify8|
+                     longctx-prefill|longctx-prefill-rope]
                     [--no-extra] [--no-cpu-baseline]
 
 ``--impl reference`` times the oracle (the plain fp64 CPU implementation) on this
@@ -50,9 +51,13 @@ def workload_spec(name):
     if name == "longctx-decode-sink":  # the same decode with a sink logit per query head
         return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False,
                     sink=True)
-    if name == "longctx-prefill":
+    if name == "longctx-decode-rope":  # the same decode with the rotary embedding fused in
+        return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False,
+                    rope=True)
+    if name in ("longctx-prefill", "longctx-prefill-rope"):
         sh = wl.SHAPES["longctx"]
-        return dict(shape=sh, S=512, lo=4096, hi=32768, bias=False, graph=False, accept=False, B=8)
+        return dict(shape=sh, S=512, lo=4096, hi=32768, bias=False, graph=False, accept=False, B=8,
+                    rope=name.endswith("rope"))
     if name == "pages-decode":
         return dict(shape=wl.SHAPES["pages"], S=1, lo=8192, hi=8192, bias=False, graph=True, accept=False)
     if name == "slack-decode":
@@ -70,7 +75,7 @@ def workload_config(name, B=None):
     return {"workload": name, "B": B if B else spec.get("B", sh.B), "S": spec["S"], "num_heads": sh.Nq,
             "kv_num_heads": sh.Nkv, "head_size": sh.D, "local_window_size": sh.W, "capacity": sh.C,
             "cache_dtype": sh.dtype, "softcap": sh.softcap, "bias": spec["bias"],
-            "head_sink": bool(spec.get("sink", False)), "contexts": "U[%d,%d]" % (spec["lo"], spec["hi"])}
+            "head_sink": bool(spec.get("sink", False)), "rotary": bool(spec.get("rope", False)), "contexts": "U[%d,%d]" % (spec["lo"], spec["hi"])}
 
 
 def resident_len(T, C, W):
@@ -279,6 +284,10 @@ class Harness:
             self.bias = wl.bias(B, sh.Nq, S, TM, seed).to(self.dev)
             self.bias_strides = (sh.Nq * S * TM, S * TM, TM)
         self.head_sink = wl.head_sink(sh.Nq, seed).to(self.dev) if spec.get("sink") else None
+        self.cos = self.sin = None
+        if spec.get("rope"):
+            self.cos, self.sin = (x.to(self.dev) for x in wl.rope_tables(int(self.T.max()) + S + 1, sh.D // 2,
+                                                                          sh.dtype))
         self.split_keys = split_keys
         self.args = []
         ws_bytes = 0
@@ -295,7 +304,8 @@ class Harness:
         return self.gqaw.make_args(
             self.q[i], self.k[i], self.v[i], self.pk, self.pv, self.pk, self.pv, self.seq[t], self.totals[t],
             sh.Nq, sh.Nkv, sh.W, self.out, workspace=ws, softcap=sh.softcap, attention_bias=self.bias,
-            bias_strides=self.bias_strides, split_keys=self.split_keys, head_sink=self.head_sink)
+            bias_strides=self.bias_strides, split_keys=self.split_keys, head_sink=self.head_sink,
+            cos_cache=self.cos, sin_cache=self.sin)
 
     def step(self, t):
         self.gqaw.check(self.gqaw.gqa_windowed_step(self.args[t], self.stream.cuda_stream))
@@ -324,8 +334,8 @@ class Harness:
         self.args_e2e = [self.gqaw.make_args(
             self.q[0], self.k[0], self.v[0], self.pk, self.pv, self.pk, self.pv, self.seq[t], self.totals[t],
             sh.Nq, sh.Nkv, sh.W, self.out, workspace=self.ws, softcap=sh.softcap, attention_bias=self.bias,
-            bias_strides=self.bias_strides, split_keys=self.split_keys, head_sink=self.head_sink)
-            for t in range(self.n)]
+            bias_strides=self.bias_strides, split_keys=self.split_keys, head_sink=self.head_sink,
+            cos_cache=self.cos, sin_cache=self.sin) for t in range(self.n)]
         e = self.q_host[0].element_size()
         self.h2d = (self.q_host[0].numel() + self.k_host[0].numel() + self.v_host[0].numel()) * e + self.B * 4
         self.d2h = self.out.numel() * self.out.element_size()
@@ -473,10 +483,11 @@ def extra_workloads(main, args):
     import torch
 
     out = {}
-    for name in ("pages-decode", "slack-decode", "verify8", "longctx-prefill", "longctx-decode-sink"):
+    for name in ("pages-decode", "slack-decode", "verify8", "longctx-prefill", "longctx-decode-sink",
+                 "longctx-decode-rope", "longctx-prefill-rope"):
         if name == main:
             continue
-        K = 64 if name != "longctx-prefill" else 8
+        K = 8 if name.startswith("longctx-prefill") else 64
         Wm = 3
         h = Harness(name, K, Wm, seed=5)
         torch.cuda.synchronize()
@@ -560,9 +571,13 @@ def oracle_item_step(name, seed, b_items, t_index=0):
         if spec["bias"]:
             bias = wl.to_numpy(wl.bias(1, sh.Nq, S, total, seed + b))
         sink = wl.to_numpy(wl.head_sink(sh.Nq, seed)) if spec.get("sink") else None
+        rope = {}
+        if spec.get("rope"):
+            cos, sin = wl.rope_tables(int(seq.max()) + 1, sh.D // 2, sh.dtype)
+            rope = dict(cos_cache=wl.to_numpy(cos), sin_cache=wl.to_numpy(sin))
         t0 = time.perf_counter()
         oracle.step(nq[b:b + 1], nk[b:b + 1], nv[b:b + 1], npk, npv, seq, total, sh.Nq, sh.Nkv, sh.W,
-                    softcap=sh.softcap, attention_bias=bias, dtype=odt, head_sink=sink)
+                    softcap=sh.softcap, attention_bias=bias, dtype=odt, head_sink=sink, **rope)
         el += time.perf_counter() - t0
     return el
 

@@ -39,7 +39,11 @@
  *     sink is given; output is the weighted sum of the values, rounded to the cache
  *     dtype;
  *   - present rows [0, Lt) receive the Lt most recent positions of the past rows
- *     [0, Lp) followed by the S new rows (bit copies).
+ *     [0, Lp) followed by the S new rows (bit copies);
+ *   - with do_rotary, the S new query and key rows are first turned by the rotary
+ *     embedding of their positions (pairs of dimensions (x1, x2) -> (x1 cos - x2 sin,
+ *     x2 cos + x1 sin) with cos/sin from row pos of the caches; RoFormer's rotation),
+ *     rounded once to dtype; the turned keys are the ones attended and stored.
  *
  * Memory.  The caller owns every buffer.  The library allocates nothing; all work is
  * enqueued on the caller's stream and the call returns without synchronising.
@@ -80,6 +84,7 @@ typedef enum gqaw_dtype {
 /* Bits of the device status word. */
 #define GQAW_DEV_BAD_SEQLEN 1u /* some seqlens_k[b] + 1 - S < 0 or > total_sequence_length */
 #define GQAW_DEV_TIMEOUT 2u    /* a bounded in-kernel wait expired (an internal fault) */
+#define GQAW_DEV_BAD_POSITION 4u /* a rotary position outside [0, rotary_cache_len) */
 
 /* Arguments of one step.  All tensor pointers are DEVICE pointers.  Layouts are
  * row-major with the shapes given; "BNSH" is (batch, kv head, row, head_size).
@@ -126,6 +131,17 @@ typedef struct gqaw_step_args {
                                     ([P3] Part 1.1, input 11); 4-byte aligned */
   int32_t smooth_softmax;        /* non-zero: a sink logit of 0 for every head ([P3]
                                     Part 1.3); ignored when head_sink is given */
+  int32_t do_rotary;             /* non-zero: turn the new query and key rows by the
+                                    rotary embedding before use ([P3] Part 1.3) */
+  int32_t rotary_interleaved;    /* non-zero: pairs (2i, 2i+1); 0: pairs (i, i + rd/2) */
+  int32_t rotary_dim;            /* rd: even, 2 <= rd <= D; 0 means D.  Dimensions from
+                                    rd on are not turned */
+  int32_t rotary_cache_len;      /* >= 1: rows of cos_cache and sin_cache */
+  const void *cos_cache;         /* (rotary_cache_len, rd/2) in dtype, element-aligned */
+  const void *sin_cache;         /* (rotary_cache_len, rd/2) in dtype, element-aligned */
+  const int64_t *position_ids;   /* NULL (token s of item b at position
+                                    seqlens_k[b] + 1 - S + s), or (B, S) int64, 8-byte
+                                    aligned ([P3] Part 1.1) */
 } gqaw_step_args;
 
 /* L(T) of [P1] in 64-bit arithmetic.  Pure host function.  Returns -1 if T < 0,

@@ -27,6 +27,7 @@ int attend_tile_f32(int D);
 int attend_tile_bf16(int D);
 cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream);
 cudaError_t launch_mma(const Params &p, const TcArgs &ta, const TcMaps &maps, int grid, cudaStream_t stream);
+cudaError_t launch_rotary(const Params &p, cudaStream_t stream);
 }  // namespace gqaw
 
 namespace {
@@ -59,6 +60,8 @@ struct Launch {
   int esize, rowbytes, group, gb, headblocks, tile, tpu, ncg;
   long long units, ctas, ncopy;
   size_t off_list, off_tickets, off_partials, ws_bytes;
+  int rot_dim;            // > 0: the rotary embedding is on, over this many dimensions
+  size_t off_qrot, off_krot;  // the turned query and key rows in the workspace
   bool tc;                // multi-token step on the tensor-core kernel
   gqaw::TcArgs ta;
   long long tc_grid;
@@ -90,6 +93,13 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   if (!(a->softcap >= 0.f) || !std::isfinite(a->softcap))
     return fail(GQAW_EINVAL, "softcap must be finite and >= 0");
   if (a->split_keys < 0) return fail(GQAW_EINVAL, "split_keys %d < 0", a->split_keys);
+  L->rot_dim = 0;
+  if (a->do_rotary) {
+    L->rot_dim = a->rotary_dim ? a->rotary_dim : a->head_size;
+    if (L->rot_dim < 2 || L->rot_dim % 2 != 0 || L->rot_dim > a->head_size)
+      return fail(GQAW_EINVAL, "rotary_dim %d must be even and in [2, head_size=%d]", a->rotary_dim, a->head_size);
+    if (a->rotary_cache_len < 1) return fail(GQAW_EINVAL, "rotary_cache_len %d < 1", a->rotary_cache_len);
+  }
 
   L->esize = a->dtype == GQAW_F32 ? 4 : 2;
   L->rowbytes = a->head_size * L->esize;
@@ -165,6 +175,14 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     L->ws_bytes = L->off_partials;
     if (ns > 1) L->ws_bytes += align256((size_t)L->tc_grid * 128 * gqaw::kTcPartialStride * 4);
   }
+  // Rotary embedding: the turned query and key rows, in the input layouts.
+  L->off_qrot = L->off_krot = 0;
+  if (L->rot_dim > 0) {
+    const size_t tokens = (size_t)a->batch_size * a->sequence_length;
+    L->off_qrot = align256(L->ws_bytes);
+    L->off_krot = L->off_qrot + align256(tokens * a->num_heads * a->head_size * L->esize);
+    L->ws_bytes = L->off_krot + align256(tokens * a->kv_num_heads * a->head_size * L->esize);
+  }
   return GQAW_OK;
 }
 
@@ -197,6 +215,13 @@ gqaw_status check_pointers(const gqaw_step_args *a, const Launch &L) {
       return fail(GQAW_EINVAL, "attention_bias strides must be >= 0");
   }
   if (a->head_sink && !aligned(a->head_sink, 4)) return fail(GQAW_EINVAL, "head_sink is not 4-byte aligned");
+  if (L.rot_dim > 0) {
+    if (!a->cos_cache || !a->sin_cache) return fail(GQAW_EINVAL, "do_rotary needs cos_cache and sin_cache");
+    if (!aligned(a->cos_cache, L.esize) || !aligned(a->sin_cache, L.esize))
+      return fail(GQAW_EINVAL, "cos_cache / sin_cache are not %d-byte aligned", L.esize);
+    if (a->position_ids && !aligned(a->position_ids, 8))
+      return fail(GQAW_EINVAL, "position_ids is not 8-byte aligned");
+  }
   if (!a->workspace) return fail(GQAW_EWORKSPACE, "workspace is NULL");
   if (!aligned(a->workspace, 256)) return fail(GQAW_EWORKSPACE, "workspace is not 256-byte aligned");
   if (a->workspace_bytes < L.ws_bytes)
@@ -278,6 +303,18 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
   p->rowbytes = L.rowbytes;
   p->sink = a->head_sink;
   p->sink_mode = a->head_sink ? 1 : (a->smooth_softmax ? 2 : 0);
+  p->rot_dim = L.rot_dim;
+  if (L.rot_dim > 0) {
+    p->q_in = a->query;
+    p->k_in = a->key;
+    p->q = ws + L.off_qrot;
+    p->k = ws + L.off_krot;
+    p->rcos = a->cos_cache;
+    p->rsin = a->sin_cache;
+    p->pos_ids = reinterpret_cast<const long long *>(a->position_ids);
+    p->rot_inter = a->rotary_interleaved ? 1 : 0;
+    p->rot_len = a->rotary_cache_len;
+  }
 }
 
 gqaw_status prepare(const gqaw_step_args *a, Launch *L, gqaw::Params *p) {
@@ -332,10 +369,10 @@ gqaw_status run_mma(const gqaw_step_args *a, const Launch &L, const gqaw::Params
   const cuuint64_t n_dims[3] = {D, (cuuint64_t)a->kv_num_heads, BS};
   const cuuint64_t n_str[2] = {D * 2, (cuuint64_t)a->kv_num_heads * D * 2};
   const cuuint32_t n_box[3] = {64, 1, 128};
-  if (!encode_map(&maps.q, a->query, 3, q_dims, q_str, q_box) ||
+  if (!encode_map(&maps.q, p.q, 3, q_dims, q_str, q_box) ||
       !encode_map(&maps.kc, a->past_key, 2, c_dims, c_str, c_box) ||
       !encode_map(&maps.vc, a->past_value, 2, c_dims, c_str, c_box) ||
-      !encode_map(&maps.kn, a->key, 3, n_dims, n_str, n_box) ||
+      !encode_map(&maps.kn, p.k, 3, n_dims, n_str, n_box) ||
       !encode_map(&maps.vn, a->value, 3, n_dims, n_str, n_box))
     return fail(GQAW_ECUDA, "cuTensorMapEncodeTiled failed for the multi-token kernel");
   const cudaError_t e = gqaw::launch_mma(p, L.ta, maps, (int)L.tc_grid, st);
@@ -345,6 +382,11 @@ gqaw_status run_mma(const gqaw_step_args *a, const Launch &L, const gqaw::Params
 }
 
 gqaw_status run_attend(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
+  if (L.rot_dim > 0) {
+    const cudaError_t e = gqaw::launch_rotary(p, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rotary kernel launch");
+    g_launches.fetch_add(1);
+  }
   if (L.tc) return run_mma(a, L, p, st);
   const cudaError_t e = a->dtype == GQAW_F32 ? gqaw::launch_attend_f32(p, L.gb, (int)L.ctas, st)
                                              : gqaw::launch_attend_bf16(p, L.gb, (int)L.ctas, st);

@@ -41,6 +41,12 @@ struct Params {
   int rowbytes;              // D * element size
   const float *sink;         // NULL or (Nq,): sink logit per query head (natural-log units)
   int sink_mode;             // 0: no sink; 1: sink[h]; 2: a sink of 0 for every head
+  // rotary embedding (rot_dim > 0): q and k above are the turned rows in the workspace,
+  // written by the rotary kernel from the step's inputs q_in and k_in
+  const void *q_in, *k_in;
+  const void *rcos, *rsin;   // (rot_len, rot_dim / 2) in the step's dtype
+  const long long *pos_ids;  // NULL (positions P_b + s) or (B, S)
+  int rot_dim, rot_inter, rot_len;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -117,6 +123,7 @@ template <> struct Elem<float> {
     f[3] = __uint_as_float(u.w);
   }
   __device__ __forceinline__ static float store(float x) { return x; }
+  __device__ __forceinline__ static float load(float x) { return x; }
 };
 template <> struct Elem<__nv_bfloat16> {
   static constexpr int kPerVec = 8;
@@ -132,6 +139,7 @@ template <> struct Elem<__nv_bfloat16> {
     f[7] = __uint_as_float(u.w & 0xffff0000u);
   }
   __device__ __forceinline__ static __nv_bfloat16 store(float x) { return __float2bfloat16_rn(x); }
+  __device__ __forceinline__ static float load(__nv_bfloat16 x) { return __bfloat162float(x); }
 };
 
 // ---------------------------------------------------------------- mbarrier + bulk copy

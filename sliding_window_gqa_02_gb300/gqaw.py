@@ -24,6 +24,7 @@ GQAW_BF16 = 1
 
 GQAW_DEV_BAD_SEQLEN = 1
 GQAW_DEV_TIMEOUT = 2
+GQAW_DEV_BAD_POSITION = 4
 
 STATUS_NAMES = {0: "GQAW_OK", 1: "GQAW_EINVAL", 2: "GQAW_EUNSUPPORTED", 3: "GQAW_ECUDA",
                 4: "GQAW_EWORKSPACE", 5: "GQAW_EDEVICE"}
@@ -69,6 +70,13 @@ class gqaw_step_args(ctypes.Structure):
         ("resident_len_out", ctypes.c_void_p),
         ("head_sink", ctypes.c_void_p),
         ("smooth_softmax", ctypes.c_int32),
+        ("do_rotary", ctypes.c_int32),
+        ("rotary_interleaved", ctypes.c_int32),
+        ("rotary_dim", ctypes.c_int32),
+        ("rotary_cache_len", ctypes.c_int32),
+        ("cos_cache", ctypes.c_void_p),
+        ("sin_cache", ctypes.c_void_p),
+        ("position_ids", ctypes.c_void_p),
     ]
 
 
@@ -196,7 +204,8 @@ def make_args(query, key, value, past_key, past_value, present_key, present_valu
               total_sequence_length: int, num_heads: int, kv_num_heads: int, local_window_size: int,
               output, workspace=None, scale: float = 0.0, softcap: float = 0.0, attention_bias=None,
               bias_strides=None, resident_len_out=None, split_keys: int = 0, head_sink=None,
-              smooth_softmax: bool = False) -> gqaw_step_args:
+              smooth_softmax: bool = False, cos_cache=None, sin_cache=None, position_ids=None,
+              rotary_interleaved: bool = False) -> gqaw_step_args:
     """Fill a ``gqaw_step_args`` from CUDA tensors (shapes as in include/gqaw.h).
 
     ``attention_bias``: fp32 tensor whose last dimension is contiguous; its (b, h, s)
@@ -204,6 +213,9 @@ def make_args(query, key, value, past_key, past_value, present_key, present_valu
     unless ``bias_strides`` gives them in elements.  ``workspace``: a uint8 CUDA
     tensor, or None when only the size is wanted.  ``head_sink``: None or a contiguous
     fp32 (num_heads,) CUDA tensor of sink logits; ``smooth_softmax``: a sink of 0.
+    ``cos_cache``/``sin_cache``: contiguous (max_pos, rd/2) CUDA tensors of the step's
+    dtype; giving them turns on the rotary embedding (rd = twice their width);
+    ``position_ids``: None or a contiguous int64 (B, S) CUDA tensor.
     """
     B, Nkv, C, D = past_key.shape
     S = query.shape[1]
@@ -237,6 +249,19 @@ def make_args(query, key, value, past_key, past_value, present_key, present_valu
             raise ValueError("head_sink: contiguous float32 tensor of shape (num_heads,)")
         a.head_sink = _ptr(head_sink)
     a.smooth_softmax = int(bool(smooth_softmax))
+    if cos_cache is not None:
+        if sin_cache is None or tuple(sin_cache.shape) != tuple(cos_cache.shape) or cos_cache.dim() != 2 \
+                or not (cos_cache.is_contiguous() and sin_cache.is_contiguous()) \
+                or cos_cache.dtype != past_key.dtype or sin_cache.dtype != past_key.dtype:
+            raise ValueError("cos_cache/sin_cache: equal contiguous (max_pos, rd/2) tensors of the cache dtype")
+        a.do_rotary, a.rotary_interleaved = 1, int(bool(rotary_interleaved))
+        a.rotary_dim, a.rotary_cache_len = 2 * int(cos_cache.shape[1]), int(cos_cache.shape[0])
+        a.cos_cache, a.sin_cache = _ptr(cos_cache), _ptr(sin_cache)
+        if position_ids is not None:
+            if str(position_ids.dtype) != "torch.int64" or tuple(position_ids.shape) != (int(B), int(S)) \
+                    or not position_ids.is_contiguous():
+                raise ValueError("position_ids: contiguous int64 tensor of shape (B, S)")
+            a.position_ids = _ptr(position_ids)
     return a
 
 

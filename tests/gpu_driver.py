@@ -17,8 +17,12 @@ TOL = {wl.F32: 1e-5, wl.BF16: 2e-2}
 
 class GpuCache:
     def __init__(self, B, Nq, Nkv, D, C, W, dtype, scale=0.0, softcap=0.0, past_key=None, past_value=None,
-                 inplace=True, split_keys=0, head_sink=None, smooth_softmax=False):
+                 inplace=True, split_keys=0, head_sink=None, smooth_softmax=False, cos_cache=None, sin_cache=None,
+                 rotary_interleaved=False):
         self.dev = torch.device("cuda:0")
+        self.cos = None if cos_cache is None else cos_cache.to(self.dev).contiguous()
+        self.sin = None if sin_cache is None else sin_cache.to(self.dev).contiguous()
+        self.rotary_interleaved = rotary_interleaved
         self.head_sink = None if head_sink is None else head_sink.to(self.dev).contiguous()
         self.smooth_softmax = smooth_softmax
         self.B, self.Nq, self.Nkv, self.D, self.C, self.W = B, Nq, Nkv, D, C, W
@@ -32,7 +36,7 @@ class GpuCache:
             self.rk = torch.full_like(self.pk, 7)  # stale rows: must never be read
             self.rv = torch.full_like(self.pv, 7)
 
-    def step(self, q, k, v, seqlens, total=None, bias=None, bias_strides=None, phases=False):
+    def step(self, q, k, v, seqlens, total=None, bias=None, bias_strides=None, phases=False, position_ids=None):
         seqlens = np.asarray(seqlens, np.int64)
         if total is None:
             total = int(seqlens.max()) + 1
@@ -44,7 +48,10 @@ class GpuCache:
         rk, rv = (self.pk, self.pv) if self.inplace else (self.rk, self.rv)
         kw = dict(scale=self.scale, softcap=self.softcap, attention_bias=dbias, bias_strides=bias_strides,
                   resident_len_out=res, split_keys=self.split_keys, head_sink=self.head_sink,
-                  smooth_softmax=self.smooth_softmax)
+                  smooth_softmax=self.smooth_softmax, cos_cache=self.cos, sin_cache=self.sin,
+                  rotary_interleaved=self.rotary_interleaved,
+                  position_ids=None if position_ids is None else
+                  torch.as_tensor(np.asarray(position_ids, np.int64)).to(self.dev).contiguous())
         args = gqaw.make_args(dq, dk, dv, self.pk, self.pv, rk, rv, seq, total, self.Nq, self.Nkv, self.W,
                               out, **kw)
         stream = torch.cuda.current_stream().cuda_stream
@@ -76,10 +83,36 @@ def oracle_dtype(dtype):
     return oracle.F32 if dtype == wl.F32 else oracle.BF16
 
 
-def compare(gpu, ref, dtype, items=None, rows=None, check_layout=True):
+def _values(a, dtype):
+    """Host cache array (float32, or bfloat16 bit patterns) as float64 values."""
+    if dtype == wl.F32:
+        return np.asarray(a, np.float32).astype(np.float64)
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _spacing(x, dtype):
+    """The spacing of the cache dtype's numbers at |x| (normal range)."""
+    s = np.spacing(np.abs(x).astype(np.float32)).astype(np.float64)
+    return s if dtype == wl.F32 else s * 65536.0  # bfloat16 keeps 16 fewer significand bits
+
+
+def keys_close(got, want, dtype):
+    """Turned key rows (rotary embedding): the kernel turns in fp32, the oracle in fp64,
+    each rounds once to the cache dtype.  Allowed: one spacing of the dtype at the
+    oracle's value plus 2^-21 of the row scale (the fp32 error of x1 c - x2 s)."""
+    gw, ww = _values(got, dtype), _values(want, dtype)
+    if gw.size == 0:
+        return True
+    scale = float(np.abs(ww).max())
+    return bool(np.all(np.abs(gw - ww) <= _spacing(ww, dtype) + scale * 2.0 ** -21))
+
+
+def compare(gpu, ref, dtype, items=None, rows=None, check_layout=True, turned_keys=False):
     """Assert parity: resident lengths equal, present rows [0, L_b) bit-exact for the
     given items (all by default), output within TOL relative to the output's scale
-    (max |oracle|) over the given items and token rows.  Returns the output error."""
+    (max |oracle|) over the given items and token rows.  Returns the output error.
+    With ``turned_keys`` (rotary embedding) the present key rows are floating-point
+    results and are held to ``keys_close`` instead of bit equality."""
     B = len(ref["resident_len"])
     items = list(range(B)) if items is None else list(items)
     assert gpu["device_flags"] == 0, "device status 0x%x" % gpu["device_flags"]
@@ -87,7 +120,12 @@ def compare(gpu, ref, dtype, items=None, rows=None, check_layout=True):
         assert gpu["resident_len"][b] == ref["resident_len"][b], (b, gpu["resident_len"][b], ref["resident_len"][b])
         if check_layout:
             n = int(ref["resident_len"][b])
-            assert np.array_equal(gpu["present_key"][b, :, :n], ref["present_key"][b, :, :n]), "present_key item %d" % b
+            if turned_keys:
+                assert keys_close(gpu["present_key"][b, :, :n], ref["present_key"][b, :, :n], dtype), \
+                    "present_key item %d" % b
+            else:
+                assert np.array_equal(gpu["present_key"][b, :, :n], ref["present_key"][b, :, :n]), \
+                    "present_key item %d" % b
             assert np.array_equal(gpu["present_value"][b, :, :n], ref["present_value"][b, :, :n]), "present_value item %d" % b
     got = gpu["output"].float().numpy()[items]
     exp = ref["output_f64"][items]

@@ -112,12 +112,28 @@ def test_workspace_bytes(lib):
     (dict(p_output=FAKE * 16 * 1), 1, "overlaps"),
     (dict(p_attention_bias=FAKE * 300 + 2), 1, "attention_bias"),
     (dict(p_attention_bias=FAKE * 300, p_bias_stride_h=-1), 1, "strides"),
+    (dict(p_head_sink=FAKE * 300 + 2), 1, "head_sink"),
+    (dict(p_do_rotary=1, p_rotary_dim=5, p_rotary_cache_len=8), 1, "rotary_dim"),
+    (dict(p_do_rotary=1, p_rotary_dim=66, p_rotary_cache_len=8), 1, "rotary_dim"),
+    (dict(p_do_rotary=1, p_rotary_cache_len=0), 1, "rotary_cache_len"),
+    (dict(p_do_rotary=1, p_rotary_cache_len=8), 1, "cos_cache and sin_cache"),
+    (dict(p_do_rotary=1, p_rotary_cache_len=8, p_cos_cache=FAKE * 300 + 1, p_sin_cache=FAKE * 301), 1,
+     "2-byte aligned"),
+    (dict(p_do_rotary=1, p_rotary_cache_len=8, p_cos_cache=FAKE * 300, p_sin_cache=FAKE * 301,
+          p_position_ids=FAKE * 302 + 4), 1, "position_ids"),
 ])
 def test_rejected_on_host(lib, over, status, msg):
     a = _args(lib, **over)
     for fn in (lib.gqa_windowed_step, lib.gqaw_attend, lib.gqaw_update_cache):
         assert fn(a, 0) == status
         assert msg in lib.gqaw_last_error(), lib.gqaw_last_error()
+
+
+def test_rotary_workspace(lib):
+    """The turned query and key rows (B*S*(Nq+Nkv)*D elements) live in the workspace."""
+    plain = lib.gqaw_workspace_bytes(_args(lib, sequence_length=4))
+    rot = lib.gqaw_workspace_bytes(_args(lib, sequence_length=4, p_do_rotary=1, p_rotary_cache_len=64))
+    assert rot - plain >= 2 * 4 * (8 + 2) * 64 * 2
 
 
 def test_empty_batch_returns_ok_without_pointers(lib):

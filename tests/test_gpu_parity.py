@@ -33,22 +33,26 @@ class Pair:
     """The same cache driven by the CUDA library and by the oracle."""
 
     def __init__(self, B, Nq, Nkv, D, C, W, dtype, scale=0.0, softcap=0.0, past_key=None, past_value=None,
-                 inplace=True, split_keys=0, head_sink=None, smooth_softmax=False):
+                 inplace=True, split_keys=0, head_sink=None, smooth_softmax=False, cos_cache=None, sin_cache=None,
+                 rotary_interleaved=False):
         self.dtype = dtype
+        self.turned = cos_cache is not None
         self.g = GpuCache(B, Nq, Nkv, D, C, W, dtype, scale, softcap, past_key, past_value, inplace, split_keys,
-                          head_sink, smooth_softmax)
+                          head_sink, smooth_softmax, cos_cache, sin_cache, rotary_interleaved)
         self.o = OracleCache(B, Nq, Nkv, D, C, W, oracle_dtype(dtype), scale, softcap,
                              None if past_key is None else wl.to_numpy(past_key),
                              None if past_value is None else wl.to_numpy(past_value),
-                             None if head_sink is None else wl.to_numpy(head_sink), smooth_softmax)
+                             None if head_sink is None else wl.to_numpy(head_sink), smooth_softmax,
+                             None if cos_cache is None else wl.to_numpy(cos_cache),
+                             None if sin_cache is None else wl.to_numpy(sin_cache), rotary_interleaved)
         self.errs = []
 
-    def step(self, q, k, v, seqlens, total=None, bias=None, bias_strides=None, phases=False):
-        rg = self.g.step(q, k, v, seqlens, total, bias, bias_strides, phases)
+    def step(self, q, k, v, seqlens, total=None, bias=None, bias_strides=None, phases=False, position_ids=None):
+        rg = self.g.step(q, k, v, seqlens, total, bias, bias_strides, phases, position_ids)
         nb = None if bias is None else wl.to_numpy(bias).reshape(-1) if bias_strides else wl.to_numpy(bias)
         ro = self.o.step(wl.to_numpy(q), wl.to_numpy(k), wl.to_numpy(v), np.asarray(seqlens, np.int32), total,
-                         nb, bias_strides)
-        self.errs.append(compare(rg, ro, self.dtype))
+                         nb, bias_strides, position_ids)
+        self.errs.append(compare(rg, ro, self.dtype, turned_keys=self.turned))
         return rg, ro
 
 

@@ -111,6 +111,16 @@ def head_sink(Nq: int, seed: int, mean: float = 0.0, std: float = 2.0) -> torch.
     return draw((Nq,), F32, seed + 400009, "normal", std) + mean
 
 
+def rope_tables(max_pos: int, half: int, dtype: str, base: float = 10000.0):
+    """cos/sin caches (max_pos, half) of the usual rotary angles pos * base^(-i/half),
+    computed in float64 and rounded once to ``dtype``: inputs of the step, as a model
+    would supply them."""
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * base ** (
+        -torch.arange(half, dtype=torch.float64)[None, :] / half)
+    td = TORCH_DTYPE[dtype]
+    return torch.cos(ang).to(td).contiguous(), torch.sin(ang).to(td).contiguous()
+
+
 def lengths(B: int, lo: int, hi: int, seed: int) -> np.ndarray:
     """Per-item token counts T_b ~ U{lo..hi} (inclusive), int64."""
     rng = np.random.Generator(np.random.Philox(seed + 300007))
