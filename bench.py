@@ -186,26 +186,52 @@ class ClockSampler:
 # ------------------------------------------------------------------ profiles (ncu traffic)
 
 
-def kernel_source_hash():
+# The attention kernel a step runs on (the library's dispatch rule), the short name of
+# its profile summaries and the sources that define it.
+KERNELS = {
+    "mmad": ("mma_decode_kernel (tcgen05)", ("gqaw_mmad.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
+    "mma": ("mma_attend_kernel (tcgen05)", ("gqaw_mma.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
+    "attend": ("attend_kernel", ("gqaw_attend.cuh", "gqaw_internal.cuh", "gqaw_attend_bf16.cu", "gqaw_attend_f32.cu")),
+}
+
+
+def attention_kernel(sh, S):
+    g = sh.Nq // sh.Nkv
+    if sh.dtype == "bf16" and sh.D == 128 and S * g <= 32:
+        return "mmad"
+    if sh.dtype == "bf16" and sh.D == 128 and S >= 2 and g <= 32 and 32 % g == 0:
+        return "mma"
+    return "attend"
+
+
+def kernel_source_hash(kernel="mmad"):
     h = hashlib.sha256()
-    for f in ("gqaw_attend.cuh", "gqaw_internal.cuh", "gqaw_attend_bf16.cu", "gqaw_attend_f32.cu"):
+    for f in KERNELS[kernel][1]:
         with open(os.path.join(ROOT, "sliding_window_gqa_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, kernel):
     """DRAM bytes per attention launch from the committed ncu summary of this workload,
-    or None if there is none or the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "attend_%s.md" % workload)
+    or None if there is none or the kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    if not m or not hm or hm.group(1) != kernel_source_hash():
+    if not m or not hm or hm.group(1) != kernel_source_hash(kernel):
         return None
     return float(m.group(1))
+
+
+def check_device(h, what):
+    """A run whose device status word is non-zero (an expired in-kernel wait, a bad
+    seqlens_k) has no valid timing: fail loudly."""
+    st, flags = h.gqaw.gqaw_device_status(int(h.ws.data_ptr()), stream=h.stream.cuda_stream)
+    if flags:
+        raise RuntimeError("%s: device status 0x%x after the timed steps" % (what, flags))
 
 
 def bf16_peak_tflops():
@@ -412,6 +438,7 @@ def run_gpu(args, rank, world):
         t_wall1 = time.time()
         attend_ms = [ev_a[j].elapsed_time(ev_m[j]) for j in range(K)]
     clocks.stop()
+    check_device(h, name)
     total_ms = _max_over_ranks(total_ms, world)
 
     sh, B, S = h.sh, h.B, h.S
@@ -447,8 +474,9 @@ def run_gpu(args, rank, world):
     if attend_ms is not None:
         am = statistics.mean(attend_ms)
         ach = att_bytes / K / (am / 1e3) / 1e9
-        traffic = profiled_traffic(name)
-        result["roofline"] = {"kernel": "attend_kernel", "bound": "hbm", "achieved": ach, "peak": peak,
+        kern = attention_kernel(sh, S)
+        traffic = profiled_traffic(name, kern)
+        result["roofline"] = {"kernel": KERNELS[kern][0], "bound": "hbm", "achieved": ach, "peak": peak,
                               "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
                               "algorithmic_bytes_per_launch": att_bytes / K, "avg_launch_ms": am,
                               "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
@@ -466,6 +494,7 @@ def run_gpu(args, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world)
+    check_device(h, name + " (e2e)")
     result["e2e"] = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h.h2d,
                      "d2h_bytes_per_step": h.d2h, "ms_per_step": e2e_ms / K}
     torch.cuda.set_stream(torch.cuda.default_stream())
@@ -511,6 +540,7 @@ def extra_workloads(main, args):
                 h.step(t)
         e1.record(h.stream)
         torch.cuda.synchronize()
+        check_device(h, name)
         ms = e0.elapsed_time(e1) / K
         _, sb = algorithmic_bytes(h.sh, h.S, h.T[Wm], h.B)
         if h.bias is not None:
@@ -527,7 +557,7 @@ def extra_workloads(main, args):
                     flops += h.sh.Nq * 4 * h.sh.D * min(int(P) + s + 1, h.sh.W)
             entry["tflops"] = flops / (ms / 1e3) / 1e12
             entry["tensor_frac"] = entry["tflops"] / bf16_peak_tflops()
-            entry["kernel"] = "mma_attend_kernel (tcgen05)" if h.sh.dtype == "bf16" and h.sh.D == 128 else "attend_kernel"
+        entry["kernel"] = KERNELS[attention_kernel(h.sh, h.S)][0]
         out[name] = entry
         torch.cuda.synchronize()
         torch.cuda.set_stream(torch.cuda.default_stream())

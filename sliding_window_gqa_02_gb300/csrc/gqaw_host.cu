@@ -28,6 +28,7 @@ int attend_tile_bf16(int D);
 cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream);
 cudaError_t launch_mma(const Params &p, const TcArgs &ta, const TcMaps &maps, int grid, cudaStream_t stream);
 cudaError_t launch_rotary(const Params &p, cudaStream_t stream);
+cudaError_t launch_mmad(const Params &p, const TdArgs &ta, const TdMaps &maps, int max_ctas, cudaStream_t stream);
 }  // namespace gqaw
 
 namespace {
@@ -65,6 +66,9 @@ struct Launch {
   bool tc;                // multi-token step on the tensor-core kernel
   gqaw::TcArgs ta;
   long long tc_grid;
+  bool td;                // small step (S x group <= 32) on the keys-as-M tensor-core kernel
+  gqaw::TdArgs tda;
+  long long td_ctas;
 };
 
 bool head_size_ok(int D) { return D == 8 || D == 16 || D == 32 || D == 64 || D == 128 || D == 256; }
@@ -174,6 +178,29 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     L->off_partials = L->off_tickets + align256((size_t)base * 4);
     L->ws_bytes = L->off_partials;
     if (ns > 1) L->ws_bytes += align256((size_t)L->tc_grid * 128 * gqaw::kTcPartialStride * 4);
+  }
+  // Steps with at most 32 query rows per (item, kv head) -- decode and short verify --
+  // with bf16 caches and head size 128 run on the tensor-core kernel that puts the keys
+  // on the MMA's M dimension: persistent, one CTA per SM, stream-K over (unit, 128-key
+  // tile); partial results of units cut by a CTA range are merged in the kernel.
+  const long long rows_all = (long long)a->batch_size * a->kv_num_heads * a->capacity;
+  L->td = a->dtype == GQAW_BF16 && a->head_size == 128 && (long long)a->sequence_length * L->group <= 32 &&
+          rows_all < 0x7fffffffLL && (long long)a->batch_size * a->sequence_length < 0x7fffffffLL;
+  if (L->td) {
+    L->tc = false;
+    const long long nv = (long long)a->sequence_length * L->group;
+    L->tda.npad = nv <= 16 ? 16 : 32;
+    const long long keys = std::min<long long>(a->local_window_size - 1,
+                                               (long long)a->total_sequence_length - a->sequence_length);
+    L->tda.tpu = (int)std::max(1LL, ceil_div(keys, 128));
+    L->tda.units = (long long)a->batch_size * a->kv_num_heads;
+    const long long vt = L->tda.units * L->tda.tpu;
+    long long ctas = std::min(vt, kSms);
+    if (a->split_keys > 0) ctas = std::max(1LL, std::min(ctas, ceil_div(vt * 128, a->split_keys)));
+    L->td_ctas = ctas;
+    L->off_tickets = L->off_list + align256((size_t)a->batch_size * 4);
+    L->off_partials = L->off_tickets + align256((size_t)L->tda.units * 4);
+    L->ws_bytes = L->off_partials + align256((size_t)ctas * 2 * L->tda.npad * (128 + 2) * 4);
   }
   // Rotary embedding: the turned query and key rows, in the input layouts.
   L->off_qrot = L->off_krot = 0;
@@ -381,12 +408,33 @@ gqaw_status run_mma(const gqaw_step_args *a, const Launch &L, const gqaw::Params
   return GQAW_OK;
 }
 
+gqaw_status run_mmad(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
+  gqaw::TdMaps maps;
+  const cuuint64_t D = 128, BS = (cuuint64_t)a->batch_size * a->sequence_length;
+  const cuuint64_t rows = (cuuint64_t)a->batch_size * a->kv_num_heads * a->capacity;
+  const cuuint64_t q_dims[3] = {D, (cuuint64_t)a->num_heads, BS};
+  const cuuint64_t q_str[2] = {D * 2, (cuuint64_t)a->num_heads * D * 2};
+  const cuuint32_t q_box[3] = {64, (cuuint32_t)L.group, (cuuint32_t)a->sequence_length};
+  const cuuint64_t c_dims[2] = {D, rows};
+  const cuuint64_t c_str[1] = {D * 2};
+  const cuuint32_t c_box[2] = {64, 128};
+  if (!encode_map(&maps.q, p.q, 3, q_dims, q_str, q_box) ||
+      !encode_map(&maps.kc, a->past_key, 2, c_dims, c_str, c_box) ||
+      !encode_map(&maps.vc, a->past_value, 2, c_dims, c_str, c_box))
+    return fail(GQAW_ECUDA, "cuTensorMapEncodeTiled failed for the small-step kernel");
+  const cudaError_t e = gqaw::launch_mmad(p, L.tda, maps, (int)L.td_ctas, st);
+  if (e != cudaSuccess) return cuda_fail(e, "small-step tensor-core kernel launch");
+  g_launches.fetch_add(1);
+  return GQAW_OK;
+}
+
 gqaw_status run_attend(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
   if (L.rot_dim > 0) {
     const cudaError_t e = gqaw::launch_rotary(p, st);
     if (e != cudaSuccess) return cuda_fail(e, "rotary kernel launch");
     g_launches.fetch_add(1);
   }
+  if (L.td) return run_mmad(a, L, p, st);
   if (L.tc) return run_mma(a, L, p, st);
   const cudaError_t e = a->dtype == GQAW_F32 ? gqaw::launch_attend_f32(p, L.gb, (int)L.ctas, st)
                                              : gqaw::launch_attend_bf16(p, L.gb, (int)L.ctas, st);
