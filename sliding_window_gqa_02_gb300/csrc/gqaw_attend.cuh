@@ -164,7 +164,6 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
   }
   __syncthreads();
   pdl_wait();                // the previous kernel (a cache update) has finished
-  pdl_launch_dependents();   // the cache-update kernel may be launched now
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -554,6 +553,7 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
     __syncthreads();  // the merge area is reused by the next unit
   }
 
+  pdl_launch_dependents();  // this CTA's work is done: the cache-update kernel may be launched
   // Drain: no copy may still be landing in shared memory when the CTA exits.
   if (threadIdx.x == 0)
     for (int u2 = issued - NST > 0 ? issued - NST : 0; u2 < issued; ++u2)

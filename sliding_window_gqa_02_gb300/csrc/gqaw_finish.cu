@@ -32,9 +32,14 @@ constexpr int kCopyVecs = 8;  // 16-byte vectors per thread per batch (32 KB per
 
 __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) {
   pdl_wait();                // the attention kernel has finished reading the cache
-  pdl_launch_dependents();   // the next step's attention may be launched now
   const unsigned nmove = *reinterpret_cast<volatile unsigned *>(p.move_count);
-  if (nmove == 0) return;    // nothing registered: nothing to reset either
+  if (nmove == 0) {          // nothing registered: nothing to reset either
+    pdl_launch_dependents(); // the next step's kernels may be launched now
+    return;
+  }
+  // With rows to move, the next step's kernels are let in only when this block is done:
+  // launched early, their CTAs would hold whole SMs (waiting for this grid) that the
+  // copies need.
   const int per_item = p.Nkv * 2 * p.ncg;
   const long long njobs = (long long)nmove * per_item;
   const int rowb = p.rowbytes;
@@ -95,6 +100,8 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) 
           *reinterpret_cast<const uint4 *>(newrows + off + col0 + (e % cvec) * 16);
     }
   }
+
+  pdl_launch_dependents();
 
   // Completion ticket: every block has read move_count above; the last one resets the
   // list so the next step's attention kernel starts from an empty list.

@@ -209,7 +209,10 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 // the stream drains.  pdl_wait() blocks until that previous kernel has completed and
 // its memory is visible; nothing produced upstream may be read before it.
 // pdl_launch_dependents() lets the next kernel in the stream be launched early (its
-// CTAs then wait in their own pdl_wait()).
+// CTAs then wait in their own pdl_wait()).  A kernel signals only when its CTA's main
+// work is done: signalled at the start, the next grid's CTAs become resident as SMs
+// free up, ahead of this grid's CTAs that are not resident yet, and hold those SMs
+// while they wait -- a persistent grid with one CTA per SM then runs partly serialised.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

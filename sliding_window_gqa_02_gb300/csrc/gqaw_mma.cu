@@ -110,7 +110,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_s = tmem, tmem_o = tmem + 2 * kKeys;
   pdl_wait();
-  pdl_launch_dependents();
 
   Plan pl;
   const bool ok = plan_item(p, b, pl);
@@ -441,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // release tensor memory (all tcgen05.ld of this CTA are complete)
   tc::fence_before_sync();
   __syncthreads();
+  pdl_launch_dependents();  // this CTA's work is done: the cache-update kernel may be launched
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);

@@ -27,8 +27,9 @@
 // The cache rows [lo, P) come in tiles of 128 keys by TMA (128-byte swizzle) through a
 // three-stage ring; the S new rows of the step, which live in the input tensors, are
 // added when the unit is finished (their logits and values are read directly), so no
-// tile ever mixes the two sources.  Warp roles: warps 0-3 softmax and epilogue, warp
-// 4 (one thread) the TMA producer, warp 5 (one thread) the MMA issuer; they meet at
+// tile ever mixes the two sources.  Warp roles: four or eight softmax warps (each owning
+// a quarter of the keys and half or all of the query rows), then one warp whose first
+// thread is the TMA producer and one whose first thread issues the MMAs; they meet at
 // mbarriers.  Persistent stream-K over the (unit, key tile) sequence, as in the decode
 // kernel: a unit cut by a CTA range boundary is merged by its last contributor.
 //
@@ -48,8 +49,6 @@ namespace {
 constexpr int kKeys = 128;                 // keys per tile (M of S^T = K Q^T)
 constexpr int kD = 128;                    // head size (M of O^T = V^T P^T)
 constexpr int kHalf = 16384;               // one 64-dim half of a K or V tile
-constexpr int kConsumers = 128;            // warps 0-3
-constexpr int kThreads = 192;              // + producer warp 4, MMA warp 5
 constexpr int kStages = 3;
 constexpr int kStageBytes = 4 * kHalf;     // K and V, two halves each
 constexpr float kRescale = 8.0f;           // lazy rescale threshold (log2 units)
@@ -218,11 +217,16 @@ struct Walker {
 }  // namespace
 
 // NPAD: query rows of the MMA (16 or 32); NVT: query rows the softmax warps process
-// (the unit's S x g rounded up to 4, 8, 16 or 32; rows past S x g are zero).
-template <int NPAD, int NVT>
-__global__ void __launch_bounds__(kThreads, 1)
+// (the unit's S x g rounded up to 4, 8, 16 or 32; rows past S x g are zero); CG: column
+// groups.  4 * CG softmax warps: warps w and w + 4 read the same TMEM lanes (the same
+// keys, the same head dimensions) and own different query rows, NC = NVT / CG each.
+template <int NPAD, int NVT, int CG>
+__global__ void __launch_bounds__(32 * (4 * CG + 2), 1)
     mma_decode_kernel(const Params p, const TdArgs ta, const __grid_constant__ TdMaps maps) {
-  static_assert(NVT <= NPAD, "processed rows within the MMA rows");
+  static_assert(NVT <= NPAD && NVT % CG == 0, "processed rows within the MMA rows");
+  constexpr int NC = NVT / CG;              // query rows per softmax thread
+  constexpr int kSoft = 128 * CG;           // softmax threads
+  constexpr int kProducer = 4 * CG;         // warp of the TMA producer; the MMA issuer is the next
   using L = Lay<NPAD>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -253,21 +257,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kConsumers);
+      mbar_init(&s_free[i], kSoft);
       mbar_init(&q_full[i], 1);
       mbar_init(&q_free[i], 1);
+      mbar_init(&p_full[i], kSoft);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(&p_full[0], kConsumers);
-    mbar_init(&p_full[1], kConsumers);
-    mbar_init(&o_done[0], 1);
-    mbar_init(&o_done[1], 1);
-    mbar_init(o_free, kConsumers);
+    mbar_init(o_free, kSoft);
     mbar_init(mma_done, 1);
     mbar_fence_init();
     s_abort = 0;
   }
   // Q and P^T rows past the unit's query rows stay zero for the whole kernel.
-  for (int e = tid; e < (8 * L::kQHalf) / 16; e += kThreads)
+  for (int e = tid; e < (8 * L::kQHalf) / 16; e += blockDim.x)
     reinterpret_cast<uint4 *>(smem + L::kQ)[e] = make_uint4(0, 0, 0, 0);
   if (warp == 0) tc::tmem_alloc(tmem_slot, L::kCols);
   tc::fence_proxy_async_smem();
@@ -277,13 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_s = tmem, tmem_o = tmem + 2 * NPAD;
   pdl_wait();                // the previous kernel in the stream has completed
-  pdl_launch_dependents();   // the cache-update kernel may be launched now
 
   auto stage = [&](int kc) { return smem + (kc % kStages) * kStageBytes; };
   auto qbuf = [&](int ui) { return smem + L::kQ + (ui & 1) * 2 * L::kQHalf; };
   auto pbuf = [&](int kc) { return smem + L::kP + (kc & 1) * 2 * L::kQHalf; };
 
-  if (warp == 4) {
+  if (warp == kProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first(), qpol = tc::policy_evict_last();
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = qissued - 1 > 0 ? qissued - 1 : 0; q <= qissued; ++q)
         if (q >= 0 && !mbar_wait(&q_full[q & 1], (q >> 1) & 1)) flag(p, GQAW_DEV_TIMEOUT);
     }
-  } else if (warp == 5) {
+  } else if (warp == kProducer + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kKeys, NPAD, 0, 0);  // K: K-major, Q: K-major
@@ -386,13 +387,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(mma_done, 0)) flag(p, GQAW_DEV_TIMEOUT);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps 0-3
-    const int t = tid;  // key of a tile (S^T lane) and head dimension (O^T lane)
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax warps
+    const int t = tid & 127;       // key of a tile (S^T lane) and head dimension (O^T lane)
+    const int col0 = (tid >> 7) * NC;  // first query row of this thread's column group
+    const int wq = warp & 3;       // TMEM lane quarter
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
     const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(p.q);
     const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(p.k);
     const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(p.v);
+    const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
     int kc = 0, ui = 0;
     bool stop = false;
     for (long long u = ufirst; u <= ulast && !stop; ++u) {
@@ -400,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long lt0 = tb - u * TPU > 0 ? tb - u * TPU : 0;
       const long long lt1 = te - u * TPU < TPU ? te - u * TPU : TPU;
       if (!x.ok) {  // every CTA touching the unit skips it: no ticket, no output
-        if (lt0 == 0 && x.kvh == 0 && t == 0) flag(p, GQAW_DEV_BAD_SEQLEN);
+        if (lt0 == 0 && x.kvh == 0 && tid == 0) flag(p, GQAW_DEV_BAD_SEQLEN);
         continue;
       }
       const int r1 = (int)(lt1 < x.real ? lt1 : x.real);
@@ -409,12 +413,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool has_fix = lt0 <= fx && fx < lt1;
       const bool moves = item_moves(p, x.pl);
       const long long P = x.pl.P;
-      if (lt0 == 0 && x.kvh == 0 && t == 0) {
+      if (lt0 == 0 && x.kvh == 0 && tid == 0) {
         if (p.resident_out) p.resident_out[x.b] = (int32_t)x.pl.Lt;
         if (moves) p.move_list[atomicAdd(p.move_count, 1u)] = x.b;
       }
       if (has_fix && !moves) {  // append the new rows at L(P) + s: no query of this step reads them
-        for (int e = t; e < 2 * S * 16; e += kConsumers) {
+        for (int e = tid; e < 2 * S * 16; e += kSoft) {
           const int tensor = e / (S * 16), rem = e % (S * 16), s = rem / 16, vec = rem % 16;
           const size_t in_row = ((size_t)x.b * S + s) * p.Nkv + x.kvh;
           const size_t out_row = ((size_t)x.b * p.Nkv + x.kvh) * (size_t)p.C + (size_t)(x.pl.Lp + s);
@@ -422,22 +426,31 @@ __global__ void __launch_bounds__(kThreads, 1)
               reinterpret_cast<const uint4 *>(static_cast<const char *>(tensor ? p.v : p.k) + in_row * kD * 2)[vec];
         }
       }
-      for (int n = t; n < NVT; n += kConsumers)
-        brow[n] = (n < NV && p.bias) ? (long long)x.b * p.bsb + (long long)(x.kvh * g + n % g) * p.bsh +
-                                           (long long)(n / g) * p.bss
-                                     : 0;
-      named_barrier(kBar, kConsumers);
+      for (int n = tid; n < NVT; n += kSoft)  // rows past S x g: the item's first bias row
+        brow[n] = !p.bias ? 0
+                          : (long long)x.b * p.bsb +
+                                (n < NV ? (long long)(x.kvh * g + n % g) * p.bsh + (long long)(n / g) * p.bss : 0);
+      named_barrier(kBar, kSoft);
 
-      // per query row: the reference maximum (uniform over the CTA), its finite stand-in
-      // for exp2, and this thread's share of the softmax denominator
-      float m_ref[NVT], mb[NVT], lsum[NVT];
+      // per query row of this thread: the reference maximum (uniform over the CTA) and
+      // this thread's share of the softmax denominator
+      float m_ref[NC], lsum[NC];
 #pragma unroll
-      for (int n = 0; n < NVT; ++n) {
-        m_ref[n] = -INFINITY;
-        mb[n] = 0.f;
-        lsum[n] = 0.f;
+      for (int i = 0; i < NC; ++i) {
+        m_ref[i] = -INFINITY;
+        lsum[i] = 0.f;
       }
-      const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
+      // Bias of this thread's key for its rows, fetched one tile ahead.  Keys past P read
+      // a column that exists (P - 1): their logits are masked anyway.
+      float bnext[NC];
+      auto fetch_bias = [&](int lt_) {
+        const long long j0_ = x.lo + (long long)lt_ * kKeys;
+        const int nv_ = (int)(P - j0_ < kKeys ? P - j0_ : kKeys);
+        const long long col = j0_ + (t < nv_ ? t : nv_ - 1);
+#pragma unroll
+        for (int i = 0; i < NC; ++i) bnext[i] = __ldg(p.bias + brow[col0 + i] + col);
+      };
+      if (p.bias && nt > 0) fetch_bias((int)lt0);
       for (int lt = (int)lt0; lt < r1; ++lt, ++kc) {
         const long long j0 = x.lo + (long long)lt * kKeys;
         const int nvalid = (int)(P - j0 < kKeys ? P - j0 : kKeys);
@@ -445,34 +458,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         // t >= P + s - W + 1 - j0; rows are token-major, so the rows that see key t are
         // n < nlim.
         const int wbase = (int)(P - p.W + 1 - j0);  // <= 0
-        const int nlim = t < nvalid ? min(t - wbase + 1, S) * g : 0;
+        const int nlim = (t < nvalid ? min(t - wbase + 1, S) * g : 0) - col0;
+        float bv[NC];
+        if (p.bias) {
+#pragma unroll
+          for (int i = 0; i < NC; ++i) bv[i] = bnext[i];
+          if (lt + 1 < r1) fetch_bias(lt + 1);
+        }
         bool ok = mbar_wait(&s_full[kc & 1], (kc >> 1) & 1);
         tc::fence_after_sync();
-        float z[NVT];
-        tmem_ld<NVT>(tmem_s + (kc & 1) * NPAD + lane_off, z);
+        float z[NC];
+        tmem_ld<NC>(tmem_s + (kc & 1) * NPAD + col0 + lane_off, z);
         tc::fence_before_sync();
         mbar_arrive(&s_free[kc & 1]);
         bool exceed = false;
         if (plain) {
 #pragma unroll
-          for (int n = 0; n < NVT; ++n) {
-            z[n] = n < nlim ? z[n] * p.qscale : -INFINITY;
-            exceed |= z[n] > m_ref[n] + kRescale;
+          for (int i = 0; i < NC; ++i) {
+            z[i] = i < nlim ? z[i] * p.qscale : -INFINITY;
+            exceed |= z[i] > m_ref[i] + kRescale;
           }
         } else {
 #pragma unroll
-          for (int n = 0; n < NVT; ++n) {
-            float v = z[n] * p.qscale;
+          for (int i = 0; i < NC; ++i) {
+            float v = z[i] * p.qscale;
             if (p.capmul != 0.f) v = p.capmul * fast_tanh(v);
-            if (p.bias && n < nlim) v = fmaf(p.biasmul, p.bias[brow[n] + j0 + t], v);
-            z[n] = n < nlim ? v : -INFINITY;
-            exceed |= z[n] > m_ref[n] + kRescale;
+            if (p.bias) v = fmaf(p.biasmul, bv[i], v);
+            z[i] = i < nlim ? v : -INFINITY;
+            exceed |= z[i] > m_ref[i] + kRescale;
           }
         }
         // one vote per tile: a logit above its row's reference, or a wait that expired
         const bool fail = !ok || *reinterpret_cast<volatile int *>(&s_abort);
-        const bool any = named_barrier_or(kBar, kConsumers, exceed || fail);
-        if (any && named_barrier_or(kBar, kConsumers, fail)) {
+        const bool any = named_barrier_or(kBar, kSoft, exceed || fail);
+        if (any && named_barrier_or(kBar, kSoft, fail)) {
           stop = true;
           break;
         }
@@ -481,35 +500,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         if (any) {
 #pragma unroll
-          for (int n = 0; n < NVT; ++n) {
-            float mx = z[n];
+          for (int i = 0; i < NC; ++i) {
+            float mx = z[i];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) red[warp * NPAD + n] = mx;
+            if (lane == 0) red[wq * NPAD + col0 + i] = mx;
           }
-          named_barrier(kBar, kConsumers);
-          float alpha[NVT];
+          named_barrier(kBar, kSoft);
+          float alpha[NC];
           bool resc = false;
 #pragma unroll
-          for (int n = 0; n < NVT; ++n) {
+          for (int i = 0; i < NC; ++i) {
+            const int n = col0 + i;
             const float mt = fmaxf(fmaxf(red[n], red[NPAD + n]), fmaxf(red[2 * NPAD + n], red[3 * NPAD + n]));
-            alpha[n] = 1.f;
-            if (mt > m_ref[n] + kRescale) {
-              alpha[n] = m_ref[n] == -INFINITY ? 0.f : fast_exp2(m_ref[n] - mt);
-              m_ref[n] = mt;
-              mb[n] = mt;
-              lsum[n] *= alpha[n];
+            alpha[i] = 1.f;
+            if (mt > m_ref[i] + kRescale) {
+              alpha[i] = m_ref[i] == -INFINITY ? 0.f : fast_exp2(m_ref[i] - mt);
+              m_ref[i] = mt;
+              lsum[i] *= alpha[i];
               resc = true;
             }
           }
-          if (resc && lt > (int)lt0) {  // O^T holds earlier tiles of this unit: rescale its columns
+          // O^T holds earlier tiles of this unit: rescale this group's columns (the
+          // decision is per column group, uniform within the group's warps)
+          if (resc && lt > (int)lt0) {
             if (!mbar_wait(&o_done[(kc - 1) & 1], ((kc - 1) >> 1) & 1)) ok = false;
             tc::fence_after_sync();
-            float o[NVT];
-            tmem_ld<NVT>(tmem_o + lane_off, o);
+            float o[NC];
+            tmem_ld<NC>(tmem_o + col0 + lane_off, o);
 #pragma unroll
-            for (int n = 0; n < NVT; ++n) o[n] *= alpha[n];
-            tmem_st<NVT>(tmem_o + lane_off, o);
+            for (int i = 0; i < NC; ++i) o[i] *= alpha[i];
+            tmem_st<NC>(tmem_o + col0 + lane_off, o);
           }
         }
         // probabilities (bf16) into P^T: row n, key t, 128-byte swizzled K-major
@@ -517,10 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int half = t >> 6, c = (t & 63) >> 3;
           unsigned char *pb = pbuf(kc) + half * L::kQHalf + (t & 7) * 2;
 #pragma unroll
-          for (int n = 0; n < NVT; ++n) {
+          for (int i = 0; i < NC; ++i) {
+            const int n = col0 + i;
             if (n < NV) {
-              const float pr = fast_exp2(z[n] - mb[n]);
-              lsum[n] += pr;
+              const float pr = fast_exp2(z[i] - (m_ref[i] == -INFINITY ? 0.f : m_ref[i]));
+              lsum[i] += pr;
               *reinterpret_cast<__nv_bfloat16 *>(pb + n * 128 + ((c ^ (n & 7)) << 4)) = __float2bfloat16_rn(pr);
             }
           }
@@ -529,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nvalid < kKeys) {
           if (!mbar_wait(&full[kc % kStages], (kc / kStages) & 1)) ok = false;
           unsigned char *vb = stage(kc) + 2 * kHalf;
-          for (int e = t; e < (kKeys - nvalid) * 16; e += kConsumers) {
+          for (int e = tid; e < (kKeys - nvalid) * 16; e += kSoft) {
             const int row = nvalid + e / 16, part = e % 16;
             *reinterpret_cast<uint4 *>(vb + (part / 8) * kHalf + row * 128 + (part % 8) * 16) = make_uint4(0, 0, 0, 0);
           }
@@ -543,27 +565,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&p_full[kc & 1]);
       }
       if (stop) break;
-      named_barrier(kBar, kConsumers);  // every thread is done with the last tile's maxima in red
+      named_barrier(kBar, kSoft);  // every thread is done with the last tile's maxima in red
 
       // ---- the unit's state in this CTA: O^T (TMEM), reference maxima, sums
       bool ok = true;
       if (nt > 0) ok = mbar_wait(&o_done[(kc - 1) & 1], ((kc - 1) >> 1) & 1);
       tc::fence_after_sync();
 #pragma unroll
-      for (int n = 0; n < NVT; ++n) {
-        float v = lsum[n];
+      for (int i = 0; i < NC; ++i) {
+        float v = lsum[i];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[warp * NPAD + n] = v;
-        if (t == 0) fin_m[n] = m_ref[n];
+        if (lane == 0) red[wq * NPAD + col0 + i] = v;
+        if (t == 0) fin_m[col0 + i] = m_ref[i];
       }
-      if (named_barrier_or(kBar, kConsumers, !ok)) {
+      if (named_barrier_or(kBar, kSoft, !ok)) {
         flag(p, GQAW_DEV_TIMEOUT);
         break;
       }
       if (has_fix) {
         // logits of the S new keys (the step's own rows) for every query row
-        for (int e = t; e < NV * S; e += kConsumers) {
+        for (int e = tid; e < NV * S; e += kSoft) {
           const int n = e / S, s2 = e % S, sn = n / g;
           const int h = x.kvh * g + n % g;
           float zz = -INFINITY;
@@ -571,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 *qr = reinterpret_cast<const uint4 *>(qin + (((size_t)x.b * S + sn) * p.Nq + h) * kD);
             const uint4 *kr = reinterpret_cast<const uint4 *>(kin + (((size_t)x.b * S + s2) * p.Nkv + x.kvh) * kD);
             float dot = 0.f;
-#pragma unroll 4
+#pragma unroll 8
             for (int vv = 0; vv < kD / 8; ++vv) {
               float qa[8], ka[8];
               Elem<__nv_bfloat16>::unpack(qr[vv], qa);
@@ -585,8 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           zn[n * NPAD + s2] = zz;
         }
-        named_barrier(kBar, kConsumers);
-        for (int n = t; n < NV; n += kConsumers) {
+        named_barrier(kBar, kSoft);
+        for (int n = tid; n < NV; n += kSoft) {
           const float m0 = fin_m[n];
           float mn = m0;
           for (int s2 = 0; s2 < S; ++s2) mn = fmaxf(mn, zn[n * NPAD + s2]);
@@ -602,92 +624,122 @@ __global__ void __launch_bounds__(kThreads, 1)
           fin_f[n] = f;
         }
       } else {
-        for (int n = t; n < NV; n += kConsumers) {
+        for (int n = tid; n < NV; n += kSoft) {
           fin_l[n] = red[n] + red[NPAD + n] + red[2 * NPAD + n] + red[3 * NPAD + n];
           fin_f[n] = 1.f;
         }
       }
-      named_barrier(kBar, kConsumers);
+      named_barrier(kBar, kSoft);
 
-      // ---- this thread's head dimension d = t of every query row
-      float o[NVT];
+      // ---- this thread's head dimension d = t of its query rows
+      float o[NC];
       if (nt > 0) {
-        tmem_ld<NVT>(tmem_o + lane_off, o);
+        tmem_ld<NC>(tmem_o + col0 + lane_off, o);
         tc::fence_before_sync();
         mbar_arrive(o_free);  // O^T may be overwritten by the next unit
         ++ui;
       } else {
 #pragma unroll
-        for (int n = 0; n < NVT; ++n) o[n] = 0.f;
+        for (int i = 0; i < NC; ++i) o[i] = 0.f;
       }
 #pragma unroll
-      for (int n = 0; n < NVT; ++n) {
-        if (n < NV) {
-          float acc = o[n] * fin_f[n];
-          if (has_fix)
-            for (int s2 = 0; s2 < S; ++s2) {
-              const float pz = zn[n * NPAD + s2];
-              if (pz != 0.f)
-                acc = fmaf(pz, __bfloat162float(vin[(((size_t)x.b * S + s2) * p.Nkv + x.kvh) * kD + t]), acc);
+      for (int i = 0; i < NC; ++i) o[i] *= col0 + i < NV ? fin_f[col0 + i] : 0.f;
+      if (has_fix) {
+        // the step's own value rows, dimension t, eight rows per batch of independent loads
+        const __nv_bfloat16 *vcol = vin + ((size_t)x.b * S * p.Nkv + x.kvh) * kD + t;
+        for (int s0 = 0; s0 < S; s0 += 8) {
+          float vv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            vv[j] = s0 + j < S ? __bfloat162float(vcol[(size_t)(s0 + j) * p.Nkv * kD]) : 0.f;
+#pragma unroll
+          for (int i = 0; i < NC; ++i) {
+            const int n = col0 + i;
+            if (n < NV) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (s0 + j < S) o[i] = fmaf(zn[n * NPAD + s0 + j], vv[j], o[i]);
             }
-          o[n] = acc;
+          }
         }
       }
       const long long cf = owner_cta(u * TPU, V, G), cl = owner_cta(u * TPU + TPU - 1, V, G);
       if (cf == cl) {
 #pragma unroll
-        for (int n = 0; n < NVT; ++n) {
+        for (int i = 0; i < NC; ++i) {
+          const int n = col0 + i;
           if (n < NV) {
             const int h = x.kvh * g + n % g;
             const size_t orow = ((size_t)x.b * S + n / g) * p.Nq + h;
-            out[orow * kD + t] = __float2bfloat16_rn(sink_divide(o[n], fin_l[n], fin_m[n], sink_log2(p, h)));
+            out[orow * kD + t] = __float2bfloat16_rn(sink_divide(o[i], fin_l[n], fin_m[n], sink_log2(p, h)));
           }
         }
       } else {
         const int slot = u == ufirst ? 0 : 1;  // only a CTA's first and last unit can be shared
 #pragma unroll
-        for (int n = 0; n < NVT; ++n) {
+        for (int i = 0; i < NC; ++i) {
+          const int n = col0 + i;
           if (n < NV) {
             float *part = p.partials + ((cta * 2 + slot) * NPAD + n) * (kD + 2);
-            part[t] = o[n];
+            part[t] = o[i];
             if (t == 0) {
               part[kD] = fin_m[n];
               part[kD + 1] = fin_l[n];
             }
           }
         }
-        named_barrier(kBar, kConsumers);
-        if (t == 0) {
+        named_barrier(kBar, kSoft);
+        if (tid == 0) {
           __threadfence();
           s_last = atomicAdd(&p.tickets[u], 1u) == (unsigned)(cl - cf);
         }
-        named_barrier(kBar, kConsumers);
+        named_barrier(kBar, kSoft);
         if (s_last) {
+          // merge the contributors' partial states, all of this thread's rows at once
+          // (independent loads: one round trip per contributor, not one per row)
           __threadfence();
-          for (int n = 0; n < NV; ++n) {
-            float M = -INFINITY;
-            for (long long c = cf; c <= cl; ++c) {
-              const int sl = u == c * V / G / TPU ? 0 : 1;
-              M = fmaxf(M, __ldcg(p.partials + ((c * 2 + sl) * NPAD + n) * (kD + 2) + kD));
-            }
-            float Lsum = 0.f, A = 0.f;
-            for (long long c = cf; c <= cl; ++c) {
-              const int sl = u == c * V / G / TPU ? 0 : 1;
-              const float *part = p.partials + ((c * 2 + sl) * NPAD + n) * (kD + 2);
-              const float mc = __ldcg(part + kD);
-              if (mc == -INFINITY) continue;  // contributor held no visible key
-              const float f = exp2f(mc - M);
-              Lsum = fmaf(f, __ldcg(part + kD + 1), Lsum);
-              A = fmaf(f, __ldcg(part + t), A);
-            }
-            const int h = x.kvh * g + n % g;
-            const size_t orow = ((size_t)x.b * S + n / g) * p.Nq + h;
-            out[orow * kD + t] = __float2bfloat16_rn(sink_divide(A, Lsum, M, sink_log2(p, h)));
+          float M[NC], Lsum[NC], A[NC];
+#pragma unroll
+          for (int i = 0; i < NC; ++i) {
+            M[i] = -INFINITY;
+            Lsum[i] = 0.f;
+            A[i] = 0.f;
           }
-          if (t == 0) p.tickets[u] = 0u;  // ready for the next step
+          for (long long c = cf; c <= cl; ++c) {
+            const int sl = u == c * V / G / TPU ? 0 : 1;
+            const float *part = p.partials + ((c * 2 + sl) * NPAD + col0) * (kD + 2);
+#pragma unroll
+            for (int i = 0; i < NC; ++i)
+              if (col0 + i < NV) M[i] = fmaxf(M[i], __ldcg(part + i * (kD + 2) + kD));
+          }
+          for (long long c = cf; c <= cl; ++c) {
+            const int sl = u == c * V / G / TPU ? 0 : 1;
+            const float *part = p.partials + ((c * 2 + sl) * NPAD + col0) * (kD + 2);
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+              if (col0 + i < NV) {
+                const float mc = __ldcg(part + i * (kD + 2) + kD);
+                const float lc = __ldcg(part + i * (kD + 2) + kD + 1);
+                const float ac = __ldcg(part + i * (kD + 2) + t);
+                const float f = mc == -INFINITY ? 0.f : exp2f(mc - M[i]);  // -inf: no visible key
+                Lsum[i] = fmaf(f, lc, Lsum[i]);
+                A[i] = fmaf(f, ac, A[i]);
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NC; ++i) {
+            const int n = col0 + i;
+            if (n < NV) {
+              const int h = x.kvh * g + n % g;
+              const size_t orow = ((size_t)x.b * S + n / g) * p.Nq + h;
+              out[orow * kD + t] = __float2bfloat16_rn(sink_divide(A[i], Lsum[i], M[i], sink_log2(p, h)));
+            }
+          }
+          if (tid == 0) p.tickets[u] = 0u;  // ready for the next step
         }
       }
-      named_barrier(kBar, kConsumers);  // scratch (fin, zn, brow) is reused by the next unit
+      named_barrier(kBar, kSoft);  // scratch (fin, zn, brow) is reused by the next unit
     }
     if (stop) flag(p, GQAW_DEV_TIMEOUT);
   }
@@ -696,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the softmax warps is complete (their loads wait in the same statement)
   tc::fence_before_sync();
   __syncthreads();
+  pdl_launch_dependents();  // every role of this CTA is done: the cache update may be launched
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, L::kCols);
@@ -710,13 +763,13 @@ cudaError_t launch_mmad(const Params &p, const TdArgs &ta, const TdMaps &maps, i
   if (e != cudaSuccess) return e;
   int sms = dev < kMaxDevices ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
   if (sms <= 0) {
-    e = cudaFuncSetAttribute(mma_decode_kernel<16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
+    e = cudaFuncSetAttribute(mma_decode_kernel<16, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mma_decode_kernel<16, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
+    e = cudaFuncSetAttribute(mma_decode_kernel<16, 8, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mma_decode_kernel<16, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
+    e = cudaFuncSetAttribute(mma_decode_kernel<16, 16, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mma_decode_kernel<32, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<32>::kAlloc);
+    e = cudaFuncSetAttribute(mma_decode_kernel<32, 32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<32>::kAlloc);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -725,25 +778,26 @@ cudaError_t launch_mmad(const Params &p, const TdArgs &ta, const TdMaps &maps, i
   const long long V = ta.units * ta.tpu;
   long long grid = max_ctas < sms ? max_ctas : sms;  // one CTA per SM: a persistent grid
   if (grid > V) grid = V;
+  const int nv = p.S * p.group;
+  const int cg = nv <= 4 ? 1 : 2;  // softmax warps: 4 per column group
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(32 * (4 * cg + 2));
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait()
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int nv = p.S * p.group;
   cfg.dynamicSmemBytes = nv <= 16 ? Lay<16>::kAlloc : Lay<32>::kAlloc;
   if (nv <= 4)
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4>, p, ta, maps);
+    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4, 1>, p, ta, maps);
   else if (nv <= 8)
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 8>, p, ta, maps);
+    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 8, 2>, p, ta, maps);
   else if (nv <= 16)
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 16>, p, ta, maps);
+    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 16, 2>, p, ta, maps);
   else
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<32, 32>, p, ta, maps);
+    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<32, 32, 2>, p, ta, maps);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

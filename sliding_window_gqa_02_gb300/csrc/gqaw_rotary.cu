@@ -31,7 +31,6 @@ constexpr int kMaxRotaryDevices = 64;
 template <typename T>
 __global__ void __launch_bounds__(kRotaryThreads) rotary_kernel(const Params p) {
   pdl_wait();               // the previous step's cache update has read these buffers
-  pdl_launch_dependents();  // the attention kernel may be scheduled; it waits for us
   const int D = p.D, half = p.rot_dim / 2, slots = D / 2;
   const long long qrows = (long long)p.B * p.S * p.Nq;
   const long long rows = qrows + (long long)p.B * p.S * p.Nkv;
@@ -72,6 +71,7 @@ __global__ void __launch_bounds__(kRotaryThreads) rotary_kernel(const Params p) 
     y[i1] = Elem<T>::store(y1);
     y[i2] = Elem<T>::store(y2);
   }
+  pdl_launch_dependents();  // done: the attention kernel may be scheduled
 }
 
 // 16-byte vectors of T: unpack to floats (Elem<T>::unpack) and pack back, rounding once.
@@ -108,7 +108,6 @@ template <typename T>
 __global__ void __launch_bounds__(kRotaryThreads) rotary_vec_kernel(const Params p) {
   constexpr int VEC = Elem<T>::kPerVec;
   pdl_wait();               // the previous step's cache update has read these buffers
-  pdl_launch_dependents();  // the attention kernel may be scheduled; it waits for us
   const unsigned D = p.D, half = p.rot_dim / 2;
   const unsigned pitems = p.rot_inter ? p.rot_dim / VEC : half / VEC;
   const unsigned ipr = pitems + (D - p.rot_dim) / VEC;
@@ -163,6 +162,7 @@ __global__ void __launch_bounds__(kRotaryThreads) rotary_vec_kernel(const Params
       *reinterpret_cast<uint4 *>(y + c + half) = pack_vec(o2, T());
     }
   }
+  pdl_launch_dependents();  // done: the attention kernel may be scheduled
 }
 
 template <typename K>
