@@ -31,6 +31,8 @@ _LIB = os.path.join(_HERE, "liboracle_gqaw.%s.so" % platform.machine())
 
 F32 = 0
 BF16 = 1
+I8 = 2      # quantized cache: int8 codes
+E4M3 = 3    # quantized cache: fp8 e4m3 codes
 
 _ERRORS = {
     1: "malformed sizes",
@@ -80,6 +82,9 @@ class _Args(ctypes.Structure):
         ("cos_cache", ctypes.c_void_p),
         ("sin_cache", ctypes.c_void_p),
         ("position_ids", ctypes.c_void_p),
+        ("cache_dtype", ctypes.c_int64),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 
@@ -109,6 +114,12 @@ def _load():
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.oracle_step.restype = ctypes.c_int
         lib.oracle_step.argtypes = [ctypes.POINTER(_Args)]
+        lib.oracle_decode_e4m3.restype = ctypes.c_double
+        lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+        lib.oracle_round_e4m3.restype = ctypes.c_uint8
+        lib.oracle_round_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_quantize.restype = ctypes.c_uint8
+        lib.oracle_quantize.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int64]
         _lib = lib
     return _lib
 
@@ -124,6 +135,21 @@ def round_bf16(x: float) -> int:
     return int(_load().oracle_round_bf16(float(x)))
 
 
+def decode_e4m3(code: int) -> float:
+    """The value of an fp8 e4m3 code (OCP 8-bit floating point, E4M3FN)."""
+    return float(_load().oracle_decode_e4m3(int(code) & 0xFF))
+
+
+def round_e4m3(x: float) -> int:
+    """The e4m3 code nearest to float32 x, ties to even, saturated to +-448."""
+    return int(_load().oracle_round_e4m3(float(x)))
+
+
+def quantize(x: float, scale: float, cache_dtype: int) -> int:
+    """The quantized-cache code (a byte) of x: x / scale in float, rounded, saturated."""
+    return int(_load().oracle_quantize(float(x), float(scale), int(cache_dtype)))
+
+
 def _ptr(a):
     return None if a is None else a.ctypes.data
 
@@ -135,7 +161,8 @@ def _elem_dtype(dtype: int):
 def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_length,
          num_heads, kv_num_heads, local_window_size, scale=0.0, softcap=0.0,
          attention_bias=None, bias_strides=None, dtype=F32, rows=None, head_sink=None, smooth_softmax=0,
-         cos_cache=None, sin_cache=None, position_ids=None, rotary_interleaved=False):
+         cos_cache=None, sin_cache=None, position_ids=None, rotary_interleaved=False,
+         cache_dtype=None, k_scale=1.0, v_scale=1.0):
     """One windowed GQA step on host arrays.
 
     Arrays are numpy: float32 for ``dtype=F32``; uint16 bfloat16 bit patterns for
@@ -154,14 +181,17 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
     ``cos_cache``/``sin_cache`` ((max_pos, rd/2) in the step's dtype) turn on the rotary
     embedding of the new query and key rows; ``position_ids`` (int64 (B, S)) overrides
     the positions P_b + s; ``rotary_interleaved`` pairs dimensions (2i, 2i+1).
+    ``cache_dtype`` (I8 or E4M3) makes the caches quantized: past/present are uint8 code
+    arrays and ``k_scale``/``v_scale`` their per-tensor scales.
     """
     lib = _load()
     et = _elem_dtype(dtype)
     query = np.ascontiguousarray(query, dtype=et)
     key = np.ascontiguousarray(key, dtype=et)
     value = np.ascontiguousarray(value, dtype=et)
-    past_key = np.ascontiguousarray(past_key, dtype=et)
-    past_value = np.ascontiguousarray(past_value, dtype=et)
+    ct = np.uint8 if cache_dtype else et
+    past_key = np.ascontiguousarray(past_key, dtype=ct)
+    past_value = np.ascontiguousarray(past_value, dtype=ct)
     seqlens_k = np.ascontiguousarray(seqlens_k, dtype=np.int32)
     if head_sink is not None:
         head_sink = np.ascontiguousarray(head_sink, dtype=np.float32)
@@ -219,6 +249,7 @@ def step(query, key, value, past_key, past_value, seqlens_k, total_sequence_leng
         rotary_cache_len=cos_cache.shape[0] if do_rotary else 0,
         cos_cache=_ptr(cos_cache), sin_cache=_ptr(sin_cache),
         position_ids=_ptr(position_ids) if do_rotary else None,
+        cache_dtype=int(cache_dtype or 0), k_scale=float(k_scale), v_scale=float(v_scale),
     )
     rc = lib.oracle_step(ctypes.byref(a))
     if rc != 0:

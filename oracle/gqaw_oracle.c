@@ -45,7 +45,16 @@
  *    through.  pos = position_ids[b, s] if given, else the absolute position P_b + s.
  *    The new query and key rows of the step are turned before use; the turned key
  *    rows are what the cache stores (rounded once to the cache dtype), the turned
- *    query stays in double.  Values are not turned.
+ *    query stays in double.  Values are not turned;
+ *  - quantized cache ([P3] Part 1.1 inputs k_scale and v_scale, "KV cache quantization
+ *    scale", named only): the caches hold int8 or fp8 e4m3 codes, one scale per tensor;
+ *    a code c stands for c * scale.  The step's new key and value rows (turned and
+ *    rounded to the step's dtype first, if rotary) are quantized once: x / scale in
+ *    float (one IEEE division: the code is an integer decision, taken in the kernel's
+ *    precision), rounded to nearest even and saturated to the type (int8 [-128, 127];
+ *    e4m3 per the OCP 8-bit floating-point format, finite values up to 448, NaN kept).
+ *    The cache stores the codes and attention reads every key and value, new ones
+ *    included, as code * scale.
  *
  * Precision: every input element is widened exactly to double; dot products,
  * softcap, softmax and the weighted sum are evaluated in double in ascending key
@@ -56,7 +65,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_I8 = 2, ORACLE_E4M3 = 3 };
 
 enum {
   ORACLE_OK = 0,
@@ -104,6 +113,8 @@ typedef struct oracle_args {
   const void *cos_cache;     /* (rotary_cache_len, rd/2) in dtype */
   const void *sin_cache;     /* (rotary_cache_len, rd/2) in dtype */
   const int64_t *position_ids; /* NULL or (B, S) */
+  int64_t cache_dtype;       /* 0: the caches hold dtype; ORACLE_I8 or ORACLE_E4M3: codes */
+  float k_scale, v_scale;    /* scales of the quantized caches */
 } oracle_args;
 
 /* [P1] Description, resident-count formula:
@@ -140,6 +151,49 @@ uint16_t oracle_round_bf16(double x) {
   return (uint16_t)(sign | (bits >> 16));
 }
 
+/* fp8 e4m3 (OCP 8-bit floating point, "E4M3FN"): sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; exponent 0 holds subnormals m * 2^-9; S.1111.111 is NaN; no
+ * infinities; the largest finite value is 1.75 * 2^8 = 448. */
+double oracle_decode_e4m3(uint8_t c) {
+  const double sign = (c & 0x80) ? -1.0 : 1.0;
+  const int e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) return sign * ldexp((double)m, -9);
+  return sign * ldexp(1.0 + m / 8.0, e - 7);
+}
+
+/* The e4m3 code nearest to x (ties to even), saturated to +-448; NaN gives NaN. */
+uint8_t oracle_round_e4m3(float x) {
+  const uint8_t sign = signbit(x) ? 0x80 : 0;
+  const double a = fabs((double)x);
+  int e, r;
+  if (isnan(x)) return (uint8_t)(sign | 0x7F);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  if (a < ldexp(1.0, -6)) {                    /* subnormal range: steps of 2^-9 */
+    r = (int)nearbyint(ldexp(a, 9));           /* 0 .. 8, ties to even */
+    return (uint8_t)(sign | r);                /* r == 8 is the smallest normal, code 0x08 */
+  }
+  frexp(a, &e);                                /* a = f * 2^e, f in [0.5, 1) */
+  e -= 1;                                      /* a = (1 + t) * 2^e, t in [0, 1) */
+  r = (int)nearbyint((ldexp(a, -e) - 1.0) * 8.0); /* 0 .. 8, ties to even */
+  if (r == 8) {
+    r = 0;
+    e += 1;
+  }
+  if (e + 7 > 15 || (e + 7 == 15 && r == 7)) return (uint8_t)(sign | 0x7E);
+  return (uint8_t)(sign | ((e + 7) << 3) | r);
+}
+
+/* The quantized code of x: x / scale in float, rounded to nearest even, saturated. */
+uint8_t oracle_quantize(float x, float scale, int64_t cache_dtype) {
+  const float q = x / scale;
+  if (cache_dtype == ORACLE_E4M3) return oracle_round_e4m3(q);
+  if (isnan(q)) return 0;
+  if (q >= 127.0f) return (uint8_t)127;
+  if (q <= -128.0f) return (uint8_t)(int8_t)-128;
+  return (uint8_t)(int8_t)(int)nearbyintf(q);
+}
+
 static double load_elem(const void *base, int64_t idx, int64_t dtype) {
   if (dtype == ORACLE_F32) {
     float f;
@@ -164,6 +218,14 @@ static void store_elem(void *base, int64_t idx, int64_t dtype, double v) {
     uint16_t h = oracle_round_bf16(v);
     memcpy((char *)base + idx * 2, &h, 2);
   }
+}
+
+/* Element idx of a key or value row of the cache's type, as a number: the element
+ * itself, or code * scale for a quantized cache. */
+static double load_kv(const oracle_args *a, const void *base, int64_t idx, float scale) {
+  if (a->cache_dtype == ORACLE_I8) return (double)((const int8_t *)base)[idx] * (double)scale;
+  if (a->cache_dtype == ORACLE_E4M3) return oracle_decode_e4m3(((const uint8_t *)base)[idx]) * (double)scale;
+  return load_elem(base, idx, a->dtype);
 }
 
 /* Element offset of row r (0-based) of slice (b, kvh) in a (B, Nkv, C, D) cache. */
@@ -219,16 +281,16 @@ static int rotate_item(const oracle_args *a, int64_t b, double *qrot, void *krot
  * X[r] = past row r for r < Lp, else new token r - Lp.  X[r] holds absolute
  * position P - Lp + r ([P1] row layout applied to the past length P). */
 static int step_item(const oracle_args *a, int64_t b, double *z, double *acc, const double *qrot,
-                     const void *krot) {
+                     const void *knew, const void *vnew) {
   const int64_t S = a->sequence_length, D = a->head_size, W = a->local_window_size;
   const int64_t Nq = a->num_heads, Nkv = a->kv_num_heads, C = a->capacity;
   const int64_t group = Nq / Nkv;
-  const int64_t esize = a->dtype == ORACLE_F32 ? 4 : 2;
+  const int64_t esize = a->cache_dtype ? 1 : (a->dtype == ORACLE_F32 ? 4 : 2); /* cache element */
   const int64_t T = (int64_t)a->seqlens_k[b] + 1; /* [P1] review: T_b = seqlens_k[b] + 1 */
   const int64_t P = T - S;                         /* [P2] review: past length */
   int64_t Lp, Lt, first_pos, s, h, kvh, r, d, j;
 
-  const void *key = krot ? krot : a->key; /* the new key rows, turned if do_rotary */
+  const void *key = knew, *value = vnew; /* the new rows as the cache holds them */
 
   if (P < 0) return ORACLE_EPAST;
   if (T > a->total_sequence_length) return ORACLE_ETOTAL;
@@ -253,7 +315,7 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc, co
         const int64_t koff = xr < Lp ? cache_row(a, b, kvh, xr) : input_row(a, b, xr - Lp, kvh);
         double dot = 0.0, zj;
         for (d = 0; d < D; ++d)
-          dot += (qrot ? qrot[qoff + d] : load_elem(a->query, qoff + d, a->dtype)) * load_elem(kb, koff + d, a->dtype);
+          dot += (qrot ? qrot[qoff + d] : load_elem(a->query, qoff + d, a->dtype)) * load_kv(a, kb, koff + d, a->k_scale);
         zj = a->scale * dot;
         if (a->softcap > 0.0) zj = a->softcap * tanh(zj / a->softcap);
         if (a->attention_bias)
@@ -271,11 +333,11 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc, co
       for (d = 0; d < D; ++d) acc[d] = 0.0;
       for (j = jlo; j <= i; ++j) {
         const int64_t xr = j - first_pos;
-        const void *vb = xr < Lp ? a->past_value : a->value;
+        const void *vb = xr < Lp ? a->past_value : value;
         const int64_t voff = xr < Lp ? cache_row(a, b, kvh, xr) : input_row(a, b, xr - Lp, kvh);
         const double p = exp(z[j - jlo] - zmax);
         denom += p;
-        for (d = 0; d < D; ++d) acc[d] += p * load_elem(vb, voff + d, a->dtype);
+        for (d = 0; d < D; ++d) acc[d] += p * load_kv(a, vb, voff + d, a->v_scale);
       }
       for (d = 0; d < D; ++d) {
         const double o = acc[d] / denom;
@@ -292,7 +354,7 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc, co
       const int64_t xr = Lp + S - Lt + r;
       const int64_t src = xr < Lp ? cache_row(a, b, kvh, xr) : input_row(a, b, xr - Lp, kvh);
       const void *ksrc = xr < Lp ? a->past_key : key;
-      const void *vsrc = xr < Lp ? a->past_value : a->value;
+      const void *vsrc = xr < Lp ? a->past_value : value;
       const int64_t dst = cache_row(a, b, kvh, r);
       memcpy((char *)a->present_key + dst * esize, (const char *)ksrc + src * esize, D * esize);
       memcpy((char *)a->present_value + dst * esize, (const char *)vsrc + src * esize, D * esize);
@@ -302,18 +364,32 @@ static int step_item(const oracle_args *a, int64_t b, double *z, double *acc, co
   return ORACLE_OK;
 }
 
+/* The S new key and value rows of item b as a quantized cache holds them (reading above):
+ * knew, vnew (B, S, Nkv*D) codes; ksrc is the key input, or the turned keys. */
+static void quantize_item(const oracle_args *a, int64_t b, const void *ksrc, uint8_t *knew, uint8_t *vnew) {
+  const int64_t n = a->kv_num_heads * a->head_size, off = b * a->sequence_length * n;
+  int64_t e;
+  for (e = 0; e < a->sequence_length * n; ++e) {
+    knew[off + e] = oracle_quantize((float)load_elem(ksrc, off + e, a->dtype), a->k_scale, a->cache_dtype);
+    vnew[off + e] = oracle_quantize((float)load_elem(a->value, off + e, a->dtype), a->v_scale, a->cache_dtype);
+  }
+}
+
 /* Items are independent; the step is item by item.  Returns ORACLE_OK or the first
  * error met (items before it are already written). */
 int oracle_step(const oracle_args *a) {
   int64_t b, nz;
   double *z, *acc, *qrot = NULL;
   void *krot = NULL;
+  uint8_t *knew = NULL, *vnew = NULL;
+  const int quant = a->cache_dtype == ORACLE_I8 || a->cache_dtype == ORACLE_E4M3;
   int rc = ORACLE_OK;
   if (a->batch_size < 0 || a->sequence_length < 1 || a->num_heads < 1 || a->kv_num_heads < 1 ||
       a->num_heads % a->kv_num_heads != 0 || a->head_size < 1 || a->capacity < 1 ||
       a->local_window_size < 1 || a->local_window_size > a->capacity ||
       (a->dtype != ORACLE_F32 && a->dtype != ORACLE_BF16))
     return ORACLE_EARGS;
+  if (a->cache_dtype != 0 && (!quant || !(a->k_scale > 0.0f) || !(a->v_scale > 0.0f))) return ORACLE_EARGS;
   if (a->do_rotary && (a->rotary_dim < 2 || a->rotary_dim % 2 != 0 || a->rotary_dim > a->head_size ||
                        a->rotary_cache_len < 0 || !a->cos_cache || !a->sin_cache))
     return ORACLE_EARGS;
@@ -325,20 +401,35 @@ int oracle_step(const oracle_args *a) {
     qrot = (double *)malloc(sizeof(double) * rows * (size_t)(a->num_heads * a->head_size) + 8);
     krot = malloc(8 * rows * (size_t)(a->kv_num_heads * a->head_size) + 8);
   }
-  if (!z || !acc || (a->do_rotary && (!qrot || !krot))) {
+  if (quant) {
+    const size_t n = (size_t)(a->batch_size * a->sequence_length * a->kv_num_heads * a->head_size) + 8;
+    knew = (uint8_t *)malloc(n);
+    vnew = (uint8_t *)malloc(n);
+  }
+  if (!z || !acc || (a->do_rotary && (!qrot || !krot)) || (quant && (!knew || !vnew))) {
     free(z);
     free(acc);
     free(qrot);
     free(krot);
+    free(knew);
+    free(vnew);
     return ORACLE_ENOMEM;
   }
   for (b = 0; b < a->batch_size && rc == ORACLE_OK; ++b) {
-    if (a->do_rotary) rc = rotate_item(a, b, qrot, krot, acc);
-    if (rc == ORACLE_OK) rc = step_item(a, b, z, acc, qrot, krot);
+    const void *ksrc = a->key;
+    if (a->do_rotary) {
+      rc = rotate_item(a, b, qrot, krot, acc);
+      ksrc = krot;
+    }
+    if (rc == ORACLE_OK && quant) quantize_item(a, b, ksrc, knew, vnew);
+    if (rc == ORACLE_OK)
+      rc = step_item(a, b, z, acc, qrot, quant ? (const void *)knew : ksrc, quant ? (const void *)vnew : a->value);
   }
   free(z);
   free(acc);
   free(qrot);
   free(krot);
+  free(knew);
+  free(vnew);
   return rc;
 }

@@ -681,3 +681,126 @@ def test_rotary_chunk_invariance():
         assert np.array_equal(ra["output_f64"][:, s], rb["output_f64"][:, 0])
     L = int(ra["resident_len"][0])
     assert np.array_equal(a.pk[:, :, :L], b.pk[:, :, :L])
+
+
+# ---------------------------------------------------------------- quantized cache
+# mobius issue #111, Part 1.1 names k_scale / v_scale ("KV cache quantization scale");
+# the reading: int8 or fp8 e4m3 codes, one scale per tensor, code * scale, codes taken
+# as x / scale in float rounded to nearest even and saturated.
+
+
+def test_e4m3_rounding_matches_torch():
+    """The oracle's float -> e4m3 rounding equals torch's float8_e4m3fn cast (an
+    independent implementation) on random values across the range, ties, subnormals,
+    zeros and the largest finite values (torch's cast is not used past 448, where the
+    reading saturates)."""
+    rng = _rng(60)
+    xs = np.concatenate([
+        rng.uniform(-448, 448, 4000), rng.normal(0, 1, 4000), rng.normal(0, 0.01, 2000),
+        np.ldexp(np.arange(-40, 40, dtype=np.float64) * 0.25 + 0.125, -9),   # ties among subnormals
+        np.array([0.0, -0.0, 448.0, -448.0, 1.0625, 1.1875, 240.0, 248.0, 2.0 ** -6, 2.0 ** -9, 2.0 ** -10]),
+    ]).astype(np.float32)
+    want = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.round_e4m3(float(x)) for x in xs], np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_e4m3_decode_all_codes():
+    """Every e4m3 code decodes to torch's value for it, and every non-NaN code rounds back
+    to itself."""
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        v = oracle.decode_e4m3(c)
+        if np.isnan(want[c]):
+            assert np.isnan(v)
+            continue
+        assert v == want[c] and math.copysign(1.0, v) == math.copysign(1.0, want[c])
+        assert oracle.round_e4m3(v) == c
+    assert oracle.round_e4m3(1e6) == 0x7E and oracle.round_e4m3(-1e6) == 0xFE  # saturated
+    assert oracle.round_e4m3(float("inf")) == 0x7E
+
+
+def test_int8_quantizer_rounding_and_saturation():
+    """Ties to even, saturation to [-128, 127], the division done in float."""
+    q = lambda x, s=1.0: int(np.int8(np.uint8(oracle.quantize(x, s, oracle.I8))))
+    assert [q(v) for v in (0.5, 1.5, 2.5, -0.5, -1.5, -2.5)] == [0, 2, 2, 0, -2, -2]
+    assert q(126.5) == 126 and q(127.5) == 127 and q(1e9) == 127
+    assert q(-127.5) == -128 and q(-128.5) == -128 and q(-1e9) == -128
+    assert q(3.0, 2.0) == 2 and q(5.0, 2.0) == 2 and q(7.0, 2.0) == 4  # 1.5, 2.5, 3.5 -> ties to even
+    # the quotient is a float: 2.4999998 / 1 stays below the tie, 0.1 / 0.04 = 2.5 in float
+    assert q(np.float32(2.4999998)) == 2
+    assert q(0.1, 0.04) == int(np.rint(np.float32(0.1) / np.float32(0.04)))
+
+
+@pytest.mark.parametrize("cache_dtype", [oracle.I8, oracle.E4M3])
+def test_quantized_cache_exact_values(cache_dtype):
+    """Keys and values that the codes represent exactly (small integers times the scale,
+    separate key and value scales): the quantized cache gives fp64-identical outputs to
+    the plain fp32 cache across compactions, and its rows hold the codes of the inputs."""
+    D, Nq, Nkv, C, W = 8, 4, 2, 7, 5
+    ks, vs = 0.25, 0.0625
+    rng = _rng(61)
+    plain = OracleCache(1, Nq, Nkv, D, C, W)
+    quant = OracleCache(1, Nq, Nkv, D, C, W)
+    quant.pk = np.zeros((1, Nkv, C, D), np.uint8)
+    quant.pv = np.zeros((1, Nkv, C, D), np.uint8)
+    T = 0
+    for S in [3, 1, 4, 1, 1, 2, 1]:
+        q = _u(rng, (1, S, Nq * D))
+        k = (rng.integers(-7, 8, size=(1, S, Nkv * D)) * ks).astype(np.float32)
+        v = (rng.integers(-7, 8, size=(1, S, Nkv * D)) * vs).astype(np.float32)
+        rp = plain.step(q, k, v, [T + S - 1])
+        rq = oracle.step(q, k, v, quant.pk, quant.pv, np.array([T + S - 1], np.int32), T + S, Nq, Nkv, W,
+                         cache_dtype=cache_dtype, k_scale=ks, v_scale=vs)
+        quant.pk, quant.pv = rq["present_key"], rq["present_value"]
+        assert np.array_equal(rp["output_f64"], rq["output_f64"])
+        T += S
+        L = int(rq["resident_len"][0])
+        for row in range(L):  # row r holds the codes of the key of position T - L + r
+            dec = np.array([(np.int8(np.uint8(c)) if cache_dtype == oracle.I8 else oracle.decode_e4m3(c))
+                            for c in quant.pk[0, 0, row]], np.float64) * ks
+            assert np.array_equal(dec, plain.pk[0, 0, row].astype(np.float64))
+
+
+def test_quantized_rounds_and_chunk_invariance():
+    """General values: a 4-token step equals four 1-token steps bit for bit (each new row
+    is quantized once, and attention reads it as the cache holds it); the outputs differ
+    from the unquantized cache only by the quantization (a few percent), and a key scale
+    that is doubled halves every key code."""
+    D, Nq, Nkv, C, W = 8, 2, 1, 6, 4
+    rng = _rng(62)
+    qp, kp, vp = _u(rng, (1, 7, Nq * D)), _u(rng, (1, 7, D)), _u(rng, (1, 7, D))
+    q4, k4, v4 = _u(rng, (1, 4, Nq * D)), _u(rng, (1, 4, D)), _u(rng, (1, 4, D))
+    for ct in (oracle.I8, oracle.E4M3):
+        ks, vs = 1.0 / 100, 1.0 / 90
+
+        def run(steps, ks=ks):
+            pk = np.zeros((1, 1, C, D), np.uint8)
+            pv = np.zeros((1, 1, C, D), np.uint8)
+            outs = []
+            for (q, k, v, seq) in steps:
+                r = oracle.step(q, k, v, pk, pv, np.array([seq], np.int32), seq + 1, Nq, Nkv, W,
+                                cache_dtype=ct, k_scale=ks, v_scale=vs)
+                pk, pv = r["present_key"], r["present_value"]
+                outs.append(r["output_f64"])
+            return outs, pk, pv, r
+
+        whole, pk_a, _, ra = run([(qp, kp, vp, 6), (q4, k4, v4, 10)])
+        parts, pk_b, _, _ = run([(qp, kp, vp, 6)] + [(q4[:, s:s + 1], k4[:, s:s + 1], v4[:, s:s + 1], 7 + s)
+                                                      for s in range(4)])
+        for s in range(4):
+            assert np.array_equal(whole[1][:, s], parts[1 + s][:, 0])
+        L = int(ra["resident_len"][0])
+        assert np.array_equal(pk_a[:, :, :L], pk_b[:, :, :L])
+        if ct == oracle.I8:
+            _, pk_2, _, _ = run([(qp, kp, vp, 6)], ks=2 * ks)
+            _, pk_1, _, _ = run([(qp, kp, vp, 6)], ks=ks)
+            c1 = pk_1[:, :, :6].view(np.int8).astype(np.int64)
+            c2 = pk_2[:, :, :6].view(np.int8).astype(np.int64)
+            assert np.all(np.abs(2 * c2 - c1) <= 1)
+        ref = OracleCache(1, Nq, Nkv, D, C, W)
+        ref.step(qp, kp, vp, [6])
+        rr = ref.step(q4, k4, v4, [10])
+        err = np.abs(rr["output_f64"] - whole[1]).max() / np.abs(rr["output_f64"]).max()
+        assert 0 < err < (0.02 if ct == oracle.I8 else 0.1)
