@@ -40,6 +40,10 @@
  *     dtype;
  *   - present rows [0, Lt) receive the Lt most recent positions of the past rows
  *     [0, Lp) followed by the S new rows (bit copies);
+ *   - with a quantized cache (cache_dtype), the S new key and value rows become codes
+ *     round_to_nearest_even(x / scale) computed in float and saturated to the code type
+ *     (int8 [-128, 127]; e4m3 finite up to 448); attention reads every key and value,
+ *     the new ones included, as code * scale;
  *   - with do_rotary, the S new query and key rows are first turned by the rotary
  *     embedding of their positions (pairs of dimensions (x1, x2) -> (x1 cos - x2 sin,
  *     x2 cos + x1 sin) with cos/sin from row pos of the caches; RoFormer's rotation),
@@ -77,8 +81,10 @@ typedef enum gqaw_status {
 } gqaw_status;
 
 typedef enum gqaw_dtype {
-  GQAW_F32 = 0, /* float32 query/key/value/cache/output */
-  GQAW_BF16 = 1 /* bfloat16 query/key/value/cache/output */
+  GQAW_F32 = 0,  /* float32 query/key/value/cache/output */
+  GQAW_BF16 = 1, /* bfloat16 query/key/value/cache/output */
+  GQAW_I8 = 2,   /* cache_dtype only: int8 codes of a quantized cache */
+  GQAW_E4M3 = 3  /* cache_dtype only: fp8 e4m3 codes (OCP 8-bit floating point) */
 } gqaw_dtype;
 
 /* Bits of the device status word. */
@@ -142,6 +148,13 @@ typedef struct gqaw_step_args {
   const int64_t *position_ids;   /* NULL (token s of item b at position
                                     seqlens_k[b] + 1 - S + s), or (B, S) int64, 8-byte
                                     aligned ([P3] Part 1.1) */
+  int32_t cache_dtype;           /* 0: the caches hold `dtype`; GQAW_I8 or GQAW_E4M3: they
+                                    hold 1-byte codes of a quantized cache ([P3] Part 1.1,
+                                    k_scale and v_scale); needs dtype GQAW_BF16 and
+                                    head_size 64, 128 or 256 */
+  const float *k_scale;          /* quantized cache: device fp32 scalar, > 0; a key code c
+                                    stands for c * k_scale.  Otherwise ignored */
+  const float *v_scale;          /* quantized cache: the same for values */
 } gqaw_step_args;
 
 /* L(T) of [P1] in 64-bit arithmetic.  Pure host function.  Returns -1 if T < 0,

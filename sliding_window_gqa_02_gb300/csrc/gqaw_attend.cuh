@@ -90,6 +90,29 @@ template <> struct Pairs<__nv_bfloat16> {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   }
 };
+template <> struct Pairs<CodeI8> {
+  // pair j (0..7) of a 16-byte vector of 16 int8 codes, as floats (exact): the byte,
+  // biased by 128, is placed in the low mantissa bits of 2^23, which is then subtracted
+  // with the bias
+  __device__ __forceinline__ static float2 get(const uint4 &u, int j) {
+    const uint32_t w = (j < 2 ? u.x : (j < 4 ? u.y : (j < 6 ? u.z : u.w))) ^ 0x80808080u;
+    const uint32_t b = (j & 1) * 2;  // first byte of the pair in the word
+    const float lo = __uint_as_float(__byte_perm(w, 0x4B000000u, b | 0x7540u)) - 8388736.f;
+    const float hi = __uint_as_float(__byte_perm(w, 0x4B000000u, (b + 1) | 0x7540u)) - 8388736.f;
+    return make_float2(lo, hi);
+  }
+};
+template <> struct Pairs<CodeE4M3> {
+  // pair j (0..7) of a 16-byte vector of 16 fp8 e4m3 codes, as floats (exact): the
+  // hardware pair conversion to half precision, then widening
+  __device__ __forceinline__ static float2 get(const uint4 &u, int j) {
+    const uint32_t w = j < 2 ? u.x : (j < 4 ? u.y : (j < 6 ? u.z : u.w));
+    const uint16_t pair = (uint16_t)(w >> ((j & 1) * 16));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+  }
+};
 
 // A unit: (item, new token, kv head, query-head block) and its visible key range.
 struct Unit {
@@ -126,10 +149,12 @@ __device__ __forceinline__ long long cta_of_tile(long long x, long long V, long 
   return ((x + 1) * G - 1) / V;
 }
 
-template <typename T, int D, int GB>
-__global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
+// T: query and output elements; TC: cache elements (T itself, or 1-byte codes of a
+// quantized cache, scaled by *p.ks and *p.vs).
+template <typename T, typename TC, int D, int GB>
+__global__ void __launch_bounds__(AttendCfg<TC, D, GB>::kThreads, 2)
     attend_kernel(const Params p) {
-  using Cfg = AttendCfg<T, D, GB>;
+  using Cfg = AttendCfg<TC, D, GB>;
   constexpr int EPV = Cfg::kEPV, VPL = Cfg::kVPL, LPR = Cfg::kLPR;
   constexpr int PAIRS = Cfg::kPairs, PPV = EPV / 2;  // pairs per vector
   constexpr int RPW = Cfg::kRPW, NW = Cfg::kWarps, TILE = Cfg::kTile, NST = Cfg::kStages;
@@ -166,6 +191,9 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
   pdl_wait();                // the previous kernel (a cache update) has finished
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // quantized cache: codes times the per-tensor scales (key scale folded into q)
+  const float qscale = p.ks ? p.qscale * *p.ks : p.qscale;
+  const float vscale = p.vs ? *p.vs : 1.f;
 
   // ---------------------------------------------------------------- producer state
   // Thread 0 walks the same (unit, tile) sequence as the consumers, NST - 1 tiles
@@ -205,8 +233,8 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
     const long long j0 = pu_x.lo + (long long)plt * TILE;
     const long long j1 = j0 + TILE < pu_x.hi ? j0 + TILE : pu_x.hi;
     const size_t slice = ((size_t)pu_x.b * p.Nkv + pu_x.kvh) * (size_t)p.C;
-    const T *pk = static_cast<const T *>(p.pk) + slice * D;
-    const T *pv = static_cast<const T *>(p.pv) + slice * D;
+    const TC *pk = static_cast<const TC *>(p.pk) + slice * D;
+    const TC *pv = static_cast<const TC *>(p.pv) + slice * D;
     unsigned char *ks = stage_base + st * Cfg::kStageBytes;
     unsigned char *vs = ks + TILE * ROWB;
     mbar_arrive_expect_tx(&full[st], (uint32_t)(2 * (j1 - j0) * ROWB));
@@ -219,8 +247,8 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
     }
     for (long long j = (j0 > pu_x.pl.P ? j0 : pu_x.pl.P); j < j1; ++j) {  // new rows: keys from P
       const size_t off = (((size_t)pu_x.b * p.S + (size_t)(j - pu_x.pl.P)) * p.Nkv + pu_x.kvh) * D;
-      bulk_g2s(ks + (j - j0) * ROWB, static_cast<const T *>(p.k) + off, ROWB, &full[st], pol);
-      bulk_g2s(vs + (j - j0) * ROWB, static_cast<const T *>(p.v) + off, ROWB, &full[st], pol);
+      bulk_g2s(ks + (j - j0) * ROWB, static_cast<const TC *>(p.k) + off, ROWB, &full[st], pol);
+      bulk_g2s(vs + (j - j0) * ROWB, static_cast<const TC *>(p.v) + off, ROWB, &full[st], pol);
     }
     ++plt;
     ++issued;
@@ -282,6 +310,9 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
 
     float2 q2[GB][PAIRS];
     {
+      // the lane's EPV query dims per cache vector take QV 16-byte vectors of T (one
+      // when T is the cache type); a quantized cache's key scale is folded in here
+      constexpr int PPT = 8 / (int)sizeof(T), QV = PPV / PPT;
       const T *qin = static_cast<const T *>(p.q);
 #pragma unroll
       for (int r = 0; r < GB; ++r) {
@@ -289,11 +320,14 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
         const T *qrow = qin + (orow0 + (ok ? r : 0)) * D;
 #pragma unroll
         for (int m = 0; m < VPL; ++m) {
-          const uint4 uq = *reinterpret_cast<const uint4 *>(qrow + (li + LPR * m) * EPV);
 #pragma unroll
-          for (int j = 0; j < PPV; ++j) {
-            const float2 f = Pairs<T>::get(uq, j);
-            q2[r][m * PPV + j] = ok ? make_float2(f.x * p.qscale, f.y * p.qscale) : make_float2(0.f, 0.f);
+          for (int qv = 0; qv < QV; ++qv) {
+            const uint4 uq = *reinterpret_cast<const uint4 *>(qrow + (li + LPR * m) * EPV + qv * 2 * PPT);
+#pragma unroll
+            for (int j = 0; j < PPT; ++j) {
+              const float2 f = Pairs<T>::get(uq, j);
+              q2[r][m * PPV + qv * PPT + j] = ok ? make_float2(f.x * qscale, f.y * qscale) : make_float2(0.f, 0.f);
+            }
           }
         }
       }
@@ -339,7 +373,7 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
             const uint4 uk = *reinterpret_cast<const uint4 *>(ks + r * ROWB + (li + LPR * m) * 16);
 #pragma unroll
             for (int j = 0; j < PPV; ++j) {
-              const float2 k2 = Pairs<T>::get(uk, j);
+              const float2 k2 = Pairs<TC>::get(uk, j);
 #pragma unroll
               for (int h = 0; h < GB; ++h) part2[h] = __ffma2_rn(q2[h][m * PPV + j], k2, part2[h]);
             }
@@ -429,7 +463,7 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
             const uint4 uv = *reinterpret_cast<const uint4 *>(vs + r * ROWB + (li + LPR * m) * 16);
 #pragma unroll
             for (int j = 0; j < PPV; ++j) {
-              const float2 v2 = Pairs<T>::get(uv, j);
+              const float2 v2 = Pairs<TC>::get(uv, j);
 #pragma unroll
               for (int h = 0; h < GB; ++h)
                 acc2[h][m * PPV + j] = __ffma2_rn(make_float2(pw[ps][h], pw[ps][h]), v2, acc2[h][m * PPV + j]);
@@ -507,7 +541,7 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
         A = fmaf(f, row[d], A);
       }
       if (cf == cl) {
-        out[(orow0 + h) * D + d] = Elem<T>::store(sink_divide(A, L, base, sink_log2(p, hq0 + h)));
+        out[(orow0 + h) * D + d] = Elem<T>::store(sink_divide(A, L, base, sink_log2(p, hq0 + h)) * vscale);
       } else {
         float *part = p.partials + ((cta * 2 + slot) * GB + h) * (D + 2);
         part[d] = A;
@@ -545,7 +579,7 @@ __global__ void __launch_bounds__(AttendCfg<T, D, GB>::kThreads, 2)
             L = fmaf(f, __ldcg(part + D + 1), L);
             A = fmaf(f, __ldcg(part + d), A);
           }
-          out[(orow0 + h) * D + d] = Elem<T>::store(sink_divide(A, L, base, sink_log2(p, hq0 + h)));
+          out[(orow0 + h) * D + d] = Elem<T>::store(sink_divide(A, L, base, sink_log2(p, hq0 + h)) * vscale);
         }
         if (threadIdx.x == 0) p.tickets[u] = 0u;  // ready for the next step
       }

@@ -20,12 +20,12 @@ cudaError_t launch_one(const Params &p, int max_ctas, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   int slots = dev < kMaxDevices ? resident[dev].load(std::memory_order_relaxed) : 0;
   if (slots <= 0) {
-    e = cudaFuncSetAttribute(attend_kernel<float, D, GB>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    e = cudaFuncSetAttribute(attend_kernel<float, float, D, GB>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attend_kernel<float, D, GB>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(attend_kernel<float, float, D, GB>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<float, D, GB>, Cfg::kThreads, Cfg::kSmem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<float, float, D, GB>, Cfg::kThreads, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -44,7 +44,7 @@ cudaError_t launch_one(const Params &p, int max_ctas, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attend_kernel<float, D, GB>, p);
+  e = cudaLaunchKernelEx(&cfg, attend_kernel<float, float, D, GB>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -28,6 +28,9 @@ int attend_tile_bf16(int D);
 cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream);
 cudaError_t launch_mma(const Params &p, const TcArgs &ta, const TcMaps &maps, int grid, cudaStream_t stream);
 cudaError_t launch_rotary(const Params &p, cudaStream_t stream);
+cudaError_t launch_attend_q8(const Params &p, int gb, int blocks, cudaStream_t stream);
+int attend_tile_q8(int D);
+cudaError_t launch_quantize(const Params &p, int max_blocks, cudaStream_t stream);
 cudaError_t launch_mmad(const Params &p, const TdArgs &ta, const TdMaps &maps, int max_ctas, cudaStream_t stream);
 }  // namespace gqaw
 
@@ -58,7 +61,10 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Launch {
-  int esize, rowbytes, group, gb, headblocks, tile, tpu, ncg;
+  int esize, rowbytes, group, gb, headblocks, tile, tpu, ncg;  // esize: cache element bytes
+  int qsize;              // query/key/value/output element bytes
+  int quant;              // cache_dtype of a quantized cache, or 0
+  size_t off_kq, off_vq;  // quantized cache: the codes of the step's new rows
   long long units, ctas, ncopy;
   size_t off_list, off_tickets, off_partials, ws_bytes;
   int rot_dim;            // > 0: the rotary embedding is on, over this many dimensions
@@ -105,13 +111,24 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     if (a->rotary_cache_len < 1) return fail(GQAW_EINVAL, "rotary_cache_len %d < 1", a->rotary_cache_len);
   }
 
-  L->esize = a->dtype == GQAW_F32 ? 4 : 2;
+  L->qsize = a->dtype == GQAW_F32 ? 4 : 2;
+  L->quant = 0;
+  if (a->cache_dtype != 0) {
+    if (a->cache_dtype != GQAW_I8 && a->cache_dtype != GQAW_E4M3)
+      return fail(GQAW_EINVAL, "unknown cache_dtype %d", a->cache_dtype);
+    if (a->dtype != GQAW_BF16) return fail(GQAW_EUNSUPPORTED, "a quantized cache needs dtype GQAW_BF16");
+    if (a->head_size != 64 && a->head_size != 128 && a->head_size != 256)
+      return fail(GQAW_EUNSUPPORTED, "a quantized cache needs head_size 64, 128 or 256");
+    L->quant = a->cache_dtype;
+  }
+  L->esize = L->quant ? 1 : L->qsize;
   L->rowbytes = a->head_size * L->esize;
   L->group = a->num_heads / a->kv_num_heads;
   L->gb = 1;  // query heads per CTA: the next power of two >= group, at most 8
   while (L->gb < L->group && L->gb < 8) L->gb *= 2;
   L->headblocks = (int)ceil_div(L->group, L->gb);
-  L->tile = a->dtype == GQAW_F32 ? gqaw::attend_tile_f32(a->head_size) : gqaw::attend_tile_bf16(a->head_size);
+  L->tile = L->quant ? gqaw::attend_tile_q8(a->head_size)
+                     : a->dtype == GQAW_F32 ? gqaw::attend_tile_f32(a->head_size) : gqaw::attend_tile_bf16(a->head_size);
   L->units = (long long)a->batch_size * a->sequence_length * a->kv_num_heads * L->headblocks;
 
   // Persistent stream-K attention: the step's work is units x tpu key tiles; the
@@ -184,7 +201,8 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   // on the MMA's M dimension: persistent, one CTA per SM, stream-K over (unit, 128-key
   // tile); partial results of units cut by a CTA range are merged in the kernel.
   const long long rows_all = (long long)a->batch_size * a->kv_num_heads * a->capacity;
-  L->td = a->dtype == GQAW_BF16 && a->head_size == 128 && (long long)a->sequence_length * L->group <= 32 &&
+  if (L->quant) L->tc = false;  // quantized caches: the FFMA kernel with a code type
+  L->td = !L->quant && a->dtype == GQAW_BF16 && a->head_size == 128 && (long long)a->sequence_length * L->group <= 32 &&
           rows_all < 0x7fffffffLL && (long long)a->batch_size * a->sequence_length < 0x7fffffffLL;
   if (L->td) {
     L->tc = false;
@@ -207,8 +225,16 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   if (L->rot_dim > 0) {
     const size_t tokens = (size_t)a->batch_size * a->sequence_length;
     L->off_qrot = align256(L->ws_bytes);
-    L->off_krot = L->off_qrot + align256(tokens * a->num_heads * a->head_size * L->esize);
-    L->ws_bytes = L->off_krot + align256(tokens * a->kv_num_heads * a->head_size * L->esize);
+    L->off_krot = L->off_qrot + align256(tokens * a->num_heads * a->head_size * L->qsize);
+    L->ws_bytes = L->off_krot + align256(tokens * a->kv_num_heads * a->head_size * L->qsize);
+  }
+  // Quantized cache: the codes of the step's new key and value rows.
+  L->off_kq = L->off_vq = 0;
+  if (L->quant) {
+    const size_t n = (size_t)a->batch_size * a->sequence_length * a->kv_num_heads * a->head_size;
+    L->off_kq = align256(L->ws_bytes);
+    L->off_vq = L->off_kq + align256(n);
+    L->ws_bytes = L->off_vq + align256(n);
   }
   return GQAW_OK;
 }
@@ -242,10 +268,15 @@ gqaw_status check_pointers(const gqaw_step_args *a, const Launch &L) {
       return fail(GQAW_EINVAL, "attention_bias strides must be >= 0");
   }
   if (a->head_sink && !aligned(a->head_sink, 4)) return fail(GQAW_EINVAL, "head_sink is not 4-byte aligned");
+  if (L.quant) {
+    if (!a->k_scale || !a->v_scale) return fail(GQAW_EINVAL, "a quantized cache needs k_scale and v_scale");
+    if (!aligned(a->k_scale, 4) || !aligned(a->v_scale, 4))
+      return fail(GQAW_EINVAL, "k_scale / v_scale are not 4-byte aligned");
+  }
   if (L.rot_dim > 0) {
     if (!a->cos_cache || !a->sin_cache) return fail(GQAW_EINVAL, "do_rotary needs cos_cache and sin_cache");
-    if (!aligned(a->cos_cache, L.esize) || !aligned(a->sin_cache, L.esize))
-      return fail(GQAW_EINVAL, "cos_cache / sin_cache are not %d-byte aligned", L.esize);
+    if (!aligned(a->cos_cache, L.qsize) || !aligned(a->sin_cache, L.qsize))
+      return fail(GQAW_EINVAL, "cos_cache / sin_cache are not %d-byte aligned", L.qsize);
     if (a->position_ids && !aligned(a->position_ids, 8))
       return fail(GQAW_EINVAL, "position_ids is not 8-byte aligned");
   }
@@ -256,7 +287,7 @@ gqaw_status check_pointers(const gqaw_step_args *a, const Launch &L) {
 
   const size_t B = (size_t)a->batch_size, S = (size_t)a->sequence_length, D = (size_t)a->head_size;
   const size_t cache = B * a->kv_num_heads * (size_t)a->capacity * D * L.esize;
-  const size_t qo = B * S * a->num_heads * D * L.esize, kv = B * S * a->kv_num_heads * D * L.esize;
+  const size_t qo = B * S * a->num_heads * D * L.qsize, kv = B * S * a->kv_num_heads * D * L.qsize;
   auto rng = [](const void *p, size_t n, const char *name) {
     return Range{static_cast<const char *>(p), static_cast<const char *>(p) + n, name};
   };
@@ -328,19 +359,30 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
   p->biasmul = gqaw::kLog2e;
   p->ncg = L.ncg;
   p->rowbytes = L.rowbytes;
+  p->qbytes = L.qsize;
   p->sink = a->head_sink;
   p->sink_mode = a->head_sink ? 1 : (a->smooth_softmax ? 2 : 0);
+  p->quant = L.quant;
   p->rot_dim = L.rot_dim;
   if (L.rot_dim > 0) {
     p->q_in = a->query;
     p->k_in = a->key;
     p->q = ws + L.off_qrot;
-    p->k = ws + L.off_krot;
+    p->krot = ws + L.off_krot;
+    p->k = p->krot;
     p->rcos = a->cos_cache;
     p->rsin = a->sin_cache;
     p->pos_ids = reinterpret_cast<const long long *>(a->position_ids);
     p->rot_inter = a->rotary_interleaved ? 1 : 0;
     p->rot_len = a->rotary_cache_len;
+  }
+  if (L.quant) {  // the codes of the new rows, from the (maybe turned) rows of dtype T
+    p->kq_in = p->k;
+    p->vq_in = a->value;
+    p->k = ws + L.off_kq;
+    p->v = ws + L.off_vq;
+    p->ks = a->k_scale;
+    p->vs = a->v_scale;
   }
 }
 
@@ -433,6 +475,15 @@ gqaw_status run_attend(const gqaw_step_args *a, const Launch &L, const gqaw::Par
     const cudaError_t e = gqaw::launch_rotary(p, st);
     if (e != cudaSuccess) return cuda_fail(e, "rotary kernel launch");
     g_launches.fetch_add(1);
+  }
+  if (L.quant) {
+    const cudaError_t e = gqaw::launch_quantize(p, (int)(kSms * 8), st);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize kernel launch");
+    g_launches.fetch_add(1);
+    const cudaError_t e2 = gqaw::launch_attend_q8(p, L.gb, (int)L.ctas, st);
+    if (e2 != cudaSuccess) return cuda_fail(e2, "attention kernel launch");
+    g_launches.fetch_add(1);
+    return GQAW_OK;
   }
   if (L.td) return run_mmad(a, L, p, st);
   if (L.tc) return run_mma(a, L, p, st);

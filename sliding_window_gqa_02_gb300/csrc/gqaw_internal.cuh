@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -38,15 +39,24 @@ struct Params {
   float capmul;              // softcap*log2(e), or 0 without softcap
   float biasmul;             // log2(e)
   int ncg;                   // column groups per cache row in the copy jobs
-  int rowbytes;              // D * element size
+  int rowbytes;              // D * cache element size
+  int qbytes;                // query/key/value/output element size (4 or 2)
   const float *sink;         // NULL or (Nq,): sink logit per query head (natural-log units)
   int sink_mode;             // 0: no sink; 1: sink[h]; 2: a sink of 0 for every head
-  // rotary embedding (rot_dim > 0): q and k above are the turned rows in the workspace,
-  // written by the rotary kernel from the step's inputs q_in and k_in
+  // rotary embedding (rot_dim > 0): q is the turned query in the workspace and krot the
+  // turned keys, written by the rotary kernel from the step's inputs q_in and k_in (k is
+  // krot, or the codes of krot with a quantized cache)
   const void *q_in, *k_in;
+  void *krot;
   const void *rcos, *rsin;   // (rot_len, rot_dim / 2) in the step's dtype
   const long long *pos_ids;  // NULL (positions P_b + s) or (B, S)
   int rot_dim, rot_inter, rot_len;
+  // quantized cache (quant > 0: GQAW_I8 or GQAW_E4M3): k and v above are the code rows of
+  // the step's new keys and values in the workspace, written by the quantize kernel from
+  // kq_in and vq_in (the step's rows of dtype T); ks, vs: device scales
+  int quant;
+  const void *kq_in, *vq_in;
+  const float *ks, *vs;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -112,6 +122,14 @@ __device__ __forceinline__ bool item_moves(const Params &p, const Plan &pl) {
 }
 
 // ---------------------------------------------------------------- conversions
+
+// 1-byte codes of a quantized cache (int8, fp8 e4m3); only their size and bits matter here.
+struct CodeI8 {
+  uint8_t bits;
+};
+struct CodeE4M3 {
+  uint8_t bits;
+};
 
 template <typename T> struct Elem;
 template <> struct Elem<float> {

@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kRotaryThreads) rotary_kernel(const Params p) 
   const long long rows = qrows + (long long)p.B * p.S * p.Nkv;
   const long long n = rows * slots;
   const T *qin = static_cast<const T *>(p.q_in), *kin = static_cast<const T *>(p.k_in);
-  T *qout = static_cast<T *>(const_cast<void *>(p.q)), *kout = static_cast<T *>(const_cast<void *>(p.k));
+  T *qout = static_cast<T *>(const_cast<void *>(p.q)), *kout = static_cast<T *>(p.krot);
   const T *rc = static_cast<const T *>(p.rcos), *rs = static_cast<const T *>(p.rsin);
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kRotaryThreads) rotary_vec_kernel(const Params
     const unsigned r = isq ? row : row - qrows;
     const unsigned token = isq ? r / Nq : r / Nkv;  // b * S + s
     const T *x = static_cast<const T *>(isq ? p.q_in : p.k_in) + (size_t)r * D;
-    T *y = static_cast<T *>(const_cast<void *>(isq ? p.q : p.k)) + (size_t)r * D;
+    T *y = static_cast<T *>(isq ? const_cast<void *>(p.q) : p.krot) + (size_t)r * D;
     if (item >= pitems) {  // past the rotary width: copy
       const unsigned c = p.rot_dim + (item - pitems) * VEC;
       *reinterpret_cast<uint4 *>(y + c) = *reinterpret_cast<const uint4 *>(x + c);
@@ -176,7 +176,7 @@ int resident_blocks(K kernel, int dev, cudaError_t *err) {
 }
 
 cudaError_t launch_rotary(const Params &p, cudaStream_t stream) {
-  const bool bf16 = p.rowbytes == p.D * 2;
+  const bool bf16 = p.qbytes == 2;
   const int vec = bf16 ? 8 : 4;  // elements per 16-byte vector
   const int half = p.rot_dim / 2;
   const long long rows = (long long)p.B * p.S * (p.Nq + p.Nkv);

@@ -22,6 +22,8 @@ GQAW_EDEVICE = 5
 GQAW_F32 = 0
 GQAW_BF16 = 1
 
+GQAW_I8 = 2
+GQAW_E4M3 = 3
 GQAW_DEV_BAD_SEQLEN = 1
 GQAW_DEV_TIMEOUT = 2
 GQAW_DEV_BAD_POSITION = 4
@@ -77,6 +79,9 @@ class gqaw_step_args(ctypes.Structure):
         ("cos_cache", ctypes.c_void_p),
         ("sin_cache", ctypes.c_void_p),
         ("position_ids", ctypes.c_void_p),
+        ("cache_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -197,7 +202,20 @@ def _dtype_code(t) -> int:
         return GQAW_F32
     if t.dtype == torch.bfloat16:
         return GQAW_BF16
-    raise TypeError("query/key/value/caches must be float32 or bfloat16, got %s" % t.dtype)
+    raise TypeError("query/key/value must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _cache_code(cache, query) -> int:
+    """0 when the caches hold the query's type; GQAW_I8 / GQAW_E4M3 for code caches."""
+    import torch
+
+    if cache.dtype == query.dtype:
+        return 0
+    if cache.dtype == torch.int8:
+        return GQAW_I8
+    if getattr(torch, "float8_e4m3fn", None) is not None and cache.dtype == torch.float8_e4m3fn:
+        return GQAW_E4M3
+    raise TypeError("caches must hold the query's type, int8 or float8_e4m3fn, got %s" % cache.dtype)
 
 
 def make_args(query, key, value, past_key, past_value, present_key, present_value, seqlens_k,
@@ -205,7 +223,7 @@ def make_args(query, key, value, past_key, past_value, present_key, present_valu
               output, workspace=None, scale: float = 0.0, softcap: float = 0.0, attention_bias=None,
               bias_strides=None, resident_len_out=None, split_keys: int = 0, head_sink=None,
               smooth_softmax: bool = False, cos_cache=None, sin_cache=None, position_ids=None,
-              rotary_interleaved: bool = False) -> gqaw_step_args:
+              rotary_interleaved: bool = False, k_scale=None, v_scale=None) -> gqaw_step_args:
     """Fill a ``gqaw_step_args`` from CUDA tensors (shapes as in include/gqaw.h).
 
     ``attention_bias``: fp32 tensor whose last dimension is contiguous; its (b, h, s)
@@ -215,7 +233,9 @@ def make_args(query, key, value, past_key, past_value, present_key, present_valu
     fp32 (num_heads,) CUDA tensor of sink logits; ``smooth_softmax``: a sink of 0.
     ``cos_cache``/``sin_cache``: contiguous (max_pos, rd/2) CUDA tensors of the step's
     dtype; giving them turns on the rotary embedding (rd = twice their width);
-    ``position_ids``: None or a contiguous int64 (B, S) CUDA tensor.
+    ``position_ids``: None or a contiguous int64 (B, S) CUDA tensor.  Caches of dtype
+    int8 or float8_e4m3fn make a quantized cache; ``k_scale`` / ``v_scale`` are then
+    one-element float32 CUDA tensors.
     """
     B, Nkv, C, D = past_key.shape
     S = query.shape[1]
@@ -223,7 +243,13 @@ def make_args(query, key, value, past_key, past_value, present_key, present_valu
     a.batch_size, a.sequence_length = int(B), int(S)
     a.num_heads, a.kv_num_heads, a.head_size = int(num_heads), int(kv_num_heads), int(D)
     a.capacity, a.local_window_size = int(C), int(local_window_size)
-    a.dtype = _dtype_code(past_key)
+    a.dtype = _dtype_code(query)
+    a.cache_dtype = _cache_code(past_key, query)
+    if a.cache_dtype:
+        for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if t is None or str(t.dtype) != "torch.float32" or t.numel() != 1:
+                raise ValueError("%s: a one-element float32 tensor is needed for a quantized cache" % name)
+        a.k_scale, a.v_scale = _ptr(k_scale), _ptr(v_scale)
     a.scale, a.softcap = float(scale), float(softcap)
     a.total_sequence_length, a.split_keys = int(total_sequence_length), int(split_keys)
     a.query, a.key, a.value = _ptr(query), _ptr(key), _ptr(value)
@@ -252,8 +278,8 @@ def make_args(query, key, value, past_key, past_value, present_key, present_valu
     if cos_cache is not None:
         if sin_cache is None or tuple(sin_cache.shape) != tuple(cos_cache.shape) or cos_cache.dim() != 2 \
                 or not (cos_cache.is_contiguous() and sin_cache.is_contiguous()) \
-                or cos_cache.dtype != past_key.dtype or sin_cache.dtype != past_key.dtype:
-            raise ValueError("cos_cache/sin_cache: equal contiguous (max_pos, rd/2) tensors of the cache dtype")
+                or cos_cache.dtype != query.dtype or sin_cache.dtype != query.dtype:
+            raise ValueError("cos_cache/sin_cache: equal contiguous (max_pos, rd/2) tensors of the query's dtype")
         a.do_rotary, a.rotary_interleaved = 1, int(bool(rotary_interleaved))
         a.rotary_dim, a.rotary_cache_len = 2 * int(cos_cache.shape[1]), int(cos_cache.shape[0])
         a.cos_cache, a.sin_cache = _ptr(cos_cache), _ptr(sin_cache)

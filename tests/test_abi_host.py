@@ -113,6 +113,11 @@ def test_workspace_bytes(lib):
     (dict(p_attention_bias=FAKE * 300 + 2), 1, "attention_bias"),
     (dict(p_attention_bias=FAKE * 300, p_bias_stride_h=-1), 1, "strides"),
     (dict(p_head_sink=FAKE * 300 + 2), 1, "head_sink"),
+    (dict(p_cache_dtype=5), 1, "cache_dtype"),
+    (dict(p_cache_dtype=2, dtype=0), 2, "GQAW_BF16"),
+    (dict(p_cache_dtype=3, head_size=32), 2, "head_size 64, 128 or 256"),
+    (dict(p_cache_dtype=2), 1, "k_scale and v_scale"),
+    (dict(p_cache_dtype=2, p_k_scale=FAKE * 300 + 2, p_v_scale=FAKE * 301), 1, "4-byte aligned"),
     (dict(p_do_rotary=1, p_rotary_dim=5, p_rotary_cache_len=8), 1, "rotary_dim"),
     (dict(p_do_rotary=1, p_rotary_dim=66, p_rotary_cache_len=8), 1, "rotary_dim"),
     (dict(p_do_rotary=1, p_rotary_cache_len=0), 1, "rotary_cache_len"),

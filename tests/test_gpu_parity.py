@@ -34,17 +34,20 @@ class Pair:
 
     def __init__(self, B, Nq, Nkv, D, C, W, dtype, scale=0.0, softcap=0.0, past_key=None, past_value=None,
                  inplace=True, split_keys=0, head_sink=None, smooth_softmax=False, cos_cache=None, sin_cache=None,
-                 rotary_interleaved=False):
+                 rotary_interleaved=False, cache_dtype=None, k_scale=1.0, v_scale=1.0):
         self.dtype = dtype
+        self.cache_dtype = cache_dtype
         self.turned = cos_cache is not None
         self.g = GpuCache(B, Nq, Nkv, D, C, W, dtype, scale, softcap, past_key, past_value, inplace, split_keys,
-                          head_sink, smooth_softmax, cos_cache, sin_cache, rotary_interleaved)
+                          head_sink, smooth_softmax, cos_cache, sin_cache, rotary_interleaved, cache_dtype, k_scale,
+                          v_scale)
         self.o = OracleCache(B, Nq, Nkv, D, C, W, oracle_dtype(dtype), scale, softcap,
                              None if past_key is None else wl.to_numpy(past_key),
                              None if past_value is None else wl.to_numpy(past_value),
                              None if head_sink is None else wl.to_numpy(head_sink), smooth_softmax,
                              None if cos_cache is None else wl.to_numpy(cos_cache),
-                             None if sin_cache is None else wl.to_numpy(sin_cache), rotary_interleaved)
+                             None if sin_cache is None else wl.to_numpy(sin_cache), rotary_interleaved,
+                             {None: None, "i8": oracle.I8, "e4m3": oracle.E4M3}[cache_dtype], k_scale, v_scale)
         self.errs = []
 
     def step(self, q, k, v, seqlens, total=None, bias=None, bias_strides=None, phases=False, position_ids=None):
@@ -52,7 +55,7 @@ class Pair:
         nb = None if bias is None else wl.to_numpy(bias).reshape(-1) if bias_strides else wl.to_numpy(bias)
         ro = self.o.step(wl.to_numpy(q), wl.to_numpy(k), wl.to_numpy(v), np.asarray(seqlens, np.int32), total,
                          nb, bias_strides, position_ids)
-        self.errs.append(compare(rg, ro, self.dtype, turned_keys=self.turned))
+        self.errs.append(compare(rg, ro, self.dtype, turned_keys=self.turned, cache_dtype=self.cache_dtype))
         return rg, ro
 
 

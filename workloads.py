@@ -121,6 +121,23 @@ def rope_tables(max_pos: int, half: int, dtype: str, base: float = 10000.0):
     return torch.cos(ang).to(td).contiguous(), torch.sin(ang).to(td).contiguous()
 
 
+def code_cache(sh: Shape, seed: int, cache_dtype: str, B: int | None = None):
+    """Random quantized-cache contents (B, Nkv, C, D): int8 codes ~ U{-100..100}, or fp8
+    e4m3 codes drawn as bytes with the two NaN codes replaced by zero."""
+    B = sh.B if B is None else B
+    g = generator(seed + 500009)
+    shape = (B, sh.Nkv, sh.C, sh.D)
+    out = []
+    for _ in range(2):
+        if cache_dtype == "i8":
+            out.append(torch.randint(-100, 101, shape, generator=g, dtype=torch.int8))
+        else:
+            c = torch.randint(0, 256, shape, generator=g, dtype=torch.int16).to(torch.uint8)
+            c[(c == 0x7F) | (c == 0xFF)] = 0
+            out.append(c.view(torch.float8_e4m3fn))
+    return out[0], out[1]
+
+
 def lengths(B: int, lo: int, hi: int, seed: int) -> np.ndarray:
     """Per-item token counts T_b ~ U{lo..hi} (inclusive), int64."""
     rng = np.random.Generator(np.random.Philox(seed + 300007))
@@ -142,6 +159,8 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
         return t.numpy()
     if t.dtype == torch.int32:
         return t.numpy()
+    if t.dtype == torch.int8 or str(t.dtype) == "torch.float8_e4m3fn":  # quantized-cache codes
+        return t.view(torch.uint8).numpy()
     raise TypeError(t.dtype)
 
 
