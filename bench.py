@@ -6,8 +6,8 @@ decode token for all 64 items through the C ABI.  The K/V window read per step
 (about 1.07 GB) is larger than the 129 MB L2, so no flush is needed between steps.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl gqaw|reference]
-                    [--workload longctx-decode|longctx-decode-sink|longctx-decode-rope|pages-decode|slack-decode|verify8|
-                     longctx-prefill|longctx-prefill-rope]
+                    [--workload longctx-decode|longctx-decode-sink|longctx-decode-rope|longctx-decode-i8|
+                     longctx-decode-e4m3|pages-decode|slack-decode|verify8|longctx-prefill|longctx-prefill-rope]
                     [--no-extra] [--no-cpu-baseline]
 
 ``--impl reference`` times the oracle (the plain fp64 CPU implementation) on this
@@ -51,6 +51,9 @@ def workload_spec(name):
     if name == "longctx-decode-sink":  # the same decode with a sink logit per query head
         return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False,
                     sink=True)
+    if name in ("longctx-decode-i8", "longctx-decode-e4m3"):  # the same decode on a quantized cache
+        return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False,
+                    quant=name.rsplit("-", 1)[1])
     if name == "longctx-decode-rope":  # the same decode with the rotary embedding fused in
         return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False,
                     rope=True)
@@ -75,7 +78,8 @@ def workload_config(name, B=None):
     return {"workload": name, "B": B if B else spec.get("B", sh.B), "S": spec["S"], "num_heads": sh.Nq,
             "kv_num_heads": sh.Nkv, "head_size": sh.D, "local_window_size": sh.W, "capacity": sh.C,
             "cache_dtype": sh.dtype, "softcap": sh.softcap, "bias": spec["bias"],
-            "head_sink": bool(spec.get("sink", False)), "rotary": bool(spec.get("rope", False)), "contexts": "U[%d,%d]" % (spec["lo"], spec["hi"])}
+            "head_sink": bool(spec.get("sink", False)), "rotary": bool(spec.get("rope", False)),
+            "kv_cache": spec.get("quant") or sh.dtype, "contexts": "U[%d,%d]" % (spec["lo"], spec["hi"])}
 
 
 def resident_len(T, C, W):
@@ -85,12 +89,13 @@ def resident_len(T, C, W):
     return gqaw.gqaw_resident_len(int(T), int(C), int(W))
 
 
-def algorithmic_bytes(sh, S, T_before, B):
+def algorithmic_bytes(sh, S, T_before, B, cache_bytes=None):
     """Bytes the step must move (in-window cache rows + new rows read, append written,
     compaction read + written, Q in, output out), per item, from the pre-step lengths.
-    Bias bytes are added by the caller."""
+    ``cache_bytes``: bytes of a cache element (1 for a quantized cache).  Bias bytes are
+    added by the caller."""
     e = 2 if sh.dtype == "bf16" else 4
-    row = sh.Nkv * sh.D * e * 2  # K and V of one position, all kv heads
+    row = sh.Nkv * sh.D * (cache_bytes or e) * 2  # K and V of one position, all kv heads
     attn = comp = app = 0
     for b in range(B):
         P = int(T_before[b])
@@ -195,8 +200,10 @@ KERNELS = {
 }
 
 
-def attention_kernel(sh, S):
+def attention_kernel(sh, S, quant=None):
     g = sh.Nq // sh.Nkv
+    if quant:
+        return "attend"
     if sh.dtype == "bf16" and sh.D == 128 and S * g <= 32:
         return "mmad"
     if sh.dtype == "bf16" and sh.D == 128 and S >= 2 and g <= 32 and 32 % g == 0:
@@ -277,7 +284,10 @@ class Harness:
         n = steps + warmup
         self.n = n
         B, S = self.B, self.S
-        pk, pv = wl.cache(sh, seed, B=self.B)
+        self.quant = spec.get("quant")
+        pk, pv = wl.code_cache(sh, seed, self.quant, B=self.B) if self.quant else wl.cache(sh, seed, B=self.B)
+        self.ks = torch.tensor([0.02 if self.quant == "i8" else 0.01], dtype=torch.float32, device=self.dev)
+        self.vs = torch.tensor([0.025 if self.quant == "i8" else 0.005], dtype=torch.float32, device=self.dev)
         self.pk, self.pv = pk.to(self.dev), pv.to(self.dev)
         del pk, pv
         T0 = wl.lengths(B, spec["lo"], spec["hi"], seed)
@@ -331,7 +341,7 @@ class Harness:
             self.q[i], self.k[i], self.v[i], self.pk, self.pv, self.pk, self.pv, self.seq[t], self.totals[t],
             sh.Nq, sh.Nkv, sh.W, self.out, workspace=ws, softcap=sh.softcap, attention_bias=self.bias,
             bias_strides=self.bias_strides, split_keys=self.split_keys, head_sink=self.head_sink,
-            cos_cache=self.cos, sin_cache=self.sin)
+            cos_cache=self.cos, sin_cache=self.sin, k_scale=self.ks, v_scale=self.vs)
 
     def step(self, t):
         self.gqaw.check(self.gqaw.gqa_windowed_step(self.args[t], self.stream.cuda_stream))
@@ -361,7 +371,7 @@ class Harness:
             self.q[0], self.k[0], self.v[0], self.pk, self.pv, self.pk, self.pv, self.seq[t], self.totals[t],
             sh.Nq, sh.Nkv, sh.W, self.out, workspace=self.ws, softcap=sh.softcap, attention_bias=self.bias,
             bias_strides=self.bias_strides, split_keys=self.split_keys, head_sink=self.head_sink,
-            cos_cache=self.cos, sin_cache=self.sin) for t in range(self.n)]
+            cos_cache=self.cos, sin_cache=self.sin, k_scale=self.ks, v_scale=self.vs) for t in range(self.n)]
         e = self.q_host[0].element_size()
         self.h2d = (self.q_host[0].numel() + self.k_host[0].numel() + self.v_host[0].numel()) * e + self.B * 4
         self.d2h = self.out.numel() * self.out.element_size()
@@ -449,7 +459,7 @@ def run_gpu(args, rank, world):
     att_bytes = step_bytes = 0.0
     bias_bytes = 0.0
     for t in range(Wm, Wm + K):
-        a, s = algorithmic_bytes(sh, S, h.T[t], B)
+        a, s = algorithmic_bytes(sh, S, h.T[t], B, 1 if h.quant else None)
         att_bytes += a
         step_bytes += s
         if h.bias is not None:
@@ -474,7 +484,7 @@ def run_gpu(args, rank, world):
     if attend_ms is not None:
         am = statistics.mean(attend_ms)
         ach = att_bytes / K / (am / 1e3) / 1e9
-        kern = attention_kernel(sh, S)
+        kern = attention_kernel(sh, S, h.quant)
         traffic = profiled_traffic(name, kern)
         result["roofline"] = {"kernel": KERNELS[kern][0], "bound": "hbm", "achieved": ach, "peak": peak,
                               "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
@@ -513,7 +523,7 @@ def extra_workloads(main, args):
 
     out = {}
     for name in ("pages-decode", "slack-decode", "verify8", "longctx-prefill", "longctx-decode-sink",
-                 "longctx-decode-rope", "longctx-prefill-rope"):
+                 "longctx-decode-rope", "longctx-prefill-rope", "longctx-decode-i8", "longctx-decode-e4m3"):
         if name == main:
             continue
         K = 8 if name.startswith("longctx-prefill") else 64
@@ -542,7 +552,7 @@ def extra_workloads(main, args):
         torch.cuda.synchronize()
         check_device(h, name)
         ms = e0.elapsed_time(e1) / K
-        _, sb = algorithmic_bytes(h.sh, h.S, h.T[Wm], h.B)
+        _, sb = algorithmic_bytes(h.sh, h.S, h.T[Wm], h.B, 1 if h.quant else None)
         if h.bias is not None:
             sb += 4 * h.sh.Nq * visible_columns(h.S, h.T[Wm], h.sh.W)
         hbm, _ = measured_peaks()
@@ -557,7 +567,7 @@ def extra_workloads(main, args):
                     flops += h.sh.Nq * 4 * h.sh.D * min(int(P) + s + 1, h.sh.W)
             entry["tflops"] = flops / (ms / 1e3) / 1e12
             entry["tensor_frac"] = entry["tflops"] / bf16_peak_tflops()
-        entry["kernel"] = KERNELS[attention_kernel(h.sh, h.S)][0]
+        entry["kernel"] = KERNELS[attention_kernel(h.sh, h.S, h.quant)][0]
         out[name] = entry
         torch.cuda.synchronize()
         torch.cuda.set_stream(torch.cuda.default_stream())
@@ -592,7 +602,8 @@ def oracle_item_step(name, seed, b_items, t_index=0):
     for b in b_items:
         ckey = ("cache", name, seed, b % 8)  # eight distinct caches serve every item: timing only
         if ckey not in _ORACLE_INPUTS:
-            pk, pv = wl.cache(sh, seed * 7919 + b % 8, B=1)
+            pk, pv = (wl.code_cache(sh, seed * 7919 + b % 8, spec["quant"], B=1) if spec.get("quant")
+                      else wl.cache(sh, seed * 7919 + b % 8, B=1))
             _ORACLE_INPUTS[ckey] = (wl.to_numpy(pk), wl.to_numpy(pv))
         npk, npv = _ORACLE_INPUTS[ckey]
         seq = (T0[b:b + 1] + S - 1).astype(np.int32)
@@ -606,8 +617,13 @@ def oracle_item_step(name, seed, b_items, t_index=0):
             cos, sin = wl.rope_tables(int(seq.max()) + 1, sh.D // 2, sh.dtype)
             rope = dict(cos_cache=wl.to_numpy(cos), sin_cache=wl.to_numpy(sin))
         t0 = time.perf_counter()
+        quant = {}
+        if spec.get("quant"):
+            quant = dict(cache_dtype=oracle.I8 if spec["quant"] == "i8" else oracle.E4M3,
+                         k_scale=0.02 if spec["quant"] == "i8" else 0.01,
+                         v_scale=0.025 if spec["quant"] == "i8" else 0.005)
         oracle.step(nq[b:b + 1], nk[b:b + 1], nv[b:b + 1], npk, npv, seq, total, sh.Nq, sh.Nkv, sh.W,
-                    softcap=sh.softcap, attention_bias=bias, dtype=odt, head_sink=sink, **rope)
+                    softcap=sh.softcap, attention_bias=bias, dtype=odt, head_sink=sink, **rope, **quant)
         el += time.perf_counter() - t0
     return el
 
