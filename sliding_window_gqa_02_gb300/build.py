@@ -21,7 +21,8 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libgqaw.so")
 
 SOURCES = ["gqaw_host.cu", "gqaw_finish.cu", "gqaw_attend_f32.cu", "gqaw_attend_bf16.cu", "gqaw_noalloc.cu", "gqaw_mma.cu",
-           "gqaw_rotary.cu", "gqaw_mmad.cu", "gqaw_attend_q8.cu", "gqaw_quant.cu"]
+           "gqaw_rotary.cu", "gqaw_mmad.cu", "gqaw_attend_q8.cu", "gqaw_quant.cu",
+           "gqaw_mmad_q8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
 

@@ -65,6 +65,7 @@ struct Launch {
   int qsize;              // query/key/value/output element bytes
   int quant;              // cache_dtype of a quantized cache, or 0
   size_t off_kq, off_vq;  // quantized cache: the codes of the step's new rows
+  size_t off_q16;         // quantized cache on the tensor-core kernel: the fp16 query copy
   long long units, ctas, ncopy;
   size_t off_list, off_tickets, off_partials, ws_bytes;
   int rot_dim;            // > 0: the rotary embedding is on, over this many dimensions
@@ -201,8 +202,8 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   // on the MMA's M dimension: persistent, one CTA per SM, stream-K over (unit, 128-key
   // tile); partial results of units cut by a CTA range are merged in the kernel.
   const long long rows_all = (long long)a->batch_size * a->kv_num_heads * a->capacity;
-  if (L->quant) L->tc = false;  // quantized caches: the FFMA kernel with a code type
-  L->td = !L->quant && a->dtype == GQAW_BF16 && a->head_size == 128 && (long long)a->sequence_length * L->group <= 32 &&
+  if (L->quant) L->tc = false;  // quantized caches: the FFMA kernel, or the small-step kernel below
+  L->td = a->dtype == GQAW_BF16 && a->head_size == 128 && (long long)a->sequence_length * L->group <= 32 &&
           rows_all < 0x7fffffffLL && (long long)a->batch_size * a->sequence_length < 0x7fffffffLL;
   if (L->td) {
     L->tc = false;
@@ -235,6 +236,11 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     L->off_kq = align256(L->ws_bytes);
     L->off_vq = L->off_kq + align256(n);
     L->ws_bytes = L->off_vq + align256(n);
+  }
+  L->off_q16 = 0;
+  if (L->quant && L->td) {
+    L->off_q16 = L->ws_bytes;
+    L->ws_bytes += align256((size_t)a->batch_size * a->sequence_length * a->num_heads * a->head_size * 2);
   }
   return GQAW_OK;
 }
@@ -383,6 +389,7 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
     p->v = ws + L.off_vq;
     p->ks = a->k_scale;
     p->vs = a->v_scale;
+    p->q16 = L.td ? ws + L.off_q16 : nullptr;
   }
 }
 
@@ -416,11 +423,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // A bf16 tensor map with 128-byte swizzle; dims/box innermost first, strides in bytes.
 bool encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                const cuuint32_t *box) {
+                const cuuint32_t *box, CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, es,
+  return fn(m, type, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -460,9 +467,15 @@ gqaw_status run_mmad(const gqaw_step_args *a, const Launch &L, const gqaw::Param
   const cuuint64_t c_dims[2] = {D, rows};
   const cuuint64_t c_str[1] = {D * 2};
   const cuuint32_t c_box[2] = {64, 128};
-  if (!encode_map(&maps.q, p.q, 3, q_dims, q_str, q_box) ||
-      !encode_map(&maps.kc, a->past_key, 2, c_dims, c_str, c_box) ||
-      !encode_map(&maps.vc, a->past_value, 2, c_dims, c_str, c_box))
+  // quantized cache: 128 one-byte codes per row, one 128 x 128 box per tile; fp16 query
+  const cuuint64_t c8_str[1] = {D};
+  const cuuint32_t c8_box[2] = {128, 128};
+  const bool q8 = L.quant != 0;
+  const CUtensorMapDataType qt = q8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType ct = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_map(&maps.q, q8 ? p.q16 : p.q, 3, q_dims, q_str, q_box, qt) ||
+      !encode_map(&maps.kc, a->past_key, 2, c_dims, q8 ? c8_str : c_str, q8 ? c8_box : c_box, ct) ||
+      !encode_map(&maps.vc, a->past_value, 2, c_dims, q8 ? c8_str : c_str, q8 ? c8_box : c_box, ct))
     return fail(GQAW_ECUDA, "cuTensorMapEncodeTiled failed for the small-step kernel");
   const cudaError_t e = gqaw::launch_mmad(p, L.tda, maps, (int)L.td_ctas, st);
   if (e != cudaSuccess) return cuda_fail(e, "small-step tensor-core kernel launch");
@@ -480,6 +493,7 @@ gqaw_status run_attend(const gqaw_step_args *a, const Launch &L, const gqaw::Par
     const cudaError_t e = gqaw::launch_quantize(p, (int)(kSms * 8), st);
     if (e != cudaSuccess) return cuda_fail(e, "quantize kernel launch");
     g_launches.fetch_add(1);
+    if (L.td) return run_mmad(a, L, p, st);
     const cudaError_t e2 = gqaw::launch_attend_q8(p, L.gb, (int)L.ctas, st);
     if (e2 != cudaSuccess) return cuda_fail(e2, "attention kernel launch");
     g_launches.fetch_add(1);

@@ -57,6 +57,7 @@ struct Params {
   int quant;
   const void *kq_in, *vq_in;
   const float *ks, *vs;
+  void *q16;                 // NULL, or an fp16 copy of the query rows for the tensor-core kernel
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -159,6 +160,47 @@ template <> struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static __nv_bfloat16 store(float x) { return __float2bfloat16_rn(x); }
   __device__ __forceinline__ static float load(__nv_bfloat16 x) { return __bfloat162float(x); }
 };
+
+// Float pairs out of a 16-byte vector of elements: pair j covers elements 2j and 2j+1.
+template <typename T> struct Pairs;
+template <> struct Pairs<float> {
+  // pair j (0..1) of a 16-byte vector of 4 floats
+  __device__ __forceinline__ static float2 get(const uint4 &u, int j) {
+    return j == 0 ? make_float2(__uint_as_float(u.x), __uint_as_float(u.y))
+                  : make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+  }
+};
+template <> struct Pairs<__nv_bfloat16> {
+  // pair j (0..3) of a 16-byte vector of 8 bfloat16: widening is a shift (exact)
+  __device__ __forceinline__ static float2 get(const uint4 &u, int j) {
+    const uint32_t w = j == 0 ? u.x : (j == 1 ? u.y : (j == 2 ? u.z : u.w));
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+};
+template <> struct Pairs<CodeI8> {
+  // pair j (0..7) of a 16-byte vector of 16 int8 codes, as floats (exact): the byte,
+  // biased by 128, is placed in the low mantissa bits of 2^23, which is then subtracted
+  // with the bias
+  __device__ __forceinline__ static float2 get(const uint4 &u, int j) {
+    const uint32_t w = (j < 2 ? u.x : (j < 4 ? u.y : (j < 6 ? u.z : u.w))) ^ 0x80808080u;
+    const uint32_t b = (j & 1) * 2;  // first byte of the pair in the word
+    const float lo = __uint_as_float(__byte_perm(w, 0x4B000000u, b | 0x7540u)) - 8388736.f;
+    const float hi = __uint_as_float(__byte_perm(w, 0x4B000000u, (b + 1) | 0x7540u)) - 8388736.f;
+    return make_float2(lo, hi);
+  }
+};
+template <> struct Pairs<CodeE4M3> {
+  // pair j (0..7) of a 16-byte vector of 16 fp8 e4m3 codes, as floats (exact): the
+  // hardware pair conversion to half precision, then widening
+  __device__ __forceinline__ static float2 get(const uint4 &u, int j) {
+    const uint32_t w = j < 2 ? u.x : (j < 4 ? u.y : (j < 6 ? u.z : u.w));
+    const uint16_t pair = (uint16_t)(w >> ((j & 1) * 16));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+  }
+};
+
 
 // ---------------------------------------------------------------- mbarrier + bulk copy
 

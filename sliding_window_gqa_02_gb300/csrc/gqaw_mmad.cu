@@ -1,805 +1,14 @@
-// gqaw_mmad.cu -- windowed GQA attention for small steps (decode, short verify) on the
-// 5th-generation tensor cores, with the keys as the MMA's M dimension.
-//
-// What it computes is the same as the other attention kernels: the query of token s
-// (absolute position i = P + s) attends keys i - W < j <= i (onnxruntime PR #34226 "Fix
-// CPU Attention causal mask for q_len=1 with past_key and kv_len > 1", Description),
-// logit softcap * tanh(scale q.k / softcap) + bias[b, h, s, j] with j the absolute key
-// position (PR #32419 "Specify GroupQueryAttention windowed KV cache layout contract",
-// Description), keys before P from the pre-step cache rows and keys from P on from the
-// step's new rows -- no staging copy (PR #31142 "[CPU] Add windowed kv cache for GQA",
-// "Staging for hazardous steps"): this kernel runs before any cache row moves.
-//
-// Design.  A unit is (item, kv head): all S x g query rows of a step that share its
-// K/V rows, at most 32, padded to NPAD = 16 or 32.  With so few query rows the usual
-// orientation (query rows as M = 128) would waste most of the tensor core and leave the
-// per-key work on the CUDA cores; here the contractions run transposed:
-//   S^T = K Q^T      M = 128 keys of a tile, N = NPAD query rows, K = 128 dims
-//   O^T += V^T P^T   M = 128 dims, N = NPAD query rows, K = 128 keys
-// so one thread of the four softmax warps owns one key (a TMEM lane) and the logits of
-// the unit's rows (S x g of the NPAD, rounded up to 4, 8, 16 or 32), and the fp32
-// accumulator O^T lives in tensor memory (lane = head dimension).
-// The online softmax keeps one reference maximum per query row, uniform over the CTA;
-// it moves only when a tile's logit exceeds it by more than 2^8 (a vote through a
-// reducing barrier), so the common tile needs no cross-thread reduction: each thread
-// sums its own probabilities and the sums are reduced once per unit.
-//
-// The cache rows [lo, P) come in tiles of 128 keys by TMA (128-byte swizzle) through a
-// three-stage ring; the S new rows of the step, which live in the input tensors, are
-// added when the unit is finished (their logits and values are read directly), so no
-// tile ever mixes the two sources.  Warp roles: four or eight softmax warps (each owning
-// a quarter of the keys and half or all of the query rows), then one warp whose first
-// thread is the TMA producer and one whose first thread issues the MMAs; they meet at
-// mbarriers.  Persistent stream-K over the (unit, key tile) sequence, as in the decode
-// kernel: a unit cut by a CTA range boundary is merged by its last contributor.
-//
-// Every mbarrier wait is bounded; a wait that expires flags GQAW_DEV_TIMEOUT and the
-// CTA winds down.  The softmax warps decide to stop only through a reducing barrier,
-// so they always meet at the same named barriers.
-#include <cuda.h>
-
-#include <atomic>
-
-#include "gqaw_tc.cuh"
+// gqaw_mmad.cu -- the small-step tensor-core kernel (gqaw_mmad.cuh) for bf16 caches,
+// and the dispatch to the quantized-cache instantiations.
+#include "gqaw_mmad.cuh"
 
 namespace gqaw {
 
-namespace {
-
-constexpr int kKeys = 128;                 // keys per tile (M of S^T = K Q^T)
-constexpr int kD = 128;                    // head size (M of O^T = V^T P^T)
-constexpr int kHalf = 16384;               // one 64-dim half of a K or V tile
-constexpr int kStages = 3;
-constexpr int kStageBytes = 4 * kHalf;     // K and V, two halves each
-constexpr float kRescale = 8.0f;           // lazy rescale threshold (log2 units)
-constexpr int kBar = 1;                    // named barrier of the softmax warps
-constexpr int kNumBars = 20;
-
-template <int NPAD>
-struct Lay {
-  static constexpr int kQHalf = NPAD * 128;                 // a 64-column half of Q or P^T
-  static constexpr int kQ = kStages * kStageBytes;          // two Q buffers
-  static constexpr int kP = kQ + 4 * kQHalf;                // two P^T buffers
-  static constexpr int kRed = kP + 4 * kQHalf;              // float [4][NPAD]
-  // The epilogue's logits of the step's own keys, float [NPAD][NPAD], live in the
-  // first rows of P^T buffer 0: those rows are rewritten by every tile.
-  static constexpr int kZn = kP;
-  static constexpr int kFin = kRed + 4 * NPAD * 4;          // float m, l, f [3][NPAD]
-  static constexpr int kBrow = kFin + 4 * NPAD * 4;         // long long [NPAD]
-  static constexpr int kBars = kBrow + NPAD * 8;            // mbarriers
-  static constexpr int kSlot = kBars + kNumBars * 8;        // TMEM base address
-  static constexpr int kTotal = kSlot + 16;
-  static constexpr int kAlloc = kTotal + 1024;              // room to align the base
-  static constexpr uint32_t kCols = NPAD == 16 ? 64 : 128;  // S^T x2 and O^T
-};
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// tanh(x) = 1 - 2 / (e^(2x) + 1), absolute error about 1e-7.
-__device__ __forceinline__ float fast_tanh(float x) {
-  const float e = fast_exp2(2.8853900817779268f * fminf(fmaxf(x, -15.f), 15.f));
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
-  return fmaf(-2.f, r, 1.f);
-}
-
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]);
-template <>
-__device__ __forceinline__ void tmem_ld<4>(uint32_t taddr, float (&v)[4]) {
-  uint32_t r[4];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
-}
-template <>
-__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16]) {
-  tc::tmem_ld16(taddr, v);
-}
-template <>
-__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&v)[32]) {
-  tc::tmem_ld32(taddr, v);
-}
-template <int N>
-__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[N]);
-template <>
-__device__ __forceinline__ void tmem_st<4>(uint32_t taddr, const float (&v)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
-               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-               "r"(__float_as_uint(v[3]))
-               : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-template <>
-__device__ __forceinline__ void tmem_st<8>(uint32_t taddr, const float (&v)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
-               : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-template <>
-__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const float (&v)[16]) {
-  tc::tmem_st16(taddr, v);
-}
-template <>
-__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const float (&v)[32]) {
-  tc::tmem_st32(taddr, v);
-}
-
-// A unit (item, kv head) and its cache keys [lo, P) in `real` tiles of 128.
-struct DUnit {
-  int b, kvh;
-  bool ok;
-  Plan pl;
-  long long lo;
-  int real;
-};
-
-__device__ __forceinline__ DUnit dunit(const Params &p, long long u) {
-  DUnit x;
-  x.b = (int)(u / p.Nkv);
-  x.kvh = (int)(u % p.Nkv);
-  x.ok = plan_item(p, x.b, x.pl);
-  x.lo = 0;
-  x.real = 0;
-  if (x.ok) {
-    x.lo = x.pl.P - p.W + 1 > 0 ? x.pl.P - p.W + 1 : 0;
-    x.real = (int)((x.pl.P - x.lo + kKeys - 1) / kKeys);
-  }
-  return x;
-}
-
-// The CTA whose range holds virtual tile x (CTA c covers [c*V/G, (c+1)*V/G)).
-__device__ __forceinline__ long long owner_cta(long long x, long long V, long long G) {
-  return ((x + 1) * G - 1) / V;
-}
-
-// One real key tile of the CTA's sequence, as the producer and MMA threads walk it.
-struct DTile {
-  DUnit x;
-  int lt;       // tile index within the unit
-  int kc;       // index among this CTA's real tiles (ring stage, barrier phases)
-  int ui;       // index among this CTA's units with real tiles (Q buffer, phases)
-  bool first;   // first real tile of the unit in this CTA
-  bool last;    // last one
-};
-
-struct Walker {
-  long long u, ulast, tb, te, TPU;
-  int lt, r1, kc, ui;
-  DUnit x;
-  __device__ bool next(const Params &p, DTile &t) {
-    bool first = false;
-    while (lt >= r1) {
-      if (++u > ulast) return false;
-      x = dunit(p, u);
-      const long long lt0 = tb - u * TPU > 0 ? tb - u * TPU : 0;
-      const long long lt1 = te - u * TPU < TPU ? te - u * TPU : TPU;
-      lt = (int)lt0;
-      r1 = x.ok ? (int)(lt1 < x.real ? lt1 : x.real) : 0;
-      if (lt < r1) {
-        ++ui;
-        first = true;
-      }
-    }
-    t.x = x;
-    t.lt = lt;
-    t.kc = kc++;
-    t.ui = ui;
-    t.first = first;
-    t.last = lt + 1 == r1;
-    ++lt;
-    return true;
-  }
-};
-
-}  // namespace
-
-// NPAD: query rows of the MMA (16 or 32); NVT: query rows the softmax warps process
-// (the unit's S x g rounded up to 4, 8, 16 or 32; rows past S x g are zero); CG: column
-// groups.  4 * CG softmax warps: warps w and w + 4 read the same TMEM lanes (the same
-// keys, the same head dimensions) and own different query rows, NC = NVT / CG each.
-template <int NPAD, int NVT, int CG>
-__global__ void __launch_bounds__(32 * (4 * CG + 2), 1)
-    mma_decode_kernel(const Params p, const TdArgs ta, const __grid_constant__ TdMaps maps) {
-  static_assert(NVT <= NPAD && NVT % CG == 0, "processed rows within the MMA rows");
-  constexpr int NC = NVT / CG;              // query rows per softmax thread
-  constexpr int kSoft = 128 * CG;           // softmax threads
-  constexpr int kProducer = 4 * CG;         // warp of the TMA producer; the MMA issuer is the next
-  using L = Lay<NPAD>;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float *red = reinterpret_cast<float *>(smem + L::kRed);
-  float *zn = reinterpret_cast<float *>(smem + L::kZn);
-  float *fin_m = reinterpret_cast<float *>(smem + L::kFin), *fin_l = fin_m + NPAD, *fin_f = fin_l + NPAD;
-  long long *brow = reinterpret_cast<long long *>(smem + L::kBrow);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBars);
-  uint64_t *full = bars, *empty = bars + 3, *s_full = bars + 6, *s_free = bars + 8;
-  // p_full[2] and o_done[2] are per P^T buffer: the softmax warps may run one tile
-  // ahead of the MMA thread, so a single barrier could complete two phases before the
-  // MMA thread looks at it, and a parity wait cannot tell two phases apart.
-  uint64_t *p_full = bars + 10, *o_done = bars + 12, *o_free = bars + 14;
-  uint64_t *q_full = bars + 15, *q_free = bars + 17, *mma_done = bars + 19;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kSlot);
-  __shared__ int s_abort, s_last;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long TPU = ta.tpu, V = ta.units * TPU, G = gridDim.x, cta = blockIdx.x;
-  const long long tb = cta * V / G, te = (cta + 1) * V / G;  // this CTA's virtual tiles
-  const long long ufirst = tb / TPU, ulast = (te - 1) / TPU;
-  const int g = p.group, S = p.S, NV = S * g;  // valid query rows of a unit
-
-  if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoft);
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_free[i], 1);
-      mbar_init(&p_full[i], kSoft);
-      mbar_init(&o_done[i], 1);
-    }
-    mbar_init(o_free, kSoft);
-    mbar_init(mma_done, 1);
-    mbar_fence_init();
-    s_abort = 0;
-  }
-  // Q and P^T rows past the unit's query rows stay zero for the whole kernel.
-  for (int e = tid; e < (8 * L::kQHalf) / 16; e += blockDim.x)
-    reinterpret_cast<uint4 *>(smem + L::kQ)[e] = make_uint4(0, 0, 0, 0);
-  if (warp == 0) tc::tmem_alloc(tmem_slot, L::kCols);
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 2 * NPAD;
-  pdl_wait();                // the previous kernel in the stream has completed
-
-  auto stage = [&](int kc) { return smem + (kc % kStages) * kStageBytes; };
-  auto qbuf = [&](int ui) { return smem + L::kQ + (ui & 1) * 2 * L::kQHalf; };
-  auto pbuf = [&](int kc) { return smem + L::kP + (kc & 1) * 2 * L::kQHalf; };
-
-  if (warp == kProducer) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first(), qpol = tc::policy_evict_last();
-      Walker w{ufirst - 1, ulast, tb, te, TPU, 0, 0, 0, -1, DUnit()};
-      DTile t;
-      int issued = 0, qissued = -1;
-      bool alive = true;
-      while (alive && !*reinterpret_cast<volatile int *>(&s_abort) && w.next(p, t)) {
-        const DUnit &x = t.x;
-        if (t.first) {
-          if (t.ui >= 2 && !mbar_wait(&q_free[t.ui & 1], ((t.ui - 2) >> 1) & 1)) {
-            alive = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&q_full[t.ui & 1], (uint32_t)(2 * NV * 128));
-          tc::tma_load_3d(qbuf(t.ui), &maps.q, 0, x.kvh * g, x.b * S, &q_full[t.ui & 1], qpol);
-          tc::tma_load_3d(qbuf(t.ui) + L::kQHalf, &maps.q, 64, x.kvh * g, x.b * S, &q_full[t.ui & 1], qpol);
-          qissued = t.ui;
-        }
-        const int st = t.kc % kStages;
-        if (t.kc >= kStages && !mbar_wait(&empty[st], ((t.kc / kStages) - 1) & 1)) {
-          alive = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&full[st], kStageBytes);
-        const int row = (int)(((long long)x.b * p.Nkv + x.kvh) * p.C + (x.lo + (long long)t.lt * kKeys - x.pl.P + x.pl.Lp));
-        unsigned char *sb = stage(t.kc);
-        tc::tma_load_2d(sb, &maps.kc, 0, row, &full[st], pol);
-        tc::tma_load_2d(sb + kHalf, &maps.kc, 64, row, &full[st], pol);
-        tc::tma_load_2d(sb + 2 * kHalf, &maps.vc, 0, row, &full[st], pol);
-        tc::tma_load_2d(sb + 3 * kHalf, &maps.vc, 64, row, &full[st], pol);
-        ++issued;
-      }
-      if (!alive) {
-        flag(p, GQAW_DEV_TIMEOUT);
-        s_abort = 1;
-      }
-      // no copy may still be landing in shared memory when the CTA exits
-      for (int k = issued - kStages > 0 ? issued - kStages : 0; k < issued; ++k)
-        if (!mbar_wait(&full[k % kStages], (k / kStages) & 1)) flag(p, GQAW_DEV_TIMEOUT);
-      for (int q = qissued - 1 > 0 ? qissued - 1 : 0; q <= qissued; ++q)
-        if (q >= 0 && !mbar_wait(&q_full[q & 1], (q >> 1) & 1)) flag(p, GQAW_DEV_TIMEOUT);
-    }
-  } else if (warp == kProducer + 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kKeys, NPAD, 0, 0);  // K: K-major, Q: K-major
-      constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kD, NPAD, 1, 0);     // V^T: MN-major, P^T: K-major
-      Walker w{ufirst - 1, ulast, tb, te, TPU, 0, 0, 0, -1, DUnit()};
-      auto mma_s = [&](const DTile &t) -> bool {
-        if (t.first && !mbar_wait(&q_full[t.ui & 1], (t.ui >> 1) & 1)) return false;
-        if (!mbar_wait(&full[t.kc % kStages], (t.kc / kStages) & 1)) return false;
-        if (t.kc >= 2 && !mbar_wait(&s_free[t.kc & 1], ((t.kc - 2) >> 1) & 1)) return false;
-        tc::fence_after_sync();
-        unsigned char *kb = stage(t.kc), *qb = qbuf(t.ui);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const int half = kk / 4, off = (kk % 4) * 32;
-          const uint64_t a = tc::smem_desc_sw128(kb + half * kHalf + off, 16, 1024);
-          const uint64_t bq = tc::smem_desc_sw128(qb + half * L::kQHalf + off, 16, 1024);
-          tc::mma_bf16_ss(tmem_s + (t.kc & 1) * NPAD, a, bq, kIdescS, kk > 0);
-        }
-        tc::mma_commit(&s_full[t.kc & 1]);
-        return true;
-      };
-      DTile cur, nxt;
-      bool hc = w.next(p, cur), fine = true;
-      if (hc) fine = mma_s(cur);
-      while (hc && fine && !*reinterpret_cast<volatile int *>(&s_abort)) {
-        const bool hn = w.next(p, nxt);
-        if (hn && !mma_s(nxt)) {  // S^T of the next tile while this one is in softmax
-          fine = false;
-          break;
-        }
-        if (!mbar_wait(&p_full[cur.kc & 1], (cur.kc >> 1) & 1) ||
-            (cur.first && cur.ui >= 1 && !mbar_wait(o_free, (cur.ui - 1) & 1))) {
-          fine = false;
-          break;
-        }
-        tc::fence_after_sync();
-        unsigned char *vb = stage(cur.kc) + 2 * kHalf;
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          // V^T: M = dims in two 64-dim halves 16 KB apart, K = keys in 8-key groups 1 KB apart
-          const uint64_t a = tc::smem_desc_sw128(vb + kk * 16 * 128, kHalf, 1024);
-          const uint64_t bp = tc::smem_desc_sw128(pbuf(cur.kc) + (kk / 4) * L::kQHalf + (kk % 4) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem_o, a, bp, kIdescO, !(cur.first && kk == 0));
-        }
-        tc::mma_commit(&o_done[cur.kc & 1]);
-        tc::mma_commit(&empty[cur.kc % kStages]);
-        if (cur.last) tc::mma_commit(&q_free[cur.ui & 1]);
-        cur = nxt;
-        hc = hn;
-      }
-      if (!fine) {
-        flag(p, GQAW_DEV_TIMEOUT);
-        s_abort = 1;
-      }
-      tc::mma_commit(mma_done);  // every MMA issued has completed before TMEM is released
-      if (!mbar_wait(mma_done, 0)) flag(p, GQAW_DEV_TIMEOUT);
-    }
-  } else {
-    // ------------------------------------------------------------ softmax warps
-    const int t = tid & 127;       // key of a tile (S^T lane) and head dimension (O^T lane)
-    const int col0 = (tid >> 7) * NC;  // first query row of this thread's column group
-    const int wq = warp & 3;       // TMEM lane quarter
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
-    const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(p.q);
-    const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(p.v);
-    const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
-    int kc = 0, ui = 0;
-    bool stop = false;
-    for (long long u = ufirst; u <= ulast && !stop; ++u) {
-      const DUnit x = dunit(p, u);
-      const long long lt0 = tb - u * TPU > 0 ? tb - u * TPU : 0;
-      const long long lt1 = te - u * TPU < TPU ? te - u * TPU : TPU;
-      if (!x.ok) {  // every CTA touching the unit skips it: no ticket, no output
-        if (lt0 == 0 && x.kvh == 0 && tid == 0) flag(p, GQAW_DEV_BAD_SEQLEN);
-        continue;
-      }
-      const int r1 = (int)(lt1 < x.real ? lt1 : x.real);
-      const int nt = r1 > (int)lt0 ? r1 - (int)lt0 : 0;  // real tiles here
-      const int fx = x.real > 0 ? x.real - 1 : 0;       // the tile that adds the new keys
-      const bool has_fix = lt0 <= fx && fx < lt1;
-      const bool moves = item_moves(p, x.pl);
-      const long long P = x.pl.P;
-      if (lt0 == 0 && x.kvh == 0 && tid == 0) {
-        if (p.resident_out) p.resident_out[x.b] = (int32_t)x.pl.Lt;
-        if (moves) p.move_list[atomicAdd(p.move_count, 1u)] = x.b;
-      }
-      if (has_fix && !moves) {  // append the new rows at L(P) + s: no query of this step reads them
-        for (int e = tid; e < 2 * S * 16; e += kSoft) {
-          const int tensor = e / (S * 16), rem = e % (S * 16), s = rem / 16, vec = rem % 16;
-          const size_t in_row = ((size_t)x.b * S + s) * p.Nkv + x.kvh;
-          const size_t out_row = ((size_t)x.b * p.Nkv + x.kvh) * (size_t)p.C + (size_t)(x.pl.Lp + s);
-          reinterpret_cast<uint4 *>(static_cast<char *>(tensor ? p.prv : p.prk) + out_row * kD * 2)[vec] =
-              reinterpret_cast<const uint4 *>(static_cast<const char *>(tensor ? p.v : p.k) + in_row * kD * 2)[vec];
-        }
-      }
-      for (int n = tid; n < NVT; n += kSoft)  // rows past S x g: the item's first bias row
-        brow[n] = !p.bias ? 0
-                          : (long long)x.b * p.bsb +
-                                (n < NV ? (long long)(x.kvh * g + n % g) * p.bsh + (long long)(n / g) * p.bss : 0);
-      named_barrier(kBar, kSoft);
-
-      // per query row of this thread: the reference maximum (uniform over the CTA) and
-      // this thread's share of the softmax denominator
-      float m_ref[NC], lsum[NC];
-#pragma unroll
-      for (int i = 0; i < NC; ++i) {
-        m_ref[i] = -INFINITY;
-        lsum[i] = 0.f;
-      }
-      // Bias of this thread's key for its rows, fetched one tile ahead.  Keys past P read
-      // a column that exists (P - 1): their logits are masked anyway.
-      float bnext[NC];
-      auto fetch_bias = [&](int lt_) {
-        const long long j0_ = x.lo + (long long)lt_ * kKeys;
-        const int nv_ = (int)(P - j0_ < kKeys ? P - j0_ : kKeys);
-        const long long col = j0_ + (t < nv_ ? t : nv_ - 1);
-#pragma unroll
-        for (int i = 0; i < NC; ++i) bnext[i] = __ldg(p.bias + brow[col0 + i] + col);
-      };
-      if (p.bias && nt > 0) fetch_bias((int)lt0);
-      for (int lt = (int)lt0; lt < r1; ++lt, ++kc) {
-        const long long j0 = x.lo + (long long)lt * kKeys;
-        const int nvalid = (int)(P - j0 < kKeys ? P - j0 : kKeys);
-        // Key t (a cache key, so before every query) is in token s's window iff
-        // t >= P + s - W + 1 - j0; rows are token-major, so the rows that see key t are
-        // n < nlim.
-        const int wbase = (int)(P - p.W + 1 - j0);  // <= 0
-        const int nlim = (t < nvalid ? min(t - wbase + 1, S) * g : 0) - col0;
-        float bv[NC];
-        if (p.bias) {
-#pragma unroll
-          for (int i = 0; i < NC; ++i) bv[i] = bnext[i];
-          if (lt + 1 < r1) fetch_bias(lt + 1);
-        }
-        bool ok = mbar_wait(&s_full[kc & 1], (kc >> 1) & 1);
-        tc::fence_after_sync();
-        float z[NC];
-        tmem_ld<NC>(tmem_s + (kc & 1) * NPAD + col0 + lane_off, z);
-        tc::fence_before_sync();
-        mbar_arrive(&s_free[kc & 1]);
-        bool exceed = false;
-        if (plain) {
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            z[i] = i < nlim ? z[i] * p.qscale : -INFINITY;
-            exceed |= z[i] > m_ref[i] + kRescale;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            float v = z[i] * p.qscale;
-            if (p.capmul != 0.f) v = p.capmul * fast_tanh(v);
-            if (p.bias) v = fmaf(p.biasmul, bv[i], v);
-            z[i] = i < nlim ? v : -INFINITY;
-            exceed |= z[i] > m_ref[i] + kRescale;
-          }
-        }
-        // one vote per tile: a logit above its row's reference, or a wait that expired
-        const bool fail = !ok || *reinterpret_cast<volatile int *>(&s_abort);
-        const bool any = named_barrier_or(kBar, kSoft, exceed || fail);
-        if (any && named_barrier_or(kBar, kSoft, fail)) {
-          stop = true;
-          break;
-        }
-        // P^T buffer kc & 1 is free once the P.V of tile kc - 2 has completed
-        if (kc >= 2) ok = mbar_wait(&o_done[kc & 1], ((kc - 2) >> 1) & 1);
-        tc::fence_after_sync();
-        if (any) {
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            float mx = z[i];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) red[wq * NPAD + col0 + i] = mx;
-          }
-          named_barrier(kBar, kSoft);
-          float alpha[NC];
-          bool resc = false;
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            const int n = col0 + i;
-            const float mt = fmaxf(fmaxf(red[n], red[NPAD + n]), fmaxf(red[2 * NPAD + n], red[3 * NPAD + n]));
-            alpha[i] = 1.f;
-            if (mt > m_ref[i] + kRescale) {
-              alpha[i] = m_ref[i] == -INFINITY ? 0.f : fast_exp2(m_ref[i] - mt);
-              m_ref[i] = mt;
-              lsum[i] *= alpha[i];
-              resc = true;
-            }
-          }
-          // O^T holds earlier tiles of this unit: rescale this group's columns (the
-          // decision is per column group, uniform within the group's warps)
-          if (resc && lt > (int)lt0) {
-            if (!mbar_wait(&o_done[(kc - 1) & 1], ((kc - 1) >> 1) & 1)) ok = false;
-            tc::fence_after_sync();
-            float o[NC];
-            tmem_ld<NC>(tmem_o + col0 + lane_off, o);
-#pragma unroll
-            for (int i = 0; i < NC; ++i) o[i] *= alpha[i];
-            tmem_st<NC>(tmem_o + col0 + lane_off, o);
-          }
-        }
-        // probabilities (bf16) into P^T: row n, key t, 128-byte swizzled K-major
-        {
-          const int half = t >> 6, c = (t & 63) >> 3;
-          unsigned char *pb = pbuf(kc) + half * L::kQHalf + (t & 7) * 2;
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            const int n = col0 + i;
-            if (n < NV) {
-              const float pr = fast_exp2(z[i] - (m_ref[i] == -INFINITY ? 0.f : m_ref[i]));
-              lsum[i] += pr;
-              *reinterpret_cast<__nv_bfloat16 *>(pb + n * 128 + ((c ^ (n & 7)) << 4)) = __float2bfloat16_rn(pr);
-            }
-          }
-        }
-        // keys past P in the tile: their V rows must be finite (0 * NaN is NaN)
-        if (nvalid < kKeys) {
-          if (!mbar_wait(&full[kc % kStages], (kc / kStages) & 1)) ok = false;
-          unsigned char *vb = stage(kc) + 2 * kHalf;
-          for (int e = tid; e < (kKeys - nvalid) * 16; e += kSoft) {
-            const int row = nvalid + e / 16, part = e % 16;
-            *reinterpret_cast<uint4 *>(vb + (part / 8) * kHalf + row * 128 + (part % 8) * 16) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        if (!ok) {
-          flag(p, GQAW_DEV_TIMEOUT);
-          s_abort = 1;
-        }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        mbar_arrive(&p_full[kc & 1]);
-      }
-      if (stop) break;
-      named_barrier(kBar, kSoft);  // every thread is done with the last tile's maxima in red
-
-      // ---- the unit's state in this CTA: O^T (TMEM), reference maxima, sums
-      bool ok = true;
-      if (nt > 0) ok = mbar_wait(&o_done[(kc - 1) & 1], ((kc - 1) >> 1) & 1);
-      tc::fence_after_sync();
-#pragma unroll
-      for (int i = 0; i < NC; ++i) {
-        float v = lsum[i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[wq * NPAD + col0 + i] = v;
-        if (t == 0) fin_m[col0 + i] = m_ref[i];
-      }
-      if (named_barrier_or(kBar, kSoft, !ok)) {
-        flag(p, GQAW_DEV_TIMEOUT);
-        break;
-      }
-      if (has_fix) {
-        // logits of the S new keys (the step's own rows) for every query row
-        for (int e = tid; e < NV * S; e += kSoft) {
-          const int n = e / S, s2 = e % S, sn = n / g;
-          const int h = x.kvh * g + n % g;
-          float zz = -INFINITY;
-          if (s2 <= sn && s2 - sn > -p.W) {
-            const uint4 *qr = reinterpret_cast<const uint4 *>(qin + (((size_t)x.b * S + sn) * p.Nq + h) * kD);
-            const uint4 *kr = reinterpret_cast<const uint4 *>(kin + (((size_t)x.b * S + s2) * p.Nkv + x.kvh) * kD);
-            float dot = 0.f;
-#pragma unroll 8
-            for (int vv = 0; vv < kD / 8; ++vv) {
-              float qa[8], ka[8];
-              Elem<__nv_bfloat16>::unpack(qr[vv], qa);
-              Elem<__nv_bfloat16>::unpack(kr[vv], ka);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) dot = fmaf(qa[i], ka[i], dot);
-            }
-            zz = dot * p.qscale;
-            if (p.capmul != 0.f) zz = p.capmul * fast_tanh(zz);
-            if (p.bias) zz = fmaf(p.biasmul, p.bias[brow[n] + P + s2], zz);
-          }
-          zn[n * NPAD + s2] = zz;
-        }
-        named_barrier(kBar, kSoft);
-        for (int n = tid; n < NV; n += kSoft) {
-          const float m0 = fin_m[n];
-          float mn = m0;
-          for (int s2 = 0; s2 < S; ++s2) mn = fmaxf(mn, zn[n * NPAD + s2]);
-          const float f = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mn);
-          float l = (red[n] + red[NPAD + n] + red[2 * NPAD + n] + red[3 * NPAD + n]) * f;
-          for (int s2 = 0; s2 < S; ++s2) {
-            const float pz = fast_exp2(zn[n * NPAD + s2] - mn);
-            zn[n * NPAD + s2] = pz;
-            l += pz;
-          }
-          fin_m[n] = mn;
-          fin_l[n] = l;
-          fin_f[n] = f;
-        }
-      } else {
-        for (int n = tid; n < NV; n += kSoft) {
-          fin_l[n] = red[n] + red[NPAD + n] + red[2 * NPAD + n] + red[3 * NPAD + n];
-          fin_f[n] = 1.f;
-        }
-      }
-      named_barrier(kBar, kSoft);
-
-      // ---- this thread's head dimension d = t of its query rows
-      float o[NC];
-      if (nt > 0) {
-        tmem_ld<NC>(tmem_o + col0 + lane_off, o);
-        tc::fence_before_sync();
-        mbar_arrive(o_free);  // O^T may be overwritten by the next unit
-        ++ui;
-      } else {
-#pragma unroll
-        for (int i = 0; i < NC; ++i) o[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < NC; ++i) o[i] *= col0 + i < NV ? fin_f[col0 + i] : 0.f;
-      if (has_fix) {
-        // the step's own value rows, dimension t, eight rows per batch of independent loads
-        const __nv_bfloat16 *vcol = vin + ((size_t)x.b * S * p.Nkv + x.kvh) * kD + t;
-        for (int s0 = 0; s0 < S; s0 += 8) {
-          float vv[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            vv[j] = s0 + j < S ? __bfloat162float(vcol[(size_t)(s0 + j) * p.Nkv * kD]) : 0.f;
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            const int n = col0 + i;
-            if (n < NV) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                if (s0 + j < S) o[i] = fmaf(zn[n * NPAD + s0 + j], vv[j], o[i]);
-            }
-          }
-        }
-      }
-      const long long cf = owner_cta(u * TPU, V, G), cl = owner_cta(u * TPU + TPU - 1, V, G);
-      if (cf == cl) {
-#pragma unroll
-        for (int i = 0; i < NC; ++i) {
-          const int n = col0 + i;
-          if (n < NV) {
-            const int h = x.kvh * g + n % g;
-            const size_t orow = ((size_t)x.b * S + n / g) * p.Nq + h;
-            out[orow * kD + t] = __float2bfloat16_rn(sink_divide(o[i], fin_l[n], fin_m[n], sink_log2(p, h)));
-          }
-        }
-      } else {
-        const int slot = u == ufirst ? 0 : 1;  // only a CTA's first and last unit can be shared
-#pragma unroll
-        for (int i = 0; i < NC; ++i) {
-          const int n = col0 + i;
-          if (n < NV) {
-            float *part = p.partials + ((cta * 2 + slot) * NPAD + n) * (kD + 2);
-            part[t] = o[i];
-            if (t == 0) {
-              part[kD] = fin_m[n];
-              part[kD + 1] = fin_l[n];
-            }
-          }
-        }
-        named_barrier(kBar, kSoft);
-        if (tid == 0) {
-          __threadfence();
-          s_last = atomicAdd(&p.tickets[u], 1u) == (unsigned)(cl - cf);
-        }
-        named_barrier(kBar, kSoft);
-        if (s_last) {
-          // merge the contributors' partial states, all of this thread's rows at once
-          // (independent loads: one round trip per contributor, not one per row)
-          __threadfence();
-          float M[NC], Lsum[NC], A[NC];
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            M[i] = -INFINITY;
-            Lsum[i] = 0.f;
-            A[i] = 0.f;
-          }
-          for (long long c = cf; c <= cl; ++c) {
-            const int sl = u == c * V / G / TPU ? 0 : 1;
-            const float *part = p.partials + ((c * 2 + sl) * NPAD + col0) * (kD + 2);
-#pragma unroll
-            for (int i = 0; i < NC; ++i)
-              if (col0 + i < NV) M[i] = fmaxf(M[i], __ldcg(part + i * (kD + 2) + kD));
-          }
-          for (long long c = cf; c <= cl; ++c) {
-            const int sl = u == c * V / G / TPU ? 0 : 1;
-            const float *part = p.partials + ((c * 2 + sl) * NPAD + col0) * (kD + 2);
-#pragma unroll
-            for (int i = 0; i < NC; ++i) {
-              if (col0 + i < NV) {
-                const float mc = __ldcg(part + i * (kD + 2) + kD);
-                const float lc = __ldcg(part + i * (kD + 2) + kD + 1);
-                const float ac = __ldcg(part + i * (kD + 2) + t);
-                const float f = mc == -INFINITY ? 0.f : exp2f(mc - M[i]);  // -inf: no visible key
-                Lsum[i] = fmaf(f, lc, Lsum[i]);
-                A[i] = fmaf(f, ac, A[i]);
-              }
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            const int n = col0 + i;
-            if (n < NV) {
-              const int h = x.kvh * g + n % g;
-              const size_t orow = ((size_t)x.b * S + n / g) * p.Nq + h;
-              out[orow * kD + t] = __float2bfloat16_rn(sink_divide(A[i], Lsum[i], M[i], sink_log2(p, h)));
-            }
-          }
-          if (tid == 0) p.tickets[u] = 0u;  // ready for the next step
-        }
-      }
-      named_barrier(kBar, kSoft);  // scratch (fin, zn, brow) is reused by the next unit
-    }
-    if (stop) flag(p, GQAW_DEV_TIMEOUT);
-  }
-
-  // release tensor memory: every MMA has completed (MMA thread) and every tcgen05.ld of
-  // the softmax warps is complete (their loads wait in the same statement)
-  tc::fence_before_sync();
-  __syncthreads();
-  pdl_launch_dependents();  // every role of this CTA is done: the cache update may be launched
-  if (warp == 0) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, L::kCols);
-  }
-}
+cudaError_t launch_mmad_q8(const Params &p, const TdArgs &ta, const TdMaps &maps, int max_ctas, cudaStream_t stream);
 
 cudaError_t launch_mmad(const Params &p, const TdArgs &ta, const TdMaps &maps, int max_ctas, cudaStream_t stream) {
-  constexpr int kMaxDevices = 64;
-  static std::atomic<int> sms_cache[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  int sms = dev < kMaxDevices ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
-  if (sms <= 0) {
-    e = cudaFuncSetAttribute(mma_decode_kernel<16, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mma_decode_kernel<16, 8, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mma_decode_kernel<16, 16, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<16>::kAlloc);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mma_decode_kernel<32, 32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<32>::kAlloc);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    if (dev < kMaxDevices) sms_cache[dev].store(sms, std::memory_order_relaxed);
-  }
-  const long long V = ta.units * ta.tpu;
-  long long grid = max_ctas < sms ? max_ctas : sms;  // one CTA per SM: a persistent grid
-  if (grid > V) grid = V;
-  const int nv = p.S * p.group;
-  const int cg = nv <= 4 ? 1 : 2;  // softmax warps: 4 per column group
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
-  cfg.blockDim = dim3(32 * (4 * cg + 2));
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait()
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.dynamicSmemBytes = nv <= 16 ? Lay<16>::kAlloc : Lay<32>::kAlloc;
-  if (nv <= 4)
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4, 1>, p, ta, maps);
-  else if (nv <= 8)
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 8, 2>, p, ta, maps);
-  else if (nv <= 16)
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 16, 2>, p, ta, maps);
-  else
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<32, 32, 2>, p, ta, maps);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  if (p.quant) return launch_mmad_q8(p, ta, maps, max_ctas, stream);
+  return launch_mmad_t<0>(p, ta, maps, max_ctas, stream);
 }
 
 }  // namespace gqaw

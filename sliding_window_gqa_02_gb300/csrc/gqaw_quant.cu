@@ -30,7 +30,21 @@ template <int QT>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const Params p) {
   pdl_wait();  // the rows to quantize (maybe turned by the rotary kernel) are written
   const long long n8 = (long long)p.B * p.S * p.Nkv * p.D / 8;  // 8-element groups per tensor
+  const long long nq8 = p.q16 ? (long long)p.B * p.S * p.Nq * p.D / 8 : 0;
   const float sk = *p.ks, sv = *p.vs;
+  // the fp16 copy of the query (the tensor-core kernel's operand), when asked for
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < nq8;
+       idx += (long long)gridDim.x * blockDim.x) {
+    float f[8];
+    Elem<__nv_bfloat16>::unpack(static_cast<const uint4 *>(p.q)[idx], f);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    static_cast<uint4 *>(p.q16)[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < 2 * n8;
        idx += (long long)gridDim.x * blockDim.x) {
     const bool val = idx >= n8;
@@ -56,7 +70,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const Params p)
 }
 
 cudaError_t launch_quantize(const Params &p, int max_blocks, cudaStream_t stream) {
-  const long long n = 2LL * p.B * p.S * p.Nkv * p.D / 8;
+  const long long n = 2LL * p.B * p.S * p.Nkv * p.D / 8 + (p.q16 ? (long long)p.B * p.S * p.Nq * p.D / 8 : 0);
   long long blocks = (n + kQuantThreads - 1) / kQuantThreads;
   if (blocks > max_blocks) blocks = max_blocks;
   cudaLaunchConfig_t cfg = {};

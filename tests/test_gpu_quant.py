@@ -84,6 +84,23 @@ def test_rotary_and_sinks(ct):
         T = T + S
 
 
+@pytest.mark.parametrize("ct", ["i8", "e4m3"])
+@pytest.mark.parametrize("heads,S", [((32, 8), 1), ((32, 8), 4), ((32, 8), 8), ((8, 8), 1), ((16, 2), 2), ((32, 1), 1)])
+@pytest.mark.parametrize("split_keys", [0, 128])
+def test_tensor_core_path(ct, heads, S, split_keys):
+    """Head size 128 with S x group <= 32: the tensor-core kernel widens the code tiles to
+    fp16 operands; every processed-row count (4, 8, 16, 32), a ragged batch with one
+    item from an empty cache and a window crossing several 128-key tiles, key splits."""
+    Nq, Nkv = heads
+    sh = wl.Shape("q8t", B=3, Nq=Nq, Nkv=Nkv, D=128, W=300, C=310, dtype=wl.BF16)
+    p = _pair(sh, ct, 55, split_keys=split_keys)
+    T = np.array([0, 150, 2000], np.int64)
+    for t in range(3):
+        q, k, v = wl.step_inputs(sh, S, 5500 + 10 * S + t)
+        p.step(q, k, v, T + S - 1)
+        T = T + S
+
+
 def test_long_context_decode_sampled():
     """The long-context shape (32/8 heads, head size 128, W 4096) on an int8 cache: the
     first step of a B=8 batch compared in full."""
