@@ -194,7 +194,7 @@ class ClockSampler:
 # The attention kernel a step runs on (the library's dispatch rule), the short name of
 # its profile summaries and the sources that define it.
 KERNELS = {
-    "mmad": ("mma_decode_kernel (tcgen05)", ("gqaw_mmad.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
+    "mmad": ("mma_decode_kernel (tcgen05)", ("gqaw_mmad.cuh", "gqaw_mmad.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
     "mma": ("mma_attend_kernel (tcgen05)", ("gqaw_mma.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
     "attend": ("attend_kernel", ("gqaw_attend.cuh", "gqaw_internal.cuh", "gqaw_attend_bf16.cu", "gqaw_attend_f32.cu")),
 }
