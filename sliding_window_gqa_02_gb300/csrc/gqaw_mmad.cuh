@@ -298,6 +298,7 @@ struct Walker {
 // warp, the MMA issuer warp.
 template <int CG, int QT>
 struct Warps {
+  static_assert(QT == 0 || CG <= 2, "code caches: at most two column groups");
   static constexpr int kWiden = QT == 0 ? 0 : (CG == 1 ? 4 : 2);
   static constexpr int kProducer = 4 * CG + kWiden;
   static constexpr int kThreads = 32 * (kProducer + 2);
@@ -957,8 +958,8 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
     e = cudaFuncSetAttribute(mma_decode_kernel<16, 16, 2, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay<16>::kAlloc);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mma_decode_kernel<32, 32, 2, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Lay<32>::kAlloc);
+    e = cudaFuncSetAttribute(mma_decode_kernel<32, 32, QT == 0 ? 4 : 2, QT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<32>::kAlloc);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -968,10 +969,11 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
   long long grid = max_ctas < sms ? max_ctas : sms;
   if (grid > V) grid = V;
   const int nv = p.S * p.group;
-  const int cg = nv <= 4 ? 1 : 2;  // softmax warps: 4 per column group
+  // softmax warps: 4 per column group; 32 rows (bf16) take four groups of 8 rows
+  const int cg = nv <= 4 ? 1 : (nv <= 16 || QT != 0 ? 2 : 4);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
-  cfg.blockDim = dim3(cg == 1 ? Warps<1, QT>::kThreads : Warps<2, QT>::kThreads);
+  cfg.blockDim = dim3(cg == 1 ? Warps<1, QT>::kThreads : cg == 2 ? Warps<2, QT>::kThreads : Warps<4, 0>::kThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait()
@@ -986,7 +988,7 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
   else if (nv <= 16)
     e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 16, 2, QT>, p, ta, maps);
   else
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<32, 32, 2, QT>, p, ta, maps);
+    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<32, 32, QT == 0 ? 4 : 2, QT>, p, ta, maps);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
