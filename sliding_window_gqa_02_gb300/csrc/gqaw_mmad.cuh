@@ -163,6 +163,14 @@ __device__ __forceinline__ float fast_tanh(float x) {
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]);
 template <>
+__device__ __forceinline__ void tmem_ld<2>(uint32_t taddr, float (&v)[2]) {
+  uint32_t r[2];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];\ntcgen05.wait::ld.sync.aligned;"
+               : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+  v[0] = __uint_as_float(r[0]);
+  v[1] = __uint_as_float(r[1]);
+}
+template <>
 __device__ __forceinline__ void tmem_ld<4>(uint32_t taddr, float (&v)[4]) {
   uint32_t r[4];
   asm volatile(
@@ -194,6 +202,13 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&v)[32]) {
 }
 template <int N>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_st<2>(uint32_t taddr, const float (&v)[2]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(__float_as_uint(v[0])),
+               "r"(__float_as_uint(v[1]))
+               : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 template <>
 __device__ __forceinline__ void tmem_st<4>(uint32_t taddr, const float (&v)[4]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
@@ -949,7 +964,7 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
   if (e != cudaSuccess) return e;
   int sms = dev < kMaxDevices ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
   if (sms <= 0) {
-    e = cudaFuncSetAttribute(mma_decode_kernel<16, 4, 1, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(mma_decode_kernel<16, 4, 2, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay<16>::kAlloc);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(mma_decode_kernel<16, 8, 2, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -969,8 +984,9 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
   long long grid = max_ctas < sms ? max_ctas : sms;
   if (grid > V) grid = V;
   const int nv = p.S * p.group;
-  // softmax warps: 4 per column group; 32 rows (bf16) take four groups of 8 rows
-  const int cg = nv <= 4 ? 1 : (nv <= 16 || QT != 0 ? 2 : 4);
+  // softmax warps: 4 per column group, two groups (four for 32 bf16 rows): more warps to
+  // overlap the per-row work than rows need
+  const int cg = nv <= 16 || QT != 0 ? 2 : 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(cg == 1 ? Warps<1, QT>::kThreads : cg == 2 ? Warps<2, QT>::kThreads : Warps<4, 0>::kThreads);
@@ -982,7 +998,7 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
   cfg.numAttrs = 1;
   cfg.dynamicSmemBytes = nv <= 16 ? Lay<16>::kAlloc : Lay<32>::kAlloc;
   if (nv <= 4)
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4, 1, QT>, p, ta, maps);
+    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4, 2, QT>, p, ta, maps);
   else if (nv <= 8)
     e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 8, 2, QT>, p, ta, maps);
   else if (nv <= 16)
