@@ -29,6 +29,7 @@ namespace gqaw {
 
 constexpr int kFinishThreads = 256;
 constexpr int kCopyVecs = 8;  // 16-byte vectors per thread per batch (32 KB per block)
+constexpr long long kMinCopyChains = 152;  // one per SM of a GB300
 
 __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) {
   pdl_wait();                // the attention kernel has finished reading the cache
@@ -40,16 +41,21 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) 
   // With rows to move, the next step's kernels are let in only when this block is done:
   // launched early, their CTAs would hold whole SMs (waiting for this grid) that the
   // copies need.
-  const int per_item = p.Nkv * 2 * p.ncg;
+  // Whole rows (one contiguous chain per slice) unless that leaves fewer chains than
+  // SMs; then rows split into column groups, up to p.ncg of them.  nmove is the same
+  // for every block, so they all agree on the job numbering.
+  int ncg = 1;
+  while (ncg < p.ncg && (long long)nmove * p.Nkv * 2 * ncg < kMinCopyChains) ncg *= 2;
+  const int per_item = p.Nkv * 2 * ncg;
   const long long njobs = (long long)nmove * per_item;
   const int rowb = p.rowbytes;
-  const int cvec = rowb / 16 / p.ncg;  // vectors per row in one column group
+  const int cvec = rowb / 16 / ncg;  // vectors per row in one column group
 
   for (long long job0 = blockIdx.x; job0 < njobs; job0 += gridDim.x) {
     const int b = p.move_list[job0 / per_item];
     int job = (int)(job0 % per_item);
-    const int cg = job % p.ncg;
-    job /= p.ncg;
+    const int cg = job % ncg;
+    job /= ncg;
     const int tensor = job & 1;  // 0: key, 1: value
     const int kvh = job >> 1;
     Plan pl;

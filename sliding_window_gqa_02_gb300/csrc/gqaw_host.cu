@@ -42,8 +42,6 @@ std::atomic<unsigned long long> g_launches{0ull};
 // Most attention CTAs of a step: GB300's 152 SMs x 2 resident CTAs per SM.
 constexpr long long kMaxCtas = 152 * 2;
 constexpr long long kSms = 152;
-// Largest cache bytes one column-group job of the finish kernel moves.
-constexpr long long kCopyChainBytes = 64 * 1024;
 // Upper bound on the cache-update kernel's blocks (152 SMs x 2).
 constexpr long long kFinishBlocks = 152 * 2;
 
@@ -159,8 +157,10 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   L->ctas = ctas;
 
   const int nv = L->rowbytes / 16;
+  // Most column groups a cache-update job may split a row into (each at least two
+  // 16-byte vectors wide); the kernel picks the count from the number of moving items.
   L->ncg = 1;
-  while (L->ncg * 2 <= nv / 2 && (long long)a->capacity * L->rowbytes / L->ncg > kCopyChainBytes) L->ncg *= 2;
+  while (L->ncg * 2 <= nv / 2) L->ncg *= 2;
 
   // Workspace: [0, 256) status word and the two counters of the cache-update list;
   // the list itself (B items); per-unit tickets; two partial-result slots per

@@ -38,7 +38,7 @@ struct Params {
   float qscale;              // q multiplier: scale*log2(e), or scale/softcap with softcap
   float capmul;              // softcap*log2(e), or 0 without softcap
   float biasmul;             // log2(e)
-  int ncg;                   // column groups per cache row in the copy jobs
+  int ncg;                   // most column groups per cache row in the copy jobs
   int rowbytes;              // D * cache element size
   int qbytes;                // query/key/value/output element size (4 or 2)
   const float *sink;         // NULL or (Nq,): sink logit per query head (natural-log units)
