@@ -119,6 +119,12 @@ def visible_columns(S, T_before, W):
     return n
 
 
+def step_flops(sh, S, T_before):
+    """Algorithmic FLOPs of one multi-token step: Q.K^T and P.V over the visible keys,
+    sum over items and tokens of Nq * 4 * D * min(P + s + 1, W)."""
+    return sh.Nq * 4 * sh.D * visible_columns(S, T_before, sh.W)
+
+
 # ------------------------------------------------------------------ clocks
 
 
@@ -483,13 +489,22 @@ def run_gpu(args, rank, world):
                           "peak_source": peak_src, "bytes_per_step": step_bytes / K}
     if attend_ms is not None:
         am = statistics.mean(attend_ms)
-        ach = att_bytes / K / (am / 1e3) / 1e9
         kern = attention_kernel(sh, S, h.quant)
         traffic = profiled_traffic(name, kern)
-        result["roofline"] = {"kernel": KERNELS[kern][0], "bound": "hbm", "achieved": ach, "peak": peak,
-                              "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
-                              "algorithmic_bytes_per_launch": att_bytes / K, "avg_launch_ms": am,
-                              "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
+        if kern == "mma":  # multi-token steps on the tensor-core kernel: tensor bound
+            flops = sum(step_flops(sh, S, h.T[t]) for t in range(Wm, Wm + K)) / K
+            ach = flops / (am / 1e3) / 1e12
+            tpk = bf16_peak_tflops()
+            result["roofline"] = {"kernel": KERNELS[kern][0], "bound": "tensor", "achieved": ach, "peak": tpk,
+                                  "unit": "TFLOP/s", "frac": ach / tpk, "traffic": traffic,
+                                  "algorithmic_flops_per_launch": flops, "avg_launch_ms": am,
+                                  "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"}
+        else:
+            ach = att_bytes / K / (am / 1e3) / 1e9
+            result["roofline"] = {"kernel": KERNELS[kern][0], "bound": "hbm", "achieved": ach, "peak": peak,
+                                  "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
+                                  "algorithmic_bytes_per_launch": att_bytes / K, "avg_launch_ms": am,
+                                  "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
     # end-to-end through the C ABI with host buffers (the e2e pass re-runs the same
     # step indices on the advanced cache: the step function is defined for any buffer)
     h.prepare_e2e()
@@ -561,10 +576,7 @@ def extra_workloads(main, args):
                  "B": h.B, "S": h.S, "cache_dtype": h.sh.dtype,
                  "launch": "CUDA graph" if h.spec["graph"] else "stream"}
         if h.S > 1:
-            flops = 0
-            for P in h.T[Wm]:
-                for s in range(h.S):
-                    flops += h.sh.Nq * 4 * h.sh.D * min(int(P) + s + 1, h.sh.W)
+            flops = step_flops(h.sh, h.S, h.T[Wm])
             entry["tflops"] = flops / (ms / 1e3) / 1e12
             entry["tensor_frac"] = entry["tflops"] / bf16_peak_tflops()
         entry["kernel"] = KERNELS[attention_kernel(h.sh, h.S, h.quant)][0]

@@ -186,8 +186,13 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     // key tiles of one query tile: the window before it plus its own tokens
     const long long nt = ceil_div(std::min<long long>(a->local_window_size, a->total_sequence_length), 128) +
                          ceil_div(L->ta.tokens_per_tile, 128) + 1;
-    long long ns = 1;  // split keys only when the query tiles fill less than 3/4 of the SMs
-    if (base > 0 && base * 4 < kSms * 3) ns = std::max(1LL, std::min({kSms / base, nt / 4, 16LL}));
+    // Key splits: the fewest waves of one-CTA-per-SM blocks, counting each block's
+    // fixed cost (query load, pipeline fill, epilogue) as about two key tiles.
+    long long ns = 1, best = -1;
+    for (long long n = 1; n <= std::min(16LL, std::max(1LL, nt / 4)); ++n) {
+      const long long cost = ceil_div(base * n, kSms) * (ceil_div(nt, n) + 2);
+      if (best < 0 || cost < best) best = cost, ns = n;
+    }
     if (a->split_keys > 0) ns = std::max(1LL, std::min(16LL, ceil_div(nt * 128, a->split_keys)));
     L->ta.nsplit = (int)ns;
     L->tc_grid = base * ns;
@@ -435,19 +440,20 @@ bool encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *di
 gqaw_status run_mma(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
   gqaw::TcMaps maps;
   const cuuint64_t D = 128, BS = (cuuint64_t)a->batch_size * a->sequence_length;
-  const cuuint64_t rows = (cuuint64_t)a->batch_size * a->kv_num_heads * a->capacity;
+  const cuuint64_t slices = (cuuint64_t)a->batch_size * a->kv_num_heads, C = (cuuint64_t)a->capacity;
   const cuuint64_t q_dims[3] = {D, (cuuint64_t)a->num_heads, BS};
   const cuuint64_t q_str[2] = {D * 2, (cuuint64_t)a->num_heads * D * 2};
   const cuuint32_t q_box[3] = {64, (cuuint32_t)L.group, (cuuint32_t)(32 / L.group)};
-  const cuuint64_t c_dims[2] = {D, rows};
-  const cuuint64_t c_str[1] = {D * 2};
-  const cuuint32_t c_box[2] = {64, 128};
+  // cache as (slice, row, dim): a box that starts below row 0 reads zeros there
+  const cuuint64_t c_dims[3] = {D, C, slices};
+  const cuuint64_t c_str[2] = {D * 2, C * D * 2};
+  const cuuint32_t c_box[3] = {64, 128, 1};
   const cuuint64_t n_dims[3] = {D, (cuuint64_t)a->kv_num_heads, BS};
   const cuuint64_t n_str[2] = {D * 2, (cuuint64_t)a->kv_num_heads * D * 2};
   const cuuint32_t n_box[3] = {64, 1, 128};
   if (!encode_map(&maps.q, p.q, 3, q_dims, q_str, q_box) ||
-      !encode_map(&maps.kc, a->past_key, 2, c_dims, c_str, c_box) ||
-      !encode_map(&maps.vc, a->past_value, 2, c_dims, c_str, c_box) ||
+      !encode_map(&maps.kc, a->past_key, 3, c_dims, c_str, c_box) ||
+      !encode_map(&maps.vc, a->past_value, 3, c_dims, c_str, c_box) ||
       !encode_map(&maps.kn, p.k, 3, n_dims, n_str, n_box) ||
       !encode_map(&maps.vn, a->value, 3, n_dims, n_str, n_box))
     return fail(GQAW_ECUDA, "cuTensorMapEncodeTiled failed for the multi-token kernel");

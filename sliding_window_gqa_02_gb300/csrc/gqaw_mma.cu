@@ -3,7 +3,7 @@
 // For steps with S > 1 new tokens (speculative verify, chunked prefill) the logits of
 // all query heads of a kv group and of many tokens share the same K/V rows, so
 // Q.K^T and P.V are genuine dense contractions: they run as tcgen05.mma (bf16
-// operands from shared memory, fp32 accumulators in tensor memory).
+// operands, fp32 accumulators in tensor memory).
 //
 // What it computes is the same as the decode kernel (gqaw_attend.cuh): query of token
 // s at absolute position i = P + s attends keys i - W < j <= i (onnxruntime PR #34226
@@ -16,16 +16,29 @@
 // before any cache row moves.
 //
 // Tiling: one CTA per (item, kv head, 128-row query tile, key split).  Query rows are
-// (token, head) pairs r = t * g + head, so one TMA box brings 128/g tokens x g heads.
-// Keys come in tiles of 128: first the cache rows [klo, P), then the new rows
-// [P, P + s_end).  Per key tile:
-//   S = Q K^T      tcgen05.mma M=128 N=128, K=128 in 8 steps (both operands K-major)
-//   softmax        one thread per query row reads its 128 logits from tensor memory
-//                  (no shuffles), masks, online max/sum, writes P (bf16) to shared
-//                  memory in the 128-byte-swizzled K-major layout
-//   O += P V       tcgen05.mma M=128 N=128 (V is the MN-major B operand)
-// K/V tiles arrive by TMA (128-byte swizzle) into a two-stage ring; the load of tile
-// t + 1 overlaps the softmax and P.V of tile t.
+// (token, head) pairs r = t * g + head, so a tile holds 128/g tokens x g heads.  Keys
+// come in tiles of 128: cache tiles ending exactly at the item's last past row (the
+// rows below the window in the first one are older resident rows, or zeros where the
+// tensor map runs below row 0: always finite), then tiles of the new rows.
+//
+// Warp roles (6 warps):
+//   warps 0-3   softmax: one thread per query row (TMEM lane); per key tile it reads
+//               the row's 128 logits twice from tensor memory (the maximum, then
+//               P = 2^(z - m) as bf16 into tensor memory), keeps the running sum
+//   warp 4      MMA issue (one thread): S(k) = Q K(k)^T into one of two tensor-memory
+//               buffers (both operands in shared memory), O += P V(k) (P from tensor
+//               memory, V from shared memory)
+//   warp 5      TMA loads of the query tile and of K tiles into a 3-stage ring
+//   warp 6      TMA loads of V tiles into a 2-stage ring
+//   warp 7      bookkeeping of the item (resident length, cache-update list) and the
+//               appends of the tile's new rows, off the softmax's path
+// Tensor memory (512 columns): S buffers [0, 128) and [128, 256), O [256, 384), P
+// buffers [384, 448) and [448, 512); nothing aliases.  Per key tile k the MMA thread
+// issues S(k+1) as soon as K(k+1) has landed and the softmax is done with S(k-1), so it
+// runs while the softmax works on S(k); then O += P(k) V(k) once P(k) is written.  The
+// completion of S(k) also covers O += P(k-2) V(k-2), issued before it, so P buffer
+// k % 2 is free when S(k) is; O += P(k-1) V(k-1) is waited for only when the softmax has
+// to rescale O.  Likewise S buffer (k+1) % 2 is free once P(k-1) is written.
 #include <cuda.h>
 
 #include "gqaw_tc.cuh"
@@ -38,16 +51,19 @@ constexpr int kRows = 128;       // query rows per CTA (M)
 constexpr int kKeys = 128;       // keys per tile (N of Q.K^T, K of P.V)
 constexpr int kD = 128;          // head size
 constexpr int kHalf = 16384;     // bytes of a [128 rows][64 bf16] swizzled block
-constexpr int kThreads = 128;
-// shared memory: Q, two K buffers, two V buffers, P -- each two 64-column halves
+constexpr int kTile = 2 * kHalf; // one 128 x 128 bf16 operand
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int kMmaWarp = 4, kLoadWarp = 5, kVLoadWarp = 6, kAppendWarp = 7;
+constexpr int kThreads = 256;
+// shared memory: Q, the K ring, the V ring (each operand two 64-column halves)
 constexpr int kSmemQ = 0;
-constexpr int kSmemK = 2 * kHalf;
-constexpr int kSmemV = kSmemK + 4 * kHalf;
-constexpr int kSmemP = kSmemV + 4 * kHalf;
-constexpr int kSmemBars = kSmemP + 2 * kHalf;
+constexpr int kSmemK = kSmemQ + kTile;
+constexpr int kSmemV = kSmemK + kKStages * kTile;
+constexpr int kSmemBars = kSmemV + kVStages * kTile;
 constexpr int kSmemTotal = kSmemBars + 256;
 constexpr int kSmemAlloc = kSmemTotal + 1024;  // room to align the base to 1024 bytes
-constexpr uint32_t kTmemCols = 512;            // S: two buffers, columns [0,256); O: [256,384)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 2 * kKeys, kTmemP = kTmemO + kD;  // P: two buffers of 64 columns
 constexpr float kRescaleLog2 = 8.0f;           // lazy rescale threshold (log2 units)
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kRows, kKeys, 0, 0);
@@ -69,21 +85,176 @@ __device__ __forceinline__ float fast_tanh(float x) {
   return fmaf(-2.f, r, 1.f);
 }
 
+// Packed pairs of fp32 (sm_100 family): one instruction computes both lanes.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x of a packed pair on the FMA pipe, for part of the softmax exponentials (the
+// special-function unit computes the rest; either unit alone would pace the tile).
+// x = n + f with n = round(x), found by adding 1.5 * 2^23 (float spacing 1 there, so
+// the low mantissa bits of the sum t hold n), f in [-0.5, 0.5]; 2^f from a cubic fitted
+// to it on that interval (iteratively reweighted least squares on the relative error:
+// at most 7.8e-5 relative error for x in [-126, 8.5], far below the bf16 rounding of
+// P); 2^n is the float whose exponent field is n + 127, i.e. (bits(t) + 127) << 23.
+// x is first clamped to -127, where that float is +0: far-underflowing x (and -inf)
+// give exactly 0.
+__device__ __forceinline__ uint64_t exp2_fma2(float x0, float x1) {
+  x0 = fmaxf(x0, -127.f);
+  x1 = fmaxf(x1, -127.f);
+  const uint64_t x = pack2(x0, x1);
+  const uint64_t t = add2(x, pack2(12582912.f, 12582912.f));
+  const uint64_t f = fma2(add2(t, pack2(-12582912.f, -12582912.f)), pack2(-1.f, -1.f), x);
+  uint64_t q = fma2(pack2(0.055171482f, 0.055171482f), f, pack2(0.24261090f, 0.24261090f));
+  q = fma2(q, f, pack2(0.69326097f, 0.69326097f));
+  q = fma2(q, f, pack2(0.99992812f, 0.99992812f));
+  float t0, t1;
+  unpack2(t, t0, t1);
+  const float s0 = __uint_as_float(__float_as_uint(t0) * 0x800000u + 0x3F800000u);
+  const float s1 = __uint_as_float(__float_as_uint(t1) * 0x800000u + 0x3F800000u);
+  return mul2(q, pack2(s0, s1));
+}
+
+__device__ __forceinline__ bool abort_set(const int *f) { return *reinterpret_cast<const volatile int *>(f) != 0; }
+
+// Bit c set when column 32 * c32 + c of a key tile lies in [c_lo, c_hi).
+__device__ __forceinline__ uint32_t chunk_mask(int c32, int c_lo, int c_hi) {
+  const int lo = min(max(c_lo - c32 * 32, 0), 32), hi = min(max(c_hi - c32 * 32, 0), 32);
+  const uint32_t below_hi = hi >= 32 ? 0xffffffffu : (1u << hi) - 1u;
+  const uint32_t below_lo = lo >= 32 ? 0xffffffffu : (1u << lo) - 1u;
+  return below_hi & ~below_lo;
+}
+
+// The largest logit of this thread's row among the tile's visible columns, read from
+// tensor memory 32 columns at a time (kMasked: only columns in [c_lo, c_hi) count).
+template <bool kMasked>
+__device__ __forceinline__ float tile_max(uint32_t ts, int c_lo, int c_hi) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+    float v[32];
+    tc::tmem_ld32(ts + c32 * 32, v);
+    if (kMasked) {
+      const uint32_t m = chunk_mask(c32, c_lo, c_hi);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], (m >> c) & 1u ? v[c] : -INFINITY);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) {
+        mx[(c / 8) & 3] = max3(mx[(c / 8) & 3], v[c], v[c + 1]);
+        mx[(c / 8) & 3] = max3(mx[(c / 8) & 3], v[c + 2], v[c + 3]);
+        mx[(c / 8) & 3] = max3(mx[(c / 8) & 3], v[c + 4], v[c + 5]);
+        mx[(c / 8) & 3] = max3(mx[(c / 8) & 3], v[c + 6], v[c + 7]);
+      }
+    }
+  }
+  return max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+}
+
+// P = 2^(z * zs - base) of the row's 128 logits (tensor memory at ts), as bf16 pairs
+// into 64 columns at tp; returns the sum of the fp32 values.  The stores are waited
+// for by the caller.  A fully visible tile works on packed pairs and sends three pairs
+// in eight to the FMA pipe.
+template <bool kMasked>
+__device__ __forceinline__ float tile_p(uint32_t ts, uint32_t tp, int c_lo, int c_hi, float zs, float base) {
+  if (kMasked) {
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+      float v[32];
+      tc::tmem_ld32(ts + c32 * 32, v);
+      const uint32_t m = chunk_mask(c32, c_lo, c_hi);
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float a0 = (m >> (2 * c)) & 1u ? fast_exp2(fmaf(v[2 * c], zs, -base)) : 0.f;
+        const float a1 = (m >> (2 * c + 1)) & 1u ? fast_exp2(fmaf(v[2 * c + 1], zs, -base)) : 0.f;
+        ls[c & 3] += a0 + a1;
+        pk[c] = tc::pack_bf16x2(a0, a1);
+      }
+      tc::tmem_st16_async(tp + c32 * 16, pk);
+    }
+    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+  }
+  const uint64_t zs2 = pack2(zs, zs), nb2 = pack2(-base, -base);
+  uint64_t acc[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+#pragma unroll
+  for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+    float v[32];
+    tc::tmem_ld32(ts + c32 * 32, v);
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint64_t x = fma2(pack2(v[2 * c], v[2 * c + 1]), zs2, nb2);
+      uint64_t e;
+      if (c % 8 >= 5) {
+        float x0, x1;
+        unpack2(x, x0, x1);
+        e = exp2_fma2(x0, x1);
+      } else {
+        float x0, x1;
+        unpack2(x, x0, x1);
+        e = pack2(fast_exp2(x0), fast_exp2(x1));
+      }
+      acc[c & 1] = add2(acc[c & 1], e);
+      float a0, a1;
+      unpack2(e, a0, a1);
+      pk[c] = tc::pack_bf16x2(a0, a1);
+    }
+    tc::tmem_st16_async(tp + c32 * 16, pk);
+  }
+  float l0, l1, l2, l3;
+  unpack2(acc[0], l0, l1);
+  unpack2(acc[1], l2, l3);
+  return (l0 + l1) + (l2 + l3);
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
     mma_attend_kernel(const Params p, const TcArgs ta, const __grid_constant__ TcMaps maps) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + kSmemBars);  // [2]: K tile landed
-  uint64_t *vfull = kfull + 2;                                        // [2]: V tile landed
-  uint64_t *bar_q = vfull + 2;
-  uint64_t *bar_s = bar_q + 1;  // [2]: S = Q K^T done, per tensor-memory buffer
-  uint64_t *bar_o = bar_s + 2;  // O += P V done
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_o + 1);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemBars);
+  uint64_t *q_full = bars;                   // the query tile landed
+  uint64_t *k_full = bars + 1;               // [3] K stage landed
+  uint64_t *k_free = bars + 4;               // [3] K stage read by its S product
+  uint64_t *v_full = bars + 7;               // [2] V stage landed
+  uint64_t *s_full = bars + 9;               // [2] S buffer written
+  // p_full and pv_done are per P buffer: the softmax may finish P(k+1) before the MMA
+  // thread has looked for P(k), and a parity wait cannot tell two phases apart.
+  uint64_t *p_full = bars + 11;              // [2] P buffer written (and O rescaled) by the softmax warps
+  uint64_t *pv_done = bars + 13;             // [2] O += P V(k) done: P buffer and V stage k % 2 free
+  uint64_t *mma_done = bars + 15;            // every MMA of the CTA done
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
   __shared__ int s_last, s_abort;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int x = blockIdx.x;
   const int sp = x % ta.nsplit;
   x /= ta.nsplit;
@@ -93,13 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = x / p.Nkv;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kfull[i], 1);
-      mbar_init(&vfull[i], 1);
-      mbar_init(&bar_s[i], 1);
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_free[i], 1);
     }
-    mbar_init(bar_q, 1);
-    mbar_init(bar_o, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(mma_done, 1);
     mbar_fence_init();
     s_abort = 0;
   }
@@ -108,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 2 * kKeys;
   pdl_wait();
 
   Plan pl;
@@ -116,328 +291,405 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = p.group;
   const int s0 = rt * ta.tokens_per_tile;
   const int s_end = s0 + ta.tokens_per_tile < p.S ? s0 + ta.tokens_per_tile : p.S;
-  const long long unit_tile = ((long long)b * p.Nkv + kvh) * ta.rowtiles + rt;
+  const long long unit = ((long long)b * p.Nkv + kvh) * ta.rowtiles + rt;
 
-  // key tiles of this query tile: cache rows [klo, P), then new rows [P, P + s_end)
-  long long klo = 0, P = 0;
-  int nc = 0, ni = 0, t_begin = 0, t_end = 0;
+  // key tiles of this query tile: nc cache tiles ending at P, then tiles of new rows
+  long long P = 0;
+  int nc = 0, t_begin = 0, t_end = 0;
   bool moves = false;
   if (ok) {
     P = pl.P;
-    klo = P + s0 - p.W + 1 > 0 ? P + s0 - p.W + 1 : 0;
+    const long long klo = P + s0 - p.W + 1 > 0 ? P + s0 - p.W + 1 : 0;
     nc = (int)((P - klo + kKeys - 1) / kKeys);
-    ni = (int)((s_end + kKeys - 1) / kKeys);
-    const int nt = nc + ni;
+    const int nt = nc + (s_end + kKeys - 1) / kKeys;
     t_begin = (int)((long long)sp * nt / ta.nsplit);
     t_end = (int)((long long)(sp + 1) * nt / ta.nsplit);
     moves = item_moves(p, pl);
-    if (kvh == 0 && rt == 0 && sp == 0 && tid == 0) {
-      if (p.resident_out) p.resident_out[b] = (int32_t)pl.Lt;
-      if (moves) p.move_list[atomicAdd(p.move_count, 1u)] = b;
-    }
-    if (!moves && sp == 0) {  // append the new rows of this query tile's tokens at L(P) + s
-      const int per_row = kD * 2 / 16;
-      const int n = 2 * (s_end - s0) * per_row;
-      for (int e = tid; e < n; e += kThreads) {
-        const int tensor = e / ((s_end - s0) * per_row);
-        const int rem = e % ((s_end - s0) * per_row);
-        const int s = s0 + rem / per_row, vec = rem % per_row;
-        const size_t in_row = ((size_t)b * p.S + s) * p.Nkv + kvh;
-        const size_t out_row = ((size_t)b * p.Nkv + kvh) * (size_t)p.C + (size_t)(pl.Lp + s);
-        reinterpret_cast<uint4 *>(static_cast<char *>(tensor ? p.prv : p.prk) + out_row * kD * 2)[vec] =
-            reinterpret_cast<const uint4 *>(static_cast<const char *>(tensor ? p.v : p.k) + in_row * kD * 2)[vec];
+  }
+  const int ntl = t_end - t_begin;  // key tiles of this CTA
+  auto key0 = [&](int t) -> long long {  // absolute position of key tile t's first column
+    return t < nc ? P - (long long)(nc - t) * kKeys : P + (long long)(t - nc) * kKeys;
+  };
+  const int tpq = (s_end - s0 + 3) / 4;  // tokens per TMEM lane quarter
+
+  if (warp == kLoadWarp || warp == kVLoadWarp) {
+    // ------------------------------------------------------------ TMA loads (K | V)
+    if (lane == 0 && ntl > 0) {
+      const bool value = warp == kVLoadWarp;
+      const uint64_t pol = tc::policy_evict_normal(), qpol = policy_evict_first();
+      const int slice = b * p.Nkv + kvh;
+      const int nst = value ? kVStages : kKStages;
+      uint64_t *full = value ? v_full : k_full, *empty = value ? pv_done : k_free;
+      unsigned char *ring = smem + (value ? kSmemV : kSmemK);
+      if (!value) {
+        mbar_arrive_expect_tx(q_full, kTile);
+        for (int q = 0; q < 4; ++q) {  // quarter q: tokens s0 + q * tpq ..., rows [32q, 32q + 32)
+          const int qtok = b * p.S + s0 + q * tpq;
+          tc::tma_load_3d(smem + kSmemQ + q * 4096, &maps.q, 0, kvh * g, qtok, q_full, qpol);
+          tc::tma_load_3d(smem + kSmemQ + kHalf + q * 4096, &maps.q, 64, kvh * g, qtok, q_full, qpol);
+        }
       }
+      int iss = 0;
+      bool fine = true;
+      for (int k = 0, st = 0, ph = 0; k < ntl && !abort_set(&s_abort); ++k) {
+        if (k >= nst && !mbar_wait(&empty[st], ph ^ 1)) {  // the tile nst back has been read
+          fine = false;
+          break;
+        }
+        const int t = t_begin + k;
+        unsigned char *dst = ring + st * kTile;
+        mbar_arrive_expect_tx(&full[st], kTile);
+        if (t < nc) {
+          const CUtensorMap *m = value ? &maps.vc : &maps.kc;
+          const int row = (int)(pl.Lp - (long long)(nc - t) * kKeys);  // may be < 0: zeros
+          tc::tma_load_3d(dst, m, 0, row, slice, &full[st], pol);
+          tc::tma_load_3d(dst + kHalf, m, 64, row, slice, &full[st], pol);
+        } else {
+          const CUtensorMap *m = value ? &maps.vn : &maps.kn;
+          const int tokrow = b * p.S + (t - nc) * kKeys;
+          tc::tma_load_3d(dst, m, 0, kvh, tokrow, &full[st], pol);
+          tc::tma_load_3d(dst + kHalf, m, 64, kvh, tokrow, &full[st], pol);
+        }
+        ++iss;
+        if (++st == nst) st = 0, ph ^= 1;  // tile j sits in stage j % nst, phase (j / nst) & 1
+      }
+      if (!fine) {
+        flag(p, GQAW_DEV_TIMEOUT);
+        s_abort = 1;
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      for (int k = iss - nst > 0 ? iss - nst : 0; k < iss; ++k)
+        if (!mbar_wait(&full[k % nst], (k / nst) & 1)) flag(p, GQAW_DEV_TIMEOUT);
+      if (!value && !mbar_wait(q_full, 0)) flag(p, GQAW_DEV_TIMEOUT);
     }
-  } else if (kvh == 0 && rt == 0 && sp == 0 && tid == 0) {
-    flag(p, GQAW_DEV_BAD_SEQLEN);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0 && ntl > 0) {
+      // Shared-memory descriptors are built once; an operand at byte offset x from a base
+      // is the base descriptor plus x / 16 (the start-address field, bits 0-13, cannot
+      // carry: every address is below 256 KB).
+      const uint64_t dq = tc::smem_desc_sw128(smem + kSmemQ, 16, 1024);
+      const uint64_t dk = tc::smem_desc_sw128(smem + kSmemK, 16, 1024);
+      const uint64_t dv = tc::smem_desc_sw128(smem + kSmemV, kHalf, 1024);
+      auto issue_s = [&](int kst, int buf) {  // S(buf) = Q K^T, K in stage kst
+        const uint64_t b0 = dk + (uint64_t)((kst * kTile) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t off = (uint64_t)(((kk / 4) * kHalf + (kk % 4) * 32) >> 4);
+          tc::mma_bf16_ss(tmem + buf * kKeys, dq + off, b0 + off, kIdescQK, kk > 0);
+        }
+      };
+      auto issue_o = [&](int buf, bool acc) {  // O += P V, P buffer and V stage buf
+        // V: rows = keys (K), 64-dim halves (MN) 16 KB apart, 8-key groups 1 KB apart
+        const uint64_t b0 = dv + (uint64_t)((buf * kTile) >> 4);
+        const uint32_t pa = tmem + kTmemP + buf * (kKeys / 2);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc::mma_bf16_ts(tmem + kTmemO, pa + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, acc || kk > 0);
+      };
+      bool fine = mbar_wait(q_full, 0) && mbar_wait(&k_full[0], 0);
+      if (fine) {
+        tc::fence_after_sync();
+        issue_s(0, 0);
+        tc::mma_commit(&s_full[0]);
+        tc::mma_commit(&k_free[0]);
+      }
+      int kst = 1, kph = 0;  // stage and phase of K(k + 1): K(j) sits in stage j % 3, phase (j / 3) & 1
+      for (int k = 0; k < ntl && fine; ++k) {
+        if (abort_set(&s_abort)) break;
+        if (k + 1 < ntl) {  // S(k + 1) while the softmax works on S(k); P(k - 1) freed its buffer
+          const int buf = (k + 1) & 1;
+          fine = mbar_wait(&k_full[kst], kph);
+          if (!fine) break;
+          tc::fence_after_sync();
+          issue_s(kst, buf);
+          tc::mma_commit(&s_full[buf]);
+          tc::mma_commit(&k_free[kst]);
+          kst = kst == kKStages - 1 ? 0 : kst + 1;
+          if (kst == 0) kph ^= 1;
+        }
+        fine = mbar_wait(&v_full[k & 1], (k >> 1) & 1) && mbar_wait(&p_full[k & 1], (k >> 1) & 1);
+        if (!fine) break;
+        tc::fence_after_sync();
+        issue_o(k & 1, k > 0);
+        tc::mma_commit(&pv_done[k & 1]);
+      }
+      if (!fine) {
+        flag(p, GQAW_DEV_TIMEOUT);
+        s_abort = 1;
+      }
+      tc::mma_commit(mma_done);  // every MMA issued has completed before TMEM is released
+      if (!mbar_wait(mma_done, 0)) flag(p, GQAW_DEV_TIMEOUT);
+    }
+  } else if (warp == kAppendWarp) {
+    // ------------------------------------------------------------ bookkeeping, appends
+    if (ok) {
+      if (kvh == 0 && rt == 0 && sp == 0 && lane == 0) {
+        if (p.resident_out) p.resident_out[b] = (int32_t)pl.Lt;
+        if (moves) p.move_list[atomicAdd(p.move_count, 1u)] = b;
+      }
+      if (!moves && sp == 0) {  // append the new rows of this tile's tokens at L(P) + s
+        constexpr int kPerRow = kD * 2 / 16, kBatch = 8;
+        const int nrow = s_end - s0;
+        const int n = 2 * nrow * kPerRow;
+        for (int e0 = 0; e0 < n; e0 += 32 * kBatch) {
+          uint4 v[kBatch];
+          size_t dst[kBatch];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * 32 + lane;
+            if (e < n) {
+              const int tensor = e / (nrow * kPerRow);
+              const int rem = e % (nrow * kPerRow);
+              const int s = s0 + rem / kPerRow, vec = rem % kPerRow;
+              const size_t in_row = ((size_t)b * p.S + s) * p.Nkv + kvh;
+              const size_t out_row = ((size_t)b * p.Nkv + kvh) * (size_t)p.C + (size_t)(pl.Lp + s);
+              v[u] = reinterpret_cast<const uint4 *>(static_cast<const char *>(tensor ? p.v : p.k) + in_row * kD * 2)[vec];
+              dst[u] = (out_row * kD * 2 + (size_t)vec * 16) | (size_t)tensor;  // 16-byte aligned: bit 0 free
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            if (e0 + u * 32 + lane < n) {
+              char *base = static_cast<char *>(dst[u] & 1 ? p.prv : p.prk);
+              *reinterpret_cast<uint4 *>(base + (dst[u] & ~(size_t)1)) = v[u];
+            }
+          }
+        }
+      }
+    } else if (kvh == 0 && rt == 0 && sp == 0 && lane == 0) {
+      flag(p, GQAW_DEV_BAD_SEQLEN);
+    }
   }
 
-  // This thread's query row.  The tile's tokens are spread evenly over the four TMEM
-  // lane quarters (one warp each), tpq tokens per quarter, so a short step (S x g < 128
-  // rows) still gives every warp real rows.
-  const int r = tid;
-  const int tpq = (s_end - s0 + 3) / 4;
-  const int tl = (r % 32) / g;  // token within the quarter
-  const int tok = s0 + (r / 32) * tpq + tl;
-  const int hh = r % g;
-  const bool row_ok = ok && tl < tpq && tok < s_end;
-  const long long qi = P + tok;  // absolute position of the row's token
+  // ---------------------------------------------------------------- softmax (warps 0-3)
+  const bool softmax = warp < 4;
+  const int r = tid & 127;                       // query row = TMEM lane
+  // The tile's tokens are spread evenly over the four lane quarters, tpq tokens each,
+  // so a short step (S x g < 128 rows) still gives every warp real rows.
+  const int tl = lane / g;                       // token within the quarter
+  const int tok = s0 + (warp & 3) * tpq + tl;
+  const int hh = lane % g;
+  const bool row_ok = softmax && ok && tl < tpq && tok < s_end;
+  const long long qi = P + tok;                  // absolute position of the row's token
   const long long rlo = qi - p.W + 1 > 0 ? qi - p.W + 1 : 0;
   const int h = kvh * g + hh;
-  const float *bias_row = (row_ok && p.bias) ? p.bias + (long long)b * p.bsb + (long long)h * p.bsh +
-                                                   (long long)tok * p.bss
-                                             : nullptr;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t to = tmem + kTmemO + lane_off, tp = tmem + kTmemP + lane_off;
+  float m_run = -INFINITY, l_run = 0.f;
+  int done = 0;
+  if (softmax && ntl > 0) {
+    const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
+    const float *bias_row = (row_ok && p.bias) ? p.bias + (long long)b * p.bsb + (long long)h * p.bsh +
+                                                     (long long)tok * p.bss
+                                               : nullptr;
+    // Visible columns of this row in tile k: [lo - 128 k, hi - 128 k) clamped to [0, 128]
+    // (consecutive key tiles start 128 positions apart, across the cache/new boundary
+    // too).  Both bounds only decrease, so they are kept at -128 once below it.
+    int lo = 0, hi = 0;
+    if (row_ok) {
+      const long long j0 = key0(t_begin);
+      lo = (int)min(max(rlo - j0, -128LL), 1LL << 30);
+      hi = (int)min(max(qi - j0 + 1, -128LL), 1LL << 30);
+    }
+    for (int k = 0; k < ntl; ++k) {  // every wait is bounded: an abort ends the loop there
+      const uint32_t ts = tmem + (k & 1) * kKeys + lane_off;  // S(k) of this row
+      const int c_lo = min(max(lo, 0), kKeys), c_hi = min(max(hi, 0), kKeys);
+      lo = max(lo - kKeys, -kKeys);
+      hi = max(hi - kKeys, -kKeys);
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[k & 1], (k >> 1) & 1))) {
+        flag(p, GQAW_DEV_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      tc::fence_after_sync();
 
-  uint64_t pol = 0;
-  const int row0_cache = (int)(((long long)b * p.Nkv + kvh) * p.C);
-  // Thread 0: load the K (or V) half-tiles of key tile t into buffer `dst`.
-  auto load_kv = [&](int t, unsigned char *dst, uint64_t *bar, bool value) {
-    mbar_arrive_expect_tx(bar, 2 * kHalf);
-    if (t < nc) {
-      const CUtensorMap *m = value ? &maps.vc : &maps.kc;
-      const int row = row0_cache + (int)(klo + (long long)t * kKeys - P + pl.Lp);
-      tc::tma_load_2d(dst, m, 0, row, bar, pol);
-      tc::tma_load_2d(dst + kHalf, m, 64, row, bar, pol);
-    } else {
-      const CUtensorMap *m = value ? &maps.vn : &maps.kn;
-      const int tokrow = b * p.S + (t - nc) * kKeys;
-      tc::tma_load_3d(dst, m, 0, kvh, tokrow, bar, pol);
-      tc::tma_load_3d(dst + kHalf, m, 64, kvh, tokrow, bar, pol);
-    }
-  };
-  auto kbuf = [&](int k) { return smem + kSmemK + (k % 2) * 2 * kHalf; };
-  auto vbuf = [&](int k) { return smem + kSmemV + (k % 2) * 2 * kHalf; };
-  const int ntl = t_end - t_begin;  // key tiles of this CTA
-  // S = Q K^T of local tile k into tensor-memory buffer k % 2 (thread 0).
-  auto issue_qk = [&](int k) {
-    if (!mbar_wait(&kfull[k % 2], (k / 2) & 1)) flag(p, GQAW_DEV_TIMEOUT);
-    tc::fence_after_sync();
+      // ---- pass 1: the row maximum over this tile's visible logits (log2 units), 32
+      // columns at a time.  Plain logits stay in tensor memory unscaled; capped or
+      // biased ones are written back transformed (invisible columns as -inf).
+      const bool whole = __all_sync(0xffffffffu, c_lo == 0 && c_hi == kKeys);
+      float mt;
+      if (plain) {
+        mt = (whole ? tile_max<false>(ts, c_lo, c_hi) : tile_max<true>(ts, c_lo, c_hi)) * p.qscale;
+      } else {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const int half = kk / 4, off = (kk % 4) * 32;
-      const uint64_t a = tc::smem_desc_sw128(smem + kSmemQ + half * kHalf + off, 16, 1024);
-      const uint64_t bd = tc::smem_desc_sw128(kbuf(k) + half * kHalf + off, 16, 1024);
-      tc::mma_bf16_ss(tmem_s + (k % 2) * kKeys, a, bd, kIdescQK, kk > 0);
+        for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+          float v[32];
+          tc::tmem_ld32(ts + c32 * 32, v);
+          const float *brow = bias_row ? bias_row + key0(t_begin + k) + c32 * 32 : nullptr;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int col = c32 * 32 + c;
+            const bool vis = col >= c_lo && col < c_hi;
+            float xv = v[c] * p.qscale;
+            if (p.capmul != 0.f) xv = p.capmul * fast_tanh(xv);
+            if (vis && brow) xv = fmaf(p.biasmul, brow[c], xv);
+            v[c] = vis ? xv : -INFINITY;
+            mx[c & 3] = fmaxf(mx[c & 3], v[c]);
+          }
+          tc::tmem_st32(ts + c32 * 32, v);
+        }
+        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      }
+
+      // lazy rescale: the reference max moves only when exceeded by more than 2^8; O is
+      // rescaled once O += P(k-1) V(k-1) has completed
+      const bool need = mt > m_run + kRescaleLog2;
+      float alpha = 1.f;
+      if (need) {
+        alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mt);
+        m_run = mt;
+        l_run *= alpha;
+      }
+      const bool rescale = k > 0 && __any_sync(0xffffffffu, need);
+      if (rescale && !__all_sync(0xffffffffu, mbar_wait(&pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1))) {
+        flag(p, GQAW_DEV_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      if (rescale) {
+#pragma unroll
+        for (int c32 = 0; c32 < kD / 32; ++c32) {
+          float v[32];
+          tc::tmem_ld32(to + c32 * 32, v);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] *= alpha;
+          tc::tmem_st32(to + c32 * 32, v);
+        }
+      }
+
+      // ---- pass 2: P = 2^(z - m) (qscale > 0 commutes with the maximum of plain logits)
+      const float base = m_run == -INFINITY ? 0.f : m_run;
+      const float zs = plain ? p.qscale : 1.f;  // plain logits are still unscaled
+      const uint32_t tpk = tp + (k & 1) * (kKeys / 2);
+      l_run += plain && !whole ? tile_p<true>(ts, tpk, c_lo, c_hi, zs, base)
+                               : tile_p<false>(ts, tpk, c_lo, c_hi, zs, base);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[k & 1]);
+      ++done;
     }
-    tc::mma_commit(&bar_s[k % 2]);
-  };
-  if (tid == 0 && ntl > 0) {
-    pol = policy_evict_first();
-    mbar_arrive_expect_tx(bar_q, 2 * kHalf);
-    for (int q = 0; q < 4; ++q) {  // quarter q: tokens s0 + q * tpq ..., rows [32q, 32q + 32)
-      const int qtok = b * p.S + s0 + q * tpq;
-      tc::tma_load_3d(smem + kSmemQ + q * 4096, &maps.q, 0, kvh * g, qtok, bar_q, tc::policy_evict_last());
-      tc::tma_load_3d(smem + kSmemQ + kHalf + q * 4096, &maps.q, 64, kvh * g, qtok, bar_q,
-                      tc::policy_evict_last());
+    // the last O += P V
+    if (done == ntl && !__all_sync(0xffffffffu, mbar_wait(&pv_done[(ntl - 1) & 1], ((ntl - 1) >> 1) & 1))) {
+      flag(p, GQAW_DEV_TIMEOUT);
+      done = 0;
     }
-    for (int k = 0; k < 2 && k < ntl; ++k) {
-      load_kv(t_begin + k, kbuf(k), &kfull[k % 2], false);
-      load_kv(t_begin + k, vbuf(k), &vfull[k % 2], true);
-    }
-    if (!mbar_wait(bar_q, 0)) flag(p, GQAW_DEV_TIMEOUT);
-    issue_qk(0);
+    tc::fence_after_sync();
   }
 
-  float m_run = -INFINITY, l_run = 0.f;
-  const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
-  // A bounded wait that expires sets s_abort; every thread reads it after the tile's
-  // barrier, so the whole CTA leaves the loop together.
-  auto bail = [&]() {
-    flag(p, GQAW_DEV_TIMEOUT);
-    s_abort = 1;
-  };
-  int done_tiles = 0;
-  for (int k = 0; k < ntl; ++k) {
-    const int t = t_begin + k;
-    const long long j0 = t < nc ? klo + (long long)t * kKeys : P + (long long)(t - nc) * kKeys;
-    const long long jhi_src = t < nc ? P : P + s_end;  // keys of this source
-    const int nvalid = (int)(jhi_src - j0 < kKeys ? jhi_src - j0 : kKeys);
-    // visible columns of this row in this tile: [c_lo, c_hi)
-    int c_lo = 0, c_hi = 0;
-    if (row_ok) {
-      const long long lo = rlo - j0, hi = qi - j0 + 1;
-      c_lo = (int)(lo < 0 ? 0 : (lo > kKeys ? kKeys : lo));
-      c_hi = (int)(hi < 0 ? 0 : (hi > nvalid ? nvalid : hi));
-    }
-
-    // ---- tensor core: S of the next tile while this one is in softmax
-    if (tid == 0 && k + 1 < ntl) issue_qk(k + 1);
-    if (!mbar_wait(&bar_s[k % 2], (k / 2) & 1)) bail();
-    tc::fence_after_sync();
-    // K buffer k % 2 is free again (Q.K^T of tile k is done): fetch K of tile k + 2
-    if (tid == 0 && k + 2 < ntl) load_kv(t + 2, kbuf(k), &kfull[k % 2], false);
-
-    // ---- logits of this row (log2 units), row maximum
-    float z[kKeys];
-    const uint32_t ts = tmem_s + (k % 2) * kKeys + ((uint32_t)(warp * 32) << 16);
-    float mt = -INFINITY;
-    if (plain) {
-#pragma unroll
-      for (int c32 = 0; c32 < kKeys / 32; ++c32) {
-        float v[32];
-        tc::tmem_ld32(ts + c32 * 32, v);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int col = c32 * 32 + c;
-          z[col] = (col >= c_lo && col < c_hi) ? v[c] : -INFINITY;
-          mt = fmaxf(mt, z[col]);
-        }
-      }
-      mt *= p.qscale;  // qscale > 0: max commutes with the scale
+  // ---- epilogue: this CTA's (O, m, l) per softmax row, 32 columns at a time (the
+  // tensor-memory loads are warp-wide: every softmax warp takes part)
+  const bool have_o = softmax && ntl > 0 && done == ntl;
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+  const long long orow = ((long long)b * p.S + tok) * p.Nq + h;
+  const int prow = r;  // row of the CTA's partial block
+  auto o_chunk = [&](int c32, float (&v)[32]) {
+    if (have_o) {
+      tc::tmem_ld32(to + c32 * 32, v);
     } else {
-      const float *brow = bias_row ? bias_row + j0 : nullptr;  // this tile's bias columns
 #pragma unroll
-      for (int c32 = 0; c32 < kKeys / 32; ++c32) {
-        float v[32];
-        tc::tmem_ld32(ts + c32 * 32, v);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int col = c32 * 32 + c;
-          const bool vis = col >= c_lo && col < c_hi;
-          float x = v[c] * p.qscale;
-          if (p.capmul != 0.f) x = p.capmul * fast_tanh(x);
-          if (vis && brow) x = fmaf(p.biasmul, brow[col], x);
-          z[col] = vis ? x : -INFINITY;
-          mt = fmaxf(mt, z[col]);
-        }
-      }
+      for (int c = 0; c < 32; ++c) v[c] = 0.f;
     }
-
-    // ---- the previous P.V has finished: P buffer, V buffer (k-1) % 2 and O are free
-    if (k > 0 && !mbar_wait(bar_o, (k - 1) & 1)) bail();
-    if (tid == 0 && k >= 1 && k + 1 < ntl) load_kv(t + 1, vbuf(k + 1), &vfull[(k + 1) % 2], true);
-    tc::fence_after_sync();
-
-    // lazy rescale: the reference max moves only when exceeded by more than 2^8
-    const bool need = mt > m_run + kRescaleLog2;
-    float alpha = 1.f;
-    if (need) {
-      alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mt);
-      m_run = mt;
-      l_run *= alpha;
-    }
-    if (k > 0 && __any_sync(0xffffffffu, need)) {
+  };
+  if (ta.nsplit == 1) {
+    if (softmax) {
+      const float inv = sink_reciprocal(l_run, m_run, sink_log2(p, h));
 #pragma unroll
       for (int c32 = 0; c32 < kD / 32; ++c32) {
         float v[32];
-        const uint32_t ta_o = tmem_o + ((uint32_t)(warp * 32) << 16) + c32 * 32;
-        tc::tmem_ld32(ta_o, v);
+        o_chunk(c32, v);
+        if (row_ok) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] *= alpha;
-        tc::tmem_st32(ta_o, v);
+          for (int c = 0; c < 32; c += 8) {
+            uint4 w;
+            w.x = tc::pack_bf16x2(v[c] * inv, v[c + 1] * inv);
+            w.y = tc::pack_bf16x2(v[c + 2] * inv, v[c + 3] * inv);
+            w.z = tc::pack_bf16x2(v[c + 4] * inv, v[c + 5] * inv);
+            w.w = tc::pack_bf16x2(v[c + 6] * inv, v[c + 7] * inv);
+            *reinterpret_cast<uint4 *>(out + orow * kD + c32 * 32 + c) = w;
+          }
+        }
       }
-    }
-    // ---- P (bf16) into shared memory, K-major with 128-byte swizzle
-    const float base = m_run == -INFINITY ? 0.f : m_run;
-    const float zs = plain ? p.qscale : 1.f;  // plain logits are still unscaled
-#pragma unroll
-    for (int q = 0; q < kKeys / 8; ++q) {
-      float pv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        pv[e] = fast_exp2(fmaf(z[q * 8 + e], zs, -base));
-        l_run += pv[e];
-      }
-      uint4 w;
-      w.x = tc::pack_bf16x2(pv[0], pv[1]);
-      w.y = tc::pack_bf16x2(pv[2], pv[3]);
-      w.z = tc::pack_bf16x2(pv[4], pv[5]);
-      w.w = tc::pack_bf16x2(pv[6], pv[7]);
-      const int half = q / 8, chunk = q % 8;
-      *reinterpret_cast<uint4 *>(smem + kSmemP + half * kHalf + r * 128 + ((chunk ^ (r & 7)) * 16)) = w;
-    }
-    // keys past this source's range: their V rows must be finite (0 * NaN is NaN)
-    unsigned char *vb = vbuf(k);
-    if (nvalid < kKeys) {
-      if (!mbar_wait(&vfull[k % 2], (k / 2) & 1)) bail();
-      for (int e = tid; e < (kKeys - nvalid) * 16; e += kThreads) {
-        const int row = nvalid + e / 16, part = e % 16;  // 16 chunks of 16 B per key (two halves)
-        *reinterpret_cast<uint4 *>(vb + (part / 8) * kHalf + row * 128 + (part % 8) * 16) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-
-    // ---- O += P V
-    if (tid == 0) {
-      if (!mbar_wait(&vfull[k % 2], (k / 2) & 1)) bail();
-      tc::fence_after_sync();
-#pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk) {
-        const int half = kk / 4, off = (kk % 4) * 32;
-        const uint64_t a = tc::smem_desc_sw128(smem + kSmemP + half * kHalf + off, 16, 1024);
-        // V: rows = keys (K), 64-dim halves (MN) 16 KB apart, 8-key groups 1 KB apart
-        const uint64_t bd = tc::smem_desc_sw128(vb + kk * 16 * 128, kHalf, 1024);
-        tc::mma_bf16_ss(tmem_o, a, bd, kIdescPV, k > 0 || kk > 0);
-      }
-      tc::mma_commit(bar_o);
-    }
-    ++done_tiles;
-    if (s_abort) break;  // uniform: read by all threads after the barrier above
-  }
-  if (done_tiles > 0 && !mbar_wait(bar_o, (done_tiles - 1) & 1)) flag(p, GQAW_DEV_TIMEOUT);
-  // an S = Q K^T issued ahead for a tile the loop did not reach must land before exit
-  if (tid == 0 && done_tiles < ntl && done_tiles + 1 <= ntl)
-    mbar_wait(&bar_s[done_tiles % 2], (done_tiles / 2) & 1);
-  tc::fence_after_sync();
-
-  // ---- epilogue: this CTA's (O, m, l) for its row
-  float o[kD];
-  if (ntl > 0) {
-#pragma unroll
-    for (int c32 = 0; c32 < kD / 32; ++c32) {
-      float v[32];
-      tc::tmem_ld32(tmem_o + ((uint32_t)(warp * 32) << 16) + c32 * 32, v);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) o[c32 * 32 + c] = v[c];
     }
   } else {
+    // Partial block of a CTA: 33 float4 columns x 128 rows, column-major so that a warp's
+    // 32 rows are contiguous; columns 0-31 hold O, column 32 holds (m, l).
+    float4 *const part = reinterpret_cast<float4 *>(p.partials);
+    auto part_at = [&](long long cta, int c4) { return part + (cta * (kTcPartialStride / 4) + c4) * kRows + prow; };
+    if (softmax) {
 #pragma unroll
-    for (int c = 0; c < kD; ++c) o[c] = 0.f;
-  }
-  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
-  const long long orow = ((long long)b * p.S + tok) * p.Nq + h;
-  if (ok) {
-    if (ta.nsplit == 1) {
+      for (int c32 = 0; c32 < kD / 32; ++c32) {
+        float v[32];
+        o_chunk(c32, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *part_at(blockIdx.x, c32 * 8 + j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
+      *part_at(blockIdx.x, kD / 4) = make_float4(m_run, l_run, 0.f, 0.f);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      s_last = ok && atomicAdd(&p.tickets[unit], 1u) == (unsigned)ta.nsplit - 1u;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
       if (row_ok) {
-        const float inv = sink_reciprocal(l_run, m_run, sink_log2(p, h));
-#pragma unroll
-        for (int c = 0; c < kD; c += 8) {
-          uint4 w;
-          w.x = tc::pack_bf16x2(o[c] * inv, o[c + 1] * inv);
-          w.y = tc::pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv);
-          w.z = tc::pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv);
-          w.w = tc::pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv);
-          *reinterpret_cast<uint4 *>(out + orow * kD + c) = w;
+        const long long first = (long long)blockIdx.x - sp;  // split 0 of this query tile
+        const int ns = ta.nsplit < 16 ? ta.nsplit : 16;
+        float mq[16], f[16];
+        float M = -INFINITY, L = 0.f;
+        for (int q = 0; q < ns; ++q) {
+          const float4 ml = __ldcg(part_at(first + q, kD / 4));
+          mq[q] = ml.x;
+          f[q] = ml.y;  // l for now
+          M = fmaxf(M, ml.x);
         }
-      }
-    } else {
-      float *part = p.partials + ((long long)blockIdx.x * kRows + r) * kTcPartialStride;
+        const float mb = M == -INFINITY ? 0.f : M;
+        for (int q = 0; q < ns; ++q) {
+          const float w = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mb);
+          L += w * f[q];
+          f[q] = w;
+        }
+        const float inv = sink_reciprocal(L, mb, sink_log2(p, h));
+#pragma unroll 1
+        for (int c32 = 0; c32 < kD / 32; ++c32) {
+          float acc[32];
 #pragma unroll
-      for (int c = 0; c < kD; c += 4)
-        *reinterpret_cast<float4 *>(part + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-      part[kD] = m_run;
-      part[kD + 1] = l_run;
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(&p.tickets[unit_tile], 1u) == (unsigned)ta.nsplit - 1u;
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        if (row_ok) {
-          const long long first = (long long)blockIdx.x - sp;  // split 0 of this query tile
-          float M = -INFINITY;
-          for (int q = 0; q < ta.nsplit; ++q)
-            M = fmaxf(M, __ldcg(p.partials + ((first + q) * kRows + r) * kTcPartialStride + kD));
-          const float mb = M == -INFINITY ? 0.f : M;
-          float L = 0.f;
-          float f[16];
-          for (int q = 0; q < ta.nsplit && q < 16; ++q) {
-            const float mq = __ldcg(p.partials + ((first + q) * kRows + r) * kTcPartialStride + kD);
-            f[q] = mq == -INFINITY ? 0.f : exp2f(mq - mb);
-            L += f[q] * __ldcg(p.partials + ((first + q) * kRows + r) * kTcPartialStride + kD + 1);
-          }
-          const float inv = sink_reciprocal(L, mb, sink_log2(p, h));
-          for (int c = 0; c < kD; c += 2) {
-            float a0 = 0.f, a1 = 0.f;
-            for (int q = 0; q < ta.nsplit && q < 16; ++q) {
-              if (f[q] == 0.f) continue;
-              const float *pq = p.partials + ((first + q) * kRows + r) * kTcPartialStride;
-              a0 = fmaf(f[q], __ldcg(pq + c), a0);
-              a1 = fmaf(f[q], __ldcg(pq + c + 1), a1);
+          for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+          for (int q = 0; q < ns; ++q) {
+            if (f[q] == 0.f) continue;
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __ldcg(part_at(first + q, c32 * 8 + j));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              acc[4 * j] = fmaf(f[q], v[j].x, acc[4 * j]);
+              acc[4 * j + 1] = fmaf(f[q], v[j].y, acc[4 * j + 1]);
+              acc[4 * j + 2] = fmaf(f[q], v[j].z, acc[4 * j + 2]);
+              acc[4 * j + 3] = fmaf(f[q], v[j].w, acc[4 * j + 3]);
             }
-            *reinterpret_cast<uint32_t *>(out + orow * kD + c) = tc::pack_bf16x2(a0 * inv, a1 * inv);
+          }
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 w;
+            w.x = tc::pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
+            w.y = tc::pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv);
+            w.z = tc::pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv);
+            w.w = tc::pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv);
+            *reinterpret_cast<uint4 *>(out + orow * kD + c32 * 32 + c) = w;
           }
         }
-        if (tid == 0) p.tickets[unit_tile] = 0u;
       }
+      if (tid == 0) p.tickets[unit] = 0u;
     }
   }
 
-  // release tensor memory (all tcgen05.ld of this CTA are complete)
+  // release tensor memory (all tcgen05 work of this CTA is complete)
   tc::fence_before_sync();
   __syncthreads();
   pdl_launch_dependents();  // this CTA's work is done: the cache-update kernel may be launched

@@ -12,7 +12,7 @@ namespace gqaw {
 // Tensor maps of the multi-token kernel (built on the host for every call).
 struct TcMaps {
   CUtensorMap q;   // query (B*S, Nq, D): box (64, g, 32/g), one TMEM lane quarter
-  CUtensorMap kc;  // past_key as (B*Nkv*C, D): box (64, 128)
+  CUtensorMap kc;  // past_key as (B*Nkv, C, D): box (64, 128, 1); rows outside [0, C) read as zero
   CUtensorMap vc;  // past_value
   CUtensorMap kn;  // key (B*S, Nkv, D): box (64, 1, 128)
   CUtensorMap vn;  // value
@@ -60,6 +60,12 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       "%3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -129,6 +135,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Store 16 consecutive 32-bit TMEM columns of this thread's lane without waiting: the
+// instruction takes its source registers like any store, only the write to tensor
+// memory completes asynchronously; tmem_wait_st() waits for every such write.
+__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // 16 consecutive 32-bit TMEM columns of this thread's lane, load and wait in one statement.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -191,6 +211,18 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.  A (M = 128 rows in the 128
+// lanes, K along the columns) packs two 16-bit elements per 32-bit column, element 2c
+// in the low half of column c; one K = 16 step reads 8 columns.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
 
