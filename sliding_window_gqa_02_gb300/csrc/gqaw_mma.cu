@@ -21,16 +21,18 @@
 // rows below the window in the first one are older resident rows, or zeros where the
 // tensor map runs below row 0: always finite), then tiles of the new rows.
 //
-// Warp roles (6 warps):
-//   warps 0-3   softmax: one thread per query row (TMEM lane); per key tile it reads
-//               the row's 128 logits twice from tensor memory (the maximum, then
-//               P = 2^(z - m) as bf16 into tensor memory), keeps the running sum
-//   warp 4      MMA issue (one thread): S(k) = Q K(k)^T into one of two tensor-memory
+// Warp roles (12 warps):
+//   warps 0-7   softmax: two threads per query row (TMEM lane), warps w and w + 4
+//               taking the row's key columns 0-63 and 64-127; per key tile each reads
+//               its 64 logits twice from tensor memory (the maximum, exchanged with
+//               the partner through shared memory; then P = 2^(z - m) as bf16 into
+//               tensor memory) and keeps a partial running sum
+//   warp 8      MMA issue (one thread): S(k) = Q K(k)^T into one of two tensor-memory
 //               buffers (both operands in shared memory), O += P V(k) (P from tensor
 //               memory, V from shared memory)
-//   warp 5      TMA loads of the query tile and of K tiles into a 3-stage ring
-//   warp 6      TMA loads of V tiles into a 2-stage ring
-//   warp 7      bookkeeping of the item (resident length, cache-update list) and the
+//   warp 9      TMA loads of the query tile and of K tiles into a 3-stage ring
+//   warp 10     TMA loads of V tiles into a 2-stage ring
+//   warp 11     bookkeeping of the item (resident length, cache-update list) and the
 //               appends of the tile's new rows, off the softmax's path
 // Tensor memory (512 columns): S buffers [0, 128) and [128, 256), O [256, 384), P
 // buffers [384, 448) and [448, 512); nothing aliases.  Per key tile k the MMA thread
@@ -49,12 +51,13 @@ namespace {
 
 constexpr int kRows = 128;       // query rows per CTA (M)
 constexpr int kKeys = 128;       // keys per tile (N of Q.K^T, K of P.V)
+constexpr int kHalfKeys = 64;    // columns of a tile row per softmax thread
 constexpr int kD = 128;          // head size
 constexpr int kHalf = 16384;     // bytes of a [128 rows][64 bf16] swizzled block
 constexpr int kTile = 2 * kHalf; // one 128 x 128 bf16 operand
 constexpr int kKStages = 3, kVStages = 2;
-constexpr int kMmaWarp = 4, kLoadWarp = 5, kVLoadWarp = 6, kAppendWarp = 7;
-constexpr int kThreads = 256;
+constexpr int kMmaWarp = 8, kLoadWarp = 9, kVLoadWarp = 10, kAppendWarp = 11;
+constexpr int kThreads = 384;
 // shared memory: Q, the K ring, the V ring (each operand two 64-column halves)
 constexpr int kSmemQ = 0;
 constexpr int kSmemK = kSmemQ + kTile;
@@ -65,6 +68,7 @@ constexpr int kSmemAlloc = kSmemTotal + 1024;  // room to align the base to 1024
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 2 * kKeys, kTmemP = kTmemO + kD;  // P: two buffers of 64 columns
 constexpr float kRescaleLog2 = 8.0f;           // lazy rescale threshold (log2 units)
+constexpr float kDangerLog2 = 16.0f;           // most a fast-path P may exceed 1 (log2 units)
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kRows, kKeys, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kRows, kD, 0, 1);
@@ -104,40 +108,10 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
-}
-
-// 2^x of a packed pair on the FMA pipe, for part of the softmax exponentials (the
-// special-function unit computes the rest; either unit alone would pace the tile).
-// x = n + f with n = round(x), found by adding 1.5 * 2^23 (float spacing 1 there, so
-// the low mantissa bits of the sum t hold n), f in [-0.5, 0.5]; 2^f from a cubic fitted
-// to it on that interval (iteratively reweighted least squares on the relative error:
-// at most 7.8e-5 relative error for x in [-126, 8.5], far below the bf16 rounding of
-// P); 2^n is the float whose exponent field is n + 127, i.e. (bits(t) + 127) << 23.
-// x is first clamped to -127, where that float is +0: far-underflowing x (and -inf)
-// give exactly 0.
-__device__ __forceinline__ uint64_t exp2_fma2(float x0, float x1) {
-  x0 = fmaxf(x0, -127.f);
-  x1 = fmaxf(x1, -127.f);
-  const uint64_t x = pack2(x0, x1);
-  const uint64_t t = add2(x, pack2(12582912.f, 12582912.f));
-  const uint64_t f = fma2(add2(t, pack2(-12582912.f, -12582912.f)), pack2(-1.f, -1.f), x);
-  uint64_t q = fma2(pack2(0.055171482f, 0.055171482f), f, pack2(0.24261090f, 0.24261090f));
-  q = fma2(q, f, pack2(0.69326097f, 0.69326097f));
-  q = fma2(q, f, pack2(0.99992812f, 0.99992812f));
-  float t0, t1;
-  unpack2(t, t0, t1);
-  const float s0 = __uint_as_float(__float_as_uint(t0) * 0x800000u + 0x3F800000u);
-  const float s1 = __uint_as_float(__float_as_uint(t1) * 0x800000u + 0x3F800000u);
-  return mul2(q, pack2(s0, s1));
 }
 
 __device__ __forceinline__ bool abort_set(const int *f) { return *reinterpret_cast<const volatile int *>(f) != 0; }
@@ -150,13 +124,14 @@ __device__ __forceinline__ uint32_t chunk_mask(int c32, int c_lo, int c_hi) {
   return below_hi & ~below_lo;
 }
 
-// The largest logit of this thread's row among the tile's visible columns, read from
-// tensor memory 32 columns at a time (kMasked: only columns in [c_lo, c_hi) count).
+// The largest logit of this thread's row among its 64 columns of the tile, read from
+// tensor memory 32 at a time (kMasked: only columns in [c_lo, c_hi), relative to the
+// first of the 64, count).
 template <bool kMasked>
 __device__ __forceinline__ float tile_max(uint32_t ts, int c_lo, int c_hi) {
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+  for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
     float v[32];
     tc::tmem_ld32(ts + c32 * 32, v);
     if (kMasked) {
@@ -176,16 +151,17 @@ __device__ __forceinline__ float tile_max(uint32_t ts, int c_lo, int c_hi) {
   return max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
 }
 
-// P = 2^(z * zs - base) of the row's 128 logits (tensor memory at ts), as bf16 pairs
-// into 64 columns at tp; returns the sum of the fp32 values.  The stores are waited
-// for by the caller.  A fully visible tile works on packed pairs and sends three pairs
-// in eight to the FMA pipe.
-template <bool kMasked>
-__device__ __forceinline__ float tile_p(uint32_t ts, uint32_t tp, int c_lo, int c_hi, float zs, float base) {
+// P = 2^(z * zs - base) of this thread's 64 logits of the row (tensor memory at ts), as
+// bf16 pairs into 32 columns at tp; returns the sum of the fp32 values.  The stores are
+// waited for by the caller.  A fully visible tile works on packed pairs; with kMax it
+// also leaves the largest raw logit of the 64 in *mx.
+template <bool kMasked, bool kMax = false>
+__device__ __forceinline__ float tile_p(uint32_t ts, uint32_t tp, int c_lo, int c_hi, float zs, float base,
+                                        float *mx = nullptr) {
   if (kMasked) {
     float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+    for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
       float v[32];
       tc::tmem_ld32(ts + c32 * 32, v);
       const uint32_t m = chunk_mask(c32, c_lo, c_hi);
@@ -203,31 +179,24 @@ __device__ __forceinline__ float tile_p(uint32_t ts, uint32_t tp, int c_lo, int 
   }
   const uint64_t zs2 = pack2(zs, zs), nb2 = pack2(-base, -base);
   uint64_t acc[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+  for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
     float v[32];
     tc::tmem_ld32(ts + c32 * 32, v);
     uint32_t pk[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const uint64_t x = fma2(pack2(v[2 * c], v[2 * c + 1]), zs2, nb2);
-      uint64_t e;
-      if (c % 8 >= 5) {
-        float x0, x1;
-        unpack2(x, x0, x1);
-        e = exp2_fma2(x0, x1);
-      } else {
-        float x0, x1;
-        unpack2(x, x0, x1);
-        e = pack2(fast_exp2(x0), fast_exp2(x1));
-      }
-      acc[c & 1] = add2(acc[c & 1], e);
-      float a0, a1;
-      unpack2(e, a0, a1);
+      if (kMax) m4[c & 3] = max3(m4[c & 3], v[2 * c], v[2 * c + 1]);
+      float x0, x1;
+      unpack2(fma2(pack2(v[2 * c], v[2 * c + 1]), zs2, nb2), x0, x1);
+      const float a0 = fast_exp2(x0), a1 = fast_exp2(x1);
+      acc[c & 1] = add2(acc[c & 1], pack2(a0, a1));
       pk[c] = tc::pack_bf16x2(a0, a1);
     }
     tc::tmem_st16_async(tp + c32 * 16, pk);
   }
+  if (kMax) *mx = max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
   float l0, l1, l2, l3;
   unpack2(acc[0], l0, l1);
   unpack2(acc[1], l2, l3);
@@ -253,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mma_done = bars + 15;            // every MMA of the CTA done
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
   __shared__ int s_last, s_abort;
+  __shared__ float xch[3][2][kRows];  // [tile & 1 | 2 for the sums][column half][row]
+  __shared__ int xok[2][2][4];        // [tile & 1][column half][lane quarter]: the wait held
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int x = blockIdx.x;
@@ -272,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], 8);
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(mma_done, 1);
@@ -394,19 +365,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(&s_full[0]);
         tc::mma_commit(&k_free[0]);
       }
-      int kst = 1, kph = 0;  // stage and phase of K(k + 1): K(j) sits in stage j % 3, phase (j / 3) & 1
+      // K(j) sits in stage j % 3 with phase (j / 3) & 1.  K(k + 1) is waited for one
+      // iteration ahead, off the path from O += P(k-1) V(k-1) to S(k+1).  An abort
+      // elsewhere shows up here as an expired wait.
+      int kst = 1, kph = 0;  // K(k + 1)
+      if (fine && ntl > 1) fine = mbar_wait(&k_full[1], 0);
       for (int k = 0; k < ntl && fine; ++k) {
-        if (abort_set(&s_abort)) break;
         if (k + 1 < ntl) {  // S(k + 1) while the softmax works on S(k); P(k - 1) freed its buffer
           const int buf = (k + 1) & 1;
-          fine = mbar_wait(&k_full[kst], kph);
-          if (!fine) break;
           tc::fence_after_sync();
           issue_s(kst, buf);
           tc::mma_commit(&s_full[buf]);
           tc::mma_commit(&k_free[kst]);
           kst = kst == kKStages - 1 ? 0 : kst + 1;
           if (kst == 0) kph ^= 1;
+          if (k + 2 < ntl && !(fine = mbar_wait(&k_full[kst], kph))) break;
         }
         fine = mbar_wait(&v_full[k & 1], (k >> 1) & 1) && mbar_wait(&p_full[k & 1], (k >> 1) & 1);
         if (!fine) break;
@@ -462,62 +435,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ---------------------------------------------------------------- softmax (warps 0-3)
-  const bool softmax = warp < 4;
-  const int r = tid & 127;                       // query row = TMEM lane
+  // ---------------------------------------------------------------- softmax (warps 0-7)
+  const bool softmax = warp < 8;
+  const int wq = warp & 3;                       // TMEM lane quarter
+  const int hf = (warp >> 2) & 1;                // column half of the row
+  const int r = wq * 32 + lane;                  // query row = TMEM lane
+  const int bar_pair = 1 + wq;                   // named barrier of warps wq and wq + 4
   // The tile's tokens are spread evenly over the four lane quarters, tpq tokens each,
   // so a short step (S x g < 128 rows) still gives every warp real rows.
   const int tl = lane / g;                       // token within the quarter
-  const int tok = s0 + (warp & 3) * tpq + tl;
+  const int tok = s0 + wq * tpq + tl;
   const int hh = lane % g;
   const bool row_ok = softmax && ok && tl < tpq && tok < s_end;
   const long long qi = P + tok;                  // absolute position of the row's token
   const long long rlo = qi - p.W + 1 > 0 ? qi - p.W + 1 : 0;
   const int h = kvh * g + hh;
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t to = tmem + kTmemO + lane_off, tp = tmem + kTmemP + lane_off;
-  float m_run = -INFINITY, l_run = 0.f;
+  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  // this thread's O columns [64 hf, 64 hf + 64) and P columns [32 hf, 32 hf + 32)
+  const uint32_t to = tmem + kTmemO + hf * kHalfKeys + lane_off, tp = tmem + kTmemP + hf * 32 + lane_off;
+  float m_run = -INFINITY, l_run = 0.f, o_owed = 1.f;
   int done = 0;
   if (softmax && ntl > 0) {
     const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
     const float *bias_row = (row_ok && p.bias) ? p.bias + (long long)b * p.bsb + (long long)h * p.bsh +
                                                      (long long)tok * p.bss
                                                : nullptr;
-    // Visible columns of this row in tile k: [lo - 128 k, hi - 128 k) clamped to [0, 128]
-    // (consecutive key tiles start 128 positions apart, across the cache/new boundary
-    // too).  Both bounds only decrease, so they are kept at -128 once below it.
+    // Visible columns of this row's half in tile k: [lo - 128 k, hi - 128 k) relative to
+    // the half's first column, clamped (consecutive key tiles start 128 positions apart,
+    // across the cache/new boundary too).  Both bounds only decrease, so they are kept
+    // at -128 once below it.
     int lo = 0, hi = 0;
     if (row_ok) {
-      const long long j0 = key0(t_begin);
+      const long long j0 = key0(t_begin) + hf * kHalfKeys;
       lo = (int)min(max(rlo - j0, -128LL), 1LL << 30);
       hi = (int)min(max(qi - j0 + 1, -128LL), 1LL << 30);
     }
-    for (int k = 0; k < ntl; ++k) {  // every wait is bounded: an abort ends the loop there
-      const uint32_t ts = tmem + (k & 1) * kKeys + lane_off;  // S(k) of this row
-      const int c_lo = min(max(lo, 0), kKeys), c_hi = min(max(hi, 0), kKeys);
+    // pend: the factor O in tensor memory still owes once O += P(k-1) V(k-1) has landed
+    // (a reference raised after P(k-1) was computed against the old one)
+    float pend = 1.f;
+    for (int k = 0; k < ntl; ++k) {
+      const uint32_t ts = tmem + (k & 1) * kKeys + hf * kHalfKeys + lane_off;  // this half of S(k)
+      const uint32_t tpk = tp + (k & 1) * (kKeys / 2);
+      const int c_lo = min(max(lo, 0), kHalfKeys), c_hi = min(max(hi, 0), kHalfKeys);
       lo = max(lo - kKeys, -kKeys);
       hi = max(hi - kKeys, -kKeys);
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[k & 1], (k >> 1) & 1))) {
-        flag(p, GQAW_DEV_TIMEOUT);
-        s_abort = 1;
-        break;
-      }
+      const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[k & 1], (k >> 1) & 1));
       tc::fence_after_sync();
+      const bool whole = __all_sync(0xffffffffu, c_lo == 0 && c_hi == kHalfKeys);
 
-      // ---- pass 1: the row maximum over this tile's visible logits (log2 units), 32
-      // columns at a time.  Plain logits stay in tensor memory unscaled; capped or
-      // biased ones are written back transformed (invisible columns as -inf).
-      const bool whole = __all_sync(0xffffffffu, c_lo == 0 && c_hi == kKeys);
-      float mt;
-      if (plain) {
+      // Fast path (a plain, fully visible tile of rows that have a reference already):
+      // P against the running reference m_run in the same pass as the tile maximum.
+      // Otherwise pass 1 finds the maximum first (capped or biased logits are written
+      // back transformed, invisible columns as -inf).
+      const bool fast = okw && plain && whole && __all_sync(0xffffffffu, m_run > -INFINITY);
+      float mt = -INFINITY, lt = 0.f;
+      if (fast) {
+        lt = tile_p<false, true>(ts, tpk, 0, kHalfKeys, p.qscale, m_run, &mt);
+        mt *= p.qscale;  // qscale > 0: max commutes with the scale
+      } else if (okw && plain) {
         mt = (whole ? tile_max<false>(ts, c_lo, c_hi) : tile_max<true>(ts, c_lo, c_hi)) * p.qscale;
-      } else {
+      } else if (okw) {
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c32 = 0; c32 < kKeys / 32; ++c32) {
+        for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
           float v[32];
           tc::tmem_ld32(ts + c32 * 32, v);
-          const float *brow = bias_row ? bias_row + key0(t_begin + k) + c32 * 32 : nullptr;
+          const float *brow = bias_row ? bias_row + key0(t_begin + k) + hf * kHalfKeys + c32 * 32 : nullptr;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int col = c32 * 32 + c;
@@ -533,50 +516,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
 
-      // lazy rescale: the reference max moves only when exceeded by more than 2^8; O is
-      // rescaled once O += P(k-1) V(k-1) has completed
+      // Exchange with the partner half (slot k & 1: the partner has read slot k & 1 of
+      // tile k - 2 before it reached the barrier of tile k - 1).  The pair takes the
+      // careful path when either half did not take the fast one or saw a logit more than
+      // 2^16 above the reference; an expired wait on either side ends both loops.
+      xch[k & 1][hf][r] = mt;
+      if (lane == 0) xok[k & 1][hf][wq] = okw;
+      const bool careful = named_barrier_or(bar_pair, 64, !fast || mt > m_run + kDangerLog2);
+      if (!okw || !xok[k & 1][hf ^ 1][wq]) {
+        flag(p, GQAW_DEV_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      mt = fmaxf(mt, xch[k & 1][hf ^ 1][r]);
+
+      // lazy rescale: the reference moves only when exceeded by more than 2^8 (both halves
+      // decide alike).  Careful path: O is rescaled now (with what it owes) and P is
+      // computed against the new reference.  Fast path: P(k) already used the old one, so
+      // the sum is rescaled after adding it and O owes the factor after O += P(k) V(k).
       const bool need = mt > m_run + kRescaleLog2;
       float alpha = 1.f;
       if (need) {
         alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mt);
         m_run = mt;
-        l_run *= alpha;
       }
-      const bool rescale = k > 0 && __any_sync(0xffffffffu, need);
-      if (rescale && !__all_sync(0xffffffffu, mbar_wait(&pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1))) {
-        flag(p, GQAW_DEV_TIMEOUT);
-        s_abort = 1;
-        break;
-      }
-      tc::fence_after_sync();
-      if (rescale) {
+      const float oscale = careful ? pend * alpha : pend;
+      if (k > 0 && __any_sync(0xffffffffu, oscale != 1.f)) {
+        const bool okp = __all_sync(0xffffffffu, mbar_wait(&pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1));
+        if (named_barrier_or(bar_pair, 64, !okp)) {
+          flag(p, GQAW_DEV_TIMEOUT);
+          s_abort = 1;
+          break;
+        }
+        tc::fence_after_sync();
 #pragma unroll
-        for (int c32 = 0; c32 < kD / 32; ++c32) {
+        for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
           float v[32];
           tc::tmem_ld32(to + c32 * 32, v);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] *= alpha;
+          for (int c = 0; c < 32; ++c) v[c] *= oscale;
           tc::tmem_st32(to + c32 * 32, v);
         }
       }
-
-      // ---- pass 2: P = 2^(z - m) (qscale > 0 commutes with the maximum of plain logits)
-      const float base = m_run == -INFINITY ? 0.f : m_run;
-      const float zs = plain ? p.qscale : 1.f;  // plain logits are still unscaled
-      const uint32_t tpk = tp + (k & 1) * (kKeys / 2);
-      l_run += plain && !whole ? tile_p<true>(ts, tpk, c_lo, c_hi, zs, base)
-                               : tile_p<false>(ts, tpk, c_lo, c_hi, zs, base);
+      if (careful) {
+        // ---- pass 2: P = 2^(z - m) (plain logits are still unscaled)
+        const float base = m_run == -INFINITY ? 0.f : m_run;
+        const float zs = plain ? p.qscale : 1.f;
+        l_run = l_run * alpha + (plain && !whole ? tile_p<true>(ts, tpk, c_lo, c_hi, zs, base)
+                                                 : tile_p<false>(ts, tpk, c_lo, c_hi, zs, base));
+        pend = 1.f;
+      } else {
+        l_run = (l_run + lt) * alpha;
+        pend = alpha;
+      }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[k & 1]);
       ++done;
     }
-    // the last O += P V
-    if (done == ntl && !__all_sync(0xffffffffu, mbar_wait(&pv_done[(ntl - 1) & 1], ((ntl - 1) >> 1) & 1))) {
+    // the last O += P V; the row sum from both halves; what O still owes joins the
+    // final scale (the epilogue multiplies O by pend)
+    const bool okf = done == ntl && __all_sync(0xffffffffu, mbar_wait(&pv_done[(ntl - 1) & 1], ((ntl - 1) >> 1) & 1));
+    xch[2][hf][r] = l_run;
+    if (named_barrier_or(bar_pair, 64, !okf)) {
       flag(p, GQAW_DEV_TIMEOUT);
       done = 0;
     }
+    l_run += xch[2][hf ^ 1][r];
+    o_owed = pend;
     tc::fence_after_sync();
   }
 
@@ -586,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
   const long long orow = ((long long)b * p.S + tok) * p.Nq + h;
   const int prow = r;  // row of the CTA's partial block
-  auto o_chunk = [&](int c32, float (&v)[32]) {
+  auto o_chunk = [&](int c32, float (&v)[32]) {  // chunk c32 of this half's 64 O columns
     if (have_o) {
       tc::tmem_ld32(to + c32 * 32, v);
     } else {
@@ -596,9 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   if (ta.nsplit == 1) {
     if (softmax) {
-      const float inv = sink_reciprocal(l_run, m_run, sink_log2(p, h));
+      const float inv = sink_reciprocal(l_run, m_run, sink_log2(p, h)) * o_owed;
 #pragma unroll
-      for (int c32 = 0; c32 < kD / 32; ++c32) {
+      for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
         float v[32];
         o_chunk(c32, v);
         if (row_ok) {
@@ -609,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             w.y = tc::pack_bf16x2(v[c + 2] * inv, v[c + 3] * inv);
             w.z = tc::pack_bf16x2(v[c + 4] * inv, v[c + 5] * inv);
             w.w = tc::pack_bf16x2(v[c + 6] * inv, v[c + 7] * inv);
-            *reinterpret_cast<uint4 *>(out + orow * kD + c32 * 32 + c) = w;
+            *reinterpret_cast<uint4 *>(out + orow * kD + hf * kHalfKeys + c32 * 32 + c) = w;
           }
         }
       }
@@ -621,14 +629,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto part_at = [&](long long cta, int c4) { return part + (cta * (kTcPartialStride / 4) + c4) * kRows + prow; };
     if (softmax) {
 #pragma unroll
-      for (int c32 = 0; c32 < kD / 32; ++c32) {
+      for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
         float v[32];
         o_chunk(c32, v);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          *part_at(blockIdx.x, c32 * 8 + j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          *part_at(blockIdx.x, hf * 16 + c32 * 8 + j) =
+              make_float4(v[4 * j] * o_owed, v[4 * j + 1] * o_owed, v[4 * j + 2] * o_owed, v[4 * j + 3] * o_owed);
       }
-      *part_at(blockIdx.x, kD / 4) = make_float4(m_run, l_run, 0.f, 0.f);
+      if (hf == 0) *part_at(blockIdx.x, kD / 4) = make_float4(m_run, l_run, 0.f, 0.f);
     }
     __syncthreads();
     if (tid == 0) {
@@ -657,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float inv = sink_reciprocal(L, mb, sink_log2(p, h));
 #pragma unroll 1
-        for (int c32 = 0; c32 < kD / 32; ++c32) {
+        for (int c32 = 2 * hf; c32 < 2 * hf + 2; ++c32) {  // this half's output columns
           float acc[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) acc[c] = 0.f;
