@@ -195,7 +195,8 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     }
     if (a->split_keys > 0) ns = std::max(1LL, std::min(16LL, ceil_div(nt * 128, a->split_keys)));
     L->ta.nsplit = (int)ns;
-    L->tc_grid = base * ns;
+    L->tc_grid = base * ns;  // units; the persistent kernel runs min(units, SMs) CTAs
+    L->ta.units = L->tc_grid;
     if (L->tc_grid > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many attention blocks");
     L->off_tickets = L->off_list + align256((size_t)a->batch_size * 4);
     L->off_partials = L->off_tickets + align256((size_t)base * 4);

@@ -15,11 +15,16 @@
 // windowed kv cache for GQA", "Staging for hazardous steps"), since this kernel runs
 // before any cache row moves.
 //
-// Tiling: one CTA per (item, kv head, 128-row query tile, key split).  Query rows are
-// (token, head) pairs r = t * g + head, so a tile holds 128/g tokens x g heads.  Keys
-// come in tiles of 128: cache tiles ending exactly at the item's last past row (the
-// rows below the window in the first one are older resident rows, or zeros where the
-// tensor map runs below row 0: always finite), then tiles of the new rows.
+// Tiling: units of (item, kv head, 128-row query tile, key split), walked grid-strided
+// by a persistent grid of one CTA per SM.  Query rows are (token, head) pairs
+// r = t * g + head, so a tile holds 128/g tokens x g heads.  Keys come in tiles of 128:
+// cache tiles ending exactly at the item's last past row (the rows below the window in
+// the first one are older resident rows, or zeros where the tensor map runs below row
+// 0: always finite), then tiles of the new rows.  Key tiles are numbered across the
+// units of a CTA, so the rings and barrier phases run on from one unit to the next: the
+// next unit's query tile loads once the last S product of the previous one is done, its
+// first S product runs while the softmax warps finish the previous unit, and its first
+// O += P V waits until they have read O out of tensor memory.
 //
 // Warp roles (12 warps):
 //   warps 0-7   softmax: two threads per query row (TMEM lane), warps w and w + 4
@@ -69,6 +74,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 2 * kKeys, kTmemP = kTmemO + kD;  // P: two buffers of 64 columns
 constexpr float kRescaleLog2 = 8.0f;           // lazy rescale threshold (log2 units)
 constexpr float kDangerLog2 = 16.0f;           // most a fast-path P may exceed 1 (log2 units)
+constexpr int kSoftmaxBar = 5;                 // named barrier of the 8 softmax warps (1-4: warp pairs)
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(kRows, kKeys, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kRows, kD, 0, 1);
@@ -203,6 +209,47 @@ __device__ __forceinline__ float tile_p(uint32_t ts, uint32_t tp, int c_lo, int 
   return (l0 + l1) + (l2 + l3);
 }
 
+// One unit of work of a CTA: (item, kv head, 128-row query tile, key split), and the
+// key tiles it covers.  Every warp role decodes the same sequence of units.
+struct Unit {
+  Plan pl;
+  long long P, id;  // id: (item, kv head, query tile), the index of the split tickets
+  int b, kvh, rt, sp, s0, s_end, tpq, nc, t_begin, ntl;
+  bool ok, moves;
+};
+
+__device__ __forceinline__ Unit unit_at(const Params &p, const TcArgs &ta, long long u) {
+  Unit x;
+  x.sp = (int)(u % ta.nsplit);
+  x.id = u / ta.nsplit;
+  x.rt = (int)(x.id % ta.rowtiles);
+  x.kvh = (int)((x.id / ta.rowtiles) % p.Nkv);
+  x.b = (int)(x.id / ta.rowtiles / p.Nkv);
+  x.ok = plan_item(p, x.b, x.pl);
+  x.s0 = x.rt * ta.tokens_per_tile;
+  x.s_end = x.s0 + ta.tokens_per_tile < p.S ? x.s0 + ta.tokens_per_tile : p.S;
+  x.tpq = (x.s_end - x.s0 + 3) / 4;  // tokens per TMEM lane quarter
+  x.P = 0;
+  x.nc = x.t_begin = x.ntl = 0;
+  x.moves = false;
+  if (x.ok) {
+    // nc cache tiles ending at P, then tiles of new rows
+    x.P = x.pl.P;
+    const long long klo = x.P + x.s0 - p.W + 1 > 0 ? x.P + x.s0 - p.W + 1 : 0;
+    x.nc = (int)((x.P - klo + kKeys - 1) / kKeys);
+    const int nt = x.nc + (x.s_end + kKeys - 1) / kKeys;
+    x.t_begin = (int)((long long)x.sp * nt / ta.nsplit);
+    x.ntl = (int)((long long)(x.sp + 1) * nt / ta.nsplit) - x.t_begin;
+    x.moves = item_moves(p, x.pl);
+  }
+  return x;
+}
+
+// Absolute position of key tile t's first column.
+__device__ __forceinline__ long long key0(const Unit &x, int t) {
+  return t < x.nc ? x.P - (long long)(x.nc - t) * kKeys : x.P + (long long)(t - x.nc) * kKeys;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -210,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemBars);
-  uint64_t *q_full = bars;                   // the query tile landed
+  uint64_t *q_full = bars;                   // the unit's query tile landed
   uint64_t *k_full = bars + 1;               // [3] K stage landed
   uint64_t *k_free = bars + 4;               // [3] K stage read by its S product
   uint64_t *v_full = bars + 7;               // [2] V stage landed
@@ -220,22 +267,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *p_full = bars + 11;              // [2] P buffer written (and O rescaled) by the softmax warps
   uint64_t *pv_done = bars + 13;             // [2] O += P V(k) done: P buffer and V stage k % 2 free
   uint64_t *mma_done = bars + 15;            // every MMA of the CTA done
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+  uint64_t *q_free = bars + 16;              // the unit's last S product done: the query tile may be replaced
+  uint64_t *o_free = bars + 17;              // the softmax warps have read the unit's O
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
   __shared__ int s_last, s_abort;
   __shared__ float xch[3][2][kRows];  // [tile & 1 | 2 for the sums][column half][row]
   __shared__ int xok[2][2][4];        // [tile & 1][column half][lane quarter]: the wait held
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int x = blockIdx.x;
-  const int sp = x % ta.nsplit;
-  x /= ta.nsplit;
-  const int rt = x % ta.rowtiles;
-  x /= ta.rowtiles;
-  const int kvh = x % p.Nkv;
-  const int b = x / p.Nkv;
-
   if (tid == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
+    mbar_init(o_free, 8);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_free[i], 1);
@@ -256,86 +299,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
-
-  Plan pl;
-  const bool ok = plan_item(p, b, pl);
   const int g = p.group;
-  const int s0 = rt * ta.tokens_per_tile;
-  const int s_end = s0 + ta.tokens_per_tile < p.S ? s0 + ta.tokens_per_tile : p.S;
-  const long long unit = ((long long)b * p.Nkv + kvh) * ta.rowtiles + rt;
-
-  // key tiles of this query tile: nc cache tiles ending at P, then tiles of new rows
-  long long P = 0;
-  int nc = 0, t_begin = 0, t_end = 0;
-  bool moves = false;
-  if (ok) {
-    P = pl.P;
-    const long long klo = P + s0 - p.W + 1 > 0 ? P + s0 - p.W + 1 : 0;
-    nc = (int)((P - klo + kKeys - 1) / kKeys);
-    const int nt = nc + (s_end + kKeys - 1) / kKeys;
-    t_begin = (int)((long long)sp * nt / ta.nsplit);
-    t_end = (int)((long long)(sp + 1) * nt / ta.nsplit);
-    moves = item_moves(p, pl);
-  }
-  const int ntl = t_end - t_begin;  // key tiles of this CTA
-  auto key0 = [&](int t) -> long long {  // absolute position of key tile t's first column
-    return t < nc ? P - (long long)(nc - t) * kKeys : P + (long long)(t - nc) * kKeys;
-  };
-  const int tpq = (s_end - s0 + 3) / 4;  // tokens per TMEM lane quarter
+  // Units u = blockIdx.x + i * gridDim.x; key tiles and query tiles are numbered across
+  // them (gk, qi), so every ring and barrier phase simply continues from unit to unit.
 
   if (warp == kLoadWarp || warp == kVLoadWarp) {
-    // ------------------------------------------------------------ TMA loads (K | V)
-    if (lane == 0 && ntl > 0) {
+    // ------------------------------------------------------------ TMA loads (K and Q | V)
+    if (lane == 0) {
       const bool value = warp == kVLoadWarp;
       const uint64_t pol = tc::policy_evict_normal(), qpol = policy_evict_first();
-      const int slice = b * p.Nkv + kvh;
       const int nst = value ? kVStages : kKStages;
       uint64_t *full = value ? v_full : k_full, *empty = value ? pv_done : k_free;
       unsigned char *ring = smem + (value ? kSmemV : kSmemK);
-      if (!value) {
-        mbar_arrive_expect_tx(q_full, kTile);
-        for (int q = 0; q < 4; ++q) {  // quarter q: tokens s0 + q * tpq ..., rows [32q, 32q + 32)
-          const int qtok = b * p.S + s0 + q * tpq;
-          tc::tma_load_3d(smem + kSmemQ + q * 4096, &maps.q, 0, kvh * g, qtok, q_full, qpol);
-          tc::tma_load_3d(smem + kSmemQ + kHalf + q * 4096, &maps.q, 64, kvh * g, qtok, q_full, qpol);
-        }
-      }
-      int iss = 0;
+      long long gk = 0;
+      int qi = 0, st = 0, ph = 0;  // tile j sits in stage j % nst, phase (j / nst) & 1
       bool fine = true;
-      for (int k = 0, st = 0, ph = 0; k < ntl && !abort_set(&s_abort); ++k) {
-        if (k >= nst && !mbar_wait(&empty[st], ph ^ 1)) {  // the tile nst back has been read
-          fine = false;
-          break;
+      for (long long u = blockIdx.x; u < ta.units && fine && !abort_set(&s_abort); u += gridDim.x) {
+        const Unit x = unit_at(p, ta, u);
+        if (x.ntl <= 0) continue;
+        const int slice = x.b * p.Nkv + x.kvh;
+        for (int k = 0; k < x.ntl; ++k) {
+          if (gk >= nst && !mbar_wait(&empty[st], ph ^ 1)) {  // the tile nst back has been read
+            fine = false;
+            break;
+          }
+          const int t = x.t_begin + k;
+          unsigned char *dst = ring + st * kTile;
+          mbar_arrive_expect_tx(&full[st], kTile);
+          if (t < x.nc) {
+            const CUtensorMap *m = value ? &maps.vc : &maps.kc;
+            const int row = (int)(x.pl.Lp - (long long)(x.nc - t) * kKeys);  // may be < 0: zeros
+            tc::tma_load_3d(dst, m, 0, row, slice, &full[st], pol);
+            tc::tma_load_3d(dst + kHalf, m, 64, row, slice, &full[st], pol);
+          } else {
+            const CUtensorMap *m = value ? &maps.vn : &maps.kn;
+            const int tokrow = x.b * p.S + (t - x.nc) * kKeys;
+            tc::tma_load_3d(dst, m, 0, x.kvh, tokrow, &full[st], pol);
+            tc::tma_load_3d(dst + kHalf, m, 64, x.kvh, tokrow, &full[st], pol);
+          }
+          ++gk;
+          if (++st == nst) st = 0, ph ^= 1;
+          // the query tile after the unit's first K tile (which only needs a free ring
+          // stage), once the previous unit's S products are done with the last one
+          if (k == 0 && !value) {
+            if (qi > 0 && !mbar_wait(q_free, (qi - 1) & 1)) {
+              fine = false;
+              break;
+            }
+            mbar_arrive_expect_tx(q_full, kTile);
+            for (int q = 0; q < 4; ++q) {  // quarter q: tokens s0 + q * tpq ..., rows [32q, 32q + 32)
+              const int qtok = x.b * p.S + x.s0 + q * x.tpq;
+              tc::tma_load_3d(smem + kSmemQ + q * 4096, &maps.q, 0, x.kvh * g, qtok, q_full, qpol);
+              tc::tma_load_3d(smem + kSmemQ + kHalf + q * 4096, &maps.q, 64, x.kvh * g, qtok, q_full, qpol);
+            }
+            ++qi;
+          }
         }
-        const int t = t_begin + k;
-        unsigned char *dst = ring + st * kTile;
-        mbar_arrive_expect_tx(&full[st], kTile);
-        if (t < nc) {
-          const CUtensorMap *m = value ? &maps.vc : &maps.kc;
-          const int row = (int)(pl.Lp - (long long)(nc - t) * kKeys);  // may be < 0: zeros
-          tc::tma_load_3d(dst, m, 0, row, slice, &full[st], pol);
-          tc::tma_load_3d(dst + kHalf, m, 64, row, slice, &full[st], pol);
-        } else {
-          const CUtensorMap *m = value ? &maps.vn : &maps.kn;
-          const int tokrow = b * p.S + (t - nc) * kKeys;
-          tc::tma_load_3d(dst, m, 0, kvh, tokrow, &full[st], pol);
-          tc::tma_load_3d(dst + kHalf, m, 64, kvh, tokrow, &full[st], pol);
-        }
-        ++iss;
-        if (++st == nst) st = 0, ph ^= 1;  // tile j sits in stage j % nst, phase (j / nst) & 1
       }
       if (!fine) {
         flag(p, GQAW_DEV_TIMEOUT);
         s_abort = 1;
       }
       // no copy may still be landing in shared memory when the CTA exits
-      for (int k = iss - nst > 0 ? iss - nst : 0; k < iss; ++k)
-        if (!mbar_wait(&full[k % nst], (k / nst) & 1)) flag(p, GQAW_DEV_TIMEOUT);
-      if (!value && !mbar_wait(q_full, 0)) flag(p, GQAW_DEV_TIMEOUT);
+      for (long long j = gk - nst > 0 ? gk - nst : 0; j < gk; ++j)
+        if (!mbar_wait(&full[j % nst], (j / nst) & 1)) flag(p, GQAW_DEV_TIMEOUT);
+      if (!value && qi > 0 && !mbar_wait(q_full, (qi - 1) & 1)) flag(p, GQAW_DEV_TIMEOUT);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0 && ntl > 0) {
+    if (lane == 0) {
       // Shared-memory descriptors are built once; an operand at byte offset x from a base
       // is the base descriptor plus x / 16 (the start-address field, bits 0-13, cannot
       // carry: every address is below 256 KB).
@@ -358,34 +390,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kKeys / 16; ++kk)
           tc::mma_bf16_ts(tmem + kTmemO, pa + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, acc || kk > 0);
       };
-      bool fine = mbar_wait(q_full, 0) && mbar_wait(&k_full[0], 0);
-      if (fine) {
-        tc::fence_after_sync();
-        issue_s(0, 0);
-        tc::mma_commit(&s_full[0]);
-        tc::mma_commit(&k_free[0]);
-      }
-      // K(j) sits in stage j % 3 with phase (j / 3) & 1.  K(k + 1) is waited for one
-      // iteration ahead, off the path from O += P(k-1) V(k-1) to S(k+1).  An abort
-      // elsewhere shows up here as an expired wait.
-      int kst = 1, kph = 0;  // K(k + 1)
-      if (fine && ntl > 1) fine = mbar_wait(&k_full[1], 0);
-      for (int k = 0; k < ntl && fine; ++k) {
-        if (k + 1 < ntl) {  // S(k + 1) while the softmax works on S(k); P(k - 1) freed its buffer
-          const int buf = (k + 1) & 1;
-          tc::fence_after_sync();
-          issue_s(kst, buf);
-          tc::mma_commit(&s_full[buf]);
-          tc::mma_commit(&k_free[kst]);
-          kst = kst == kKStages - 1 ? 0 : kst + 1;
-          if (kst == 0) kph ^= 1;
-          if (k + 2 < ntl && !(fine = mbar_wait(&k_full[kst], kph))) break;
-        }
-        fine = mbar_wait(&v_full[k & 1], (k >> 1) & 1) && mbar_wait(&p_full[k & 1], (k >> 1) & 1);
+      // K(j) sits in stage j % 3 with phase (j / 3) & 1; (kst, kph) track the next K to
+      // read.  K(k + 1) is waited for one tile ahead, off the path from O += P(k-1) V(k-1)
+      // to S(k+1).  An abort elsewhere shows up here as an expired wait.
+      long long gk = 0;
+      int qi = 0, kst = 0, kph = 0;
+      auto next_k = [&]() {
+        kst = kst == kKStages - 1 ? 0 : kst + 1;
+        if (kst == 0) kph ^= 1;
+      };
+      bool fine = true;
+      for (long long u = blockIdx.x; u < ta.units && fine; u += gridDim.x) {
+        const Unit x = unit_at(p, ta, u);
+        if (x.ntl <= 0) continue;
+        fine = mbar_wait(q_full, qi & 1) && mbar_wait(&k_full[kst], kph);
         if (!fine) break;
         tc::fence_after_sync();
-        issue_o(k & 1, k > 0);
-        tc::mma_commit(&pv_done[k & 1]);
+        issue_s(kst, (int)(gk & 1));
+        tc::mma_commit(&s_full[gk & 1]);
+        tc::mma_commit(&k_free[kst]);
+        next_k();
+        if (x.ntl == 1) tc::mma_commit(q_free);
+        if (x.ntl > 1 && !(fine = mbar_wait(&k_full[kst], kph))) break;
+        for (int k = 0; k < x.ntl && fine; ++k) {
+          const long long gt = gk + k;
+          if (k + 1 < x.ntl) {  // S(k + 1) while the softmax works on S(k); P(k - 1) freed its buffer
+            const int buf = (int)((gt + 1) & 1);
+            tc::fence_after_sync();
+            issue_s(kst, buf);
+            tc::mma_commit(&s_full[buf]);
+            tc::mma_commit(&k_free[kst]);
+            next_k();
+            if (k + 2 == x.ntl) tc::mma_commit(q_free);  // the unit's last S product
+            if (k + 2 < x.ntl && !(fine = mbar_wait(&k_full[kst], kph))) break;
+          }
+          // the first O += P V of a unit overwrites O: the softmax has read the last unit's
+          fine = mbar_wait(&v_full[gt & 1], (gt >> 1) & 1) && mbar_wait(&p_full[gt & 1], (gt >> 1) & 1) &&
+                 (k > 0 || qi == 0 || mbar_wait(o_free, (qi - 1) & 1));
+          if (!fine) break;
+          tc::fence_after_sync();
+          issue_o((int)(gt & 1), k > 0);
+          tc::mma_commit(&pv_done[gt & 1]);
+        }
+        gk += x.ntl;
+        ++qi;
       }
       if (!fine) {
         flag(p, GQAW_DEV_TIMEOUT);
@@ -396,305 +444,315 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kAppendWarp) {
     // ------------------------------------------------------------ bookkeeping, appends
-    if (ok) {
-      if (kvh == 0 && rt == 0 && sp == 0 && lane == 0) {
-        if (p.resident_out) p.resident_out[b] = (int32_t)pl.Lt;
-        if (moves) p.move_list[atomicAdd(p.move_count, 1u)] = b;
+    for (long long u = blockIdx.x; u < ta.units; u += gridDim.x) {
+      const Unit x = unit_at(p, ta, u);
+      if (!x.ok) {
+        if (x.kvh == 0 && x.rt == 0 && x.sp == 0 && lane == 0) flag(p, GQAW_DEV_BAD_SEQLEN);
+        continue;
       }
-      if (!moves && sp == 0) {  // append the new rows of this tile's tokens at L(P) + s
+      if (x.kvh == 0 && x.rt == 0 && x.sp == 0 && lane == 0) {
+        if (p.resident_out) p.resident_out[x.b] = (int32_t)x.pl.Lt;
+        if (x.moves) p.move_list[atomicAdd(p.move_count, 1u)] = x.b;
+      }
+      if (!x.moves && x.sp == 0) {  // append the new rows of this tile's tokens at L(P) + s
         constexpr int kPerRow = kD * 2 / 16, kBatch = 8;
-        const int nrow = s_end - s0;
+        const int nrow = x.s_end - x.s0;
         const int n = 2 * nrow * kPerRow;
         for (int e0 = 0; e0 < n; e0 += 32 * kBatch) {
           uint4 v[kBatch];
           size_t dst[kBatch];
 #pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            const int e = e0 + u * 32 + lane;
+          for (int uu = 0; uu < kBatch; ++uu) {
+            const int e = e0 + uu * 32 + lane;
             if (e < n) {
               const int tensor = e / (nrow * kPerRow);
               const int rem = e % (nrow * kPerRow);
-              const int s = s0 + rem / kPerRow, vec = rem % kPerRow;
-              const size_t in_row = ((size_t)b * p.S + s) * p.Nkv + kvh;
-              const size_t out_row = ((size_t)b * p.Nkv + kvh) * (size_t)p.C + (size_t)(pl.Lp + s);
-              v[u] = reinterpret_cast<const uint4 *>(static_cast<const char *>(tensor ? p.v : p.k) + in_row * kD * 2)[vec];
-              dst[u] = (out_row * kD * 2 + (size_t)vec * 16) | (size_t)tensor;  // 16-byte aligned: bit 0 free
+              const int s = x.s0 + rem / kPerRow, vec = rem % kPerRow;
+              const size_t in_row = ((size_t)x.b * p.S + s) * p.Nkv + x.kvh;
+              const size_t out_row = ((size_t)x.b * p.Nkv + x.kvh) * (size_t)p.C + (size_t)(x.pl.Lp + s);
+              v[uu] = reinterpret_cast<const uint4 *>(static_cast<const char *>(tensor ? p.v : p.k) + in_row * kD * 2)[vec];
+              dst[uu] = (out_row * kD * 2 + (size_t)vec * 16) | (size_t)tensor;  // 16-byte aligned: bit 0 free
             }
           }
 #pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            if (e0 + u * 32 + lane < n) {
-              char *base = static_cast<char *>(dst[u] & 1 ? p.prv : p.prk);
-              *reinterpret_cast<uint4 *>(base + (dst[u] & ~(size_t)1)) = v[u];
+          for (int uu = 0; uu < kBatch; ++uu) {
+            if (e0 + uu * 32 + lane < n) {
+              char *base = static_cast<char *>(dst[uu] & 1 ? p.prv : p.prk);
+              *reinterpret_cast<uint4 *>(base + (dst[uu] & ~(size_t)1)) = v[uu];
             }
           }
         }
       }
-    } else if (kvh == 0 && rt == 0 && sp == 0 && lane == 0) {
-      flag(p, GQAW_DEV_BAD_SEQLEN);
     }
   }
 
   // ---------------------------------------------------------------- softmax (warps 0-7)
-  const bool softmax = warp < 8;
-  const int wq = warp & 3;                       // TMEM lane quarter
-  const int hf = (warp >> 2) & 1;                // column half of the row
-  const int r = wq * 32 + lane;                  // query row = TMEM lane
-  const int bar_pair = 1 + wq;                   // named barrier of warps wq and wq + 4
-  // The tile's tokens are spread evenly over the four lane quarters, tpq tokens each,
-  // so a short step (S x g < 128 rows) still gives every warp real rows.
-  const int tl = lane / g;                       // token within the quarter
-  const int tok = s0 + wq * tpq + tl;
-  const int hh = lane % g;
-  const bool row_ok = softmax && ok && tl < tpq && tok < s_end;
-  const long long qi = P + tok;                  // absolute position of the row's token
-  const long long rlo = qi - p.W + 1 > 0 ? qi - p.W + 1 : 0;
-  const int h = kvh * g + hh;
-  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-  // this thread's O columns [64 hf, 64 hf + 64) and P columns [32 hf, 32 hf + 32)
-  const uint32_t to = tmem + kTmemO + hf * kHalfKeys + lane_off, tp = tmem + kTmemP + hf * 32 + lane_off;
-  float m_run = -INFINITY, l_run = 0.f, o_owed = 1.f;
-  int done = 0;
-  if (softmax && ntl > 0) {
+  if (warp < 8) {
+    const int wq = warp & 3;                       // TMEM lane quarter
+    const int hf = (warp >> 2) & 1;                // column half of the row
+    const int r = wq * 32 + lane;                  // query row = TMEM lane
+    const int bar_pair = 1 + wq;                   // named barrier of warps wq and wq + 4
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    // this thread's O columns [64 hf, 64 hf + 64) and P columns [32 hf, 32 hf + 32)
+    const uint32_t to = tmem + kTmemO + hf * kHalfKeys + lane_off, tp = tmem + kTmemP + hf * 32 + lane_off;
     const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
-    const float *bias_row = (row_ok && p.bias) ? p.bias + (long long)b * p.bsb + (long long)h * p.bsh +
-                                                     (long long)tok * p.bss
-                                               : nullptr;
-    // Visible columns of this row's half in tile k: [lo - 128 k, hi - 128 k) relative to
-    // the half's first column, clamped (consecutive key tiles start 128 positions apart,
-    // across the cache/new boundary too).  Both bounds only decrease, so they are kept
-    // at -128 once below it.
-    int lo = 0, hi = 0;
-    if (row_ok) {
-      const long long j0 = key0(t_begin) + hf * kHalfKeys;
-      lo = (int)min(max(rlo - j0, -128LL), 1LL << 30);
-      hi = (int)min(max(qi - j0 + 1, -128LL), 1LL << 30);
-    }
-    // pend: the factor O in tensor memory still owes once O += P(k-1) V(k-1) has landed
-    // (a reference raised after P(k-1) was computed against the old one)
-    float pend = 1.f;
-    for (int k = 0; k < ntl; ++k) {
-      const uint32_t ts = tmem + (k & 1) * kKeys + hf * kHalfKeys + lane_off;  // this half of S(k)
-      const uint32_t tpk = tp + (k & 1) * (kKeys / 2);
-      const int c_lo = min(max(lo, 0), kHalfKeys), c_hi = min(max(hi, 0), kHalfKeys);
-      lo = max(lo - kKeys, -kKeys);
-      hi = max(hi - kKeys, -kKeys);
-      const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[k & 1], (k >> 1) & 1));
-      tc::fence_after_sync();
-      const bool whole = __all_sync(0xffffffffu, c_lo == 0 && c_hi == kHalfKeys);
-
-      // Fast path (a plain, fully visible tile of rows that have a reference already):
-      // P against the running reference m_run in the same pass as the tile maximum.
-      // Otherwise pass 1 finds the maximum first (capped or biased logits are written
-      // back transformed, invisible columns as -inf).
-      const bool fast = okw && plain && whole && __all_sync(0xffffffffu, m_run > -INFINITY);
-      float mt = -INFINITY, lt = 0.f;
-      if (fast) {
-        lt = tile_p<false, true>(ts, tpk, 0, kHalfKeys, p.qscale, m_run, &mt);
-        mt *= p.qscale;  // qscale > 0: max commutes with the scale
-      } else if (okw && plain) {
-        mt = (whole ? tile_max<false>(ts, c_lo, c_hi) : tile_max<true>(ts, c_lo, c_hi)) * p.qscale;
-      } else if (okw) {
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
-          float v[32];
-          tc::tmem_ld32(ts + c32 * 32, v);
-          const float *brow = bias_row ? bias_row + key0(t_begin + k) + hf * kHalfKeys + c32 * 32 : nullptr;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int col = c32 * 32 + c;
-            const bool vis = col >= c_lo && col < c_hi;
-            float xv = v[c] * p.qscale;
-            if (p.capmul != 0.f) xv = p.capmul * fast_tanh(xv);
-            if (vis && brow) xv = fmaf(p.biasmul, brow[c], xv);
-            v[c] = vis ? xv : -INFINITY;
-            mx[c & 3] = fmaxf(mx[c & 3], v[c]);
-          }
-          tc::tmem_st32(ts + c32 * 32, v);
-        }
-        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      }
-
-      // Exchange with the partner half (slot k & 1: the partner has read slot k & 1 of
-      // tile k - 2 before it reached the barrier of tile k - 1).  The pair takes the
-      // careful path when either half did not take the fast one or saw a logit more than
-      // 2^16 above the reference; an expired wait on either side ends both loops.
-      xch[k & 1][hf][r] = mt;
-      if (lane == 0) xok[k & 1][hf][wq] = okw;
-      const bool careful = named_barrier_or(bar_pair, 64, !fast || mt > m_run + kDangerLog2);
-      if (!okw || !xok[k & 1][hf ^ 1][wq]) {
-        flag(p, GQAW_DEV_TIMEOUT);
-        s_abort = 1;
-        break;
-      }
-      mt = fmaxf(mt, xch[k & 1][hf ^ 1][r]);
-
-      // lazy rescale: the reference moves only when exceeded by more than 2^8 (both halves
-      // decide alike).  Careful path: O is rescaled now (with what it owes) and P is
-      // computed against the new reference.  Fast path: P(k) already used the old one, so
-      // the sum is rescaled after adding it and O owes the factor after O += P(k) V(k).
-      const bool need = mt > m_run + kRescaleLog2;
-      float alpha = 1.f;
-      if (need) {
-        alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mt);
-        m_run = mt;
-      }
-      const float oscale = careful ? pend * alpha : pend;
-      if (k > 0 && __any_sync(0xffffffffu, oscale != 1.f)) {
-        const bool okp = __all_sync(0xffffffffu, mbar_wait(&pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1));
-        if (named_barrier_or(bar_pair, 64, !okp)) {
-          flag(p, GQAW_DEV_TIMEOUT);
-          s_abort = 1;
-          break;
-        }
-        tc::fence_after_sync();
-#pragma unroll
-        for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
-          float v[32];
-          tc::tmem_ld32(to + c32 * 32, v);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] *= oscale;
-          tc::tmem_st32(to + c32 * 32, v);
-        }
-      }
-      if (careful) {
-        // ---- pass 2: P = 2^(z - m) (plain logits are still unscaled)
-        const float base = m_run == -INFINITY ? 0.f : m_run;
-        const float zs = plain ? p.qscale : 1.f;
-        l_run = l_run * alpha + (plain && !whole ? tile_p<true>(ts, tpk, c_lo, c_hi, zs, base)
-                                                 : tile_p<false>(ts, tpk, c_lo, c_hi, zs, base));
-        pend = 1.f;
-      } else {
-        l_run = (l_run + lt) * alpha;
-        pend = alpha;
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[k & 1]);
-      ++done;
-    }
-    // the last O += P V; the row sum from both halves; what O still owes joins the
-    // final scale (the epilogue multiplies O by pend)
-    const bool okf = done == ntl && __all_sync(0xffffffffu, mbar_wait(&pv_done[(ntl - 1) & 1], ((ntl - 1) >> 1) & 1));
-    xch[2][hf][r] = l_run;
-    if (named_barrier_or(bar_pair, 64, !okf)) {
-      flag(p, GQAW_DEV_TIMEOUT);
-      done = 0;
-    }
-    l_run += xch[2][hf ^ 1][r];
-    o_owed = pend;
-    tc::fence_after_sync();
-  }
-
-  // ---- epilogue: this CTA's (O, m, l) per softmax row, 32 columns at a time (the
-  // tensor-memory loads are warp-wide: every softmax warp takes part)
-  const bool have_o = softmax && ntl > 0 && done == ntl;
-  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
-  const long long orow = ((long long)b * p.S + tok) * p.Nq + h;
-  const int prow = r;  // row of the CTA's partial block
-  auto o_chunk = [&](int c32, float (&v)[32]) {  // chunk c32 of this half's 64 O columns
-    if (have_o) {
-      tc::tmem_ld32(to + c32 * 32, v);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 32; ++c) v[c] = 0.f;
-    }
-  };
-  if (ta.nsplit == 1) {
-    if (softmax) {
-      const float inv = sink_reciprocal(l_run, m_run, sink_log2(p, h)) * o_owed;
-#pragma unroll
-      for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
-        float v[32];
-        o_chunk(c32, v);
+    long long gk = 0;  // key tiles of earlier units
+    for (long long u = blockIdx.x; u < ta.units; u += gridDim.x) {
+      const Unit x = unit_at(p, ta, u);
+      // The tile's tokens are spread evenly over the four lane quarters, tpq tokens
+      // each, so a short step (S x g < 128 rows) still gives every warp real rows.
+      const int tl = lane / g;                     // token within the quarter
+      const int tok = x.s0 + wq * x.tpq + tl;
+      const int hh = lane % g;
+      const bool row_ok = x.ok && tl < x.tpq && tok < x.s_end;
+      const long long qpos = x.P + tok;            // absolute position of the row's token
+      const long long rlo = qpos - p.W + 1 > 0 ? qpos - p.W + 1 : 0;
+      const int h = x.kvh * g + hh;
+      float m_run = -INFINITY, l_run = 0.f, o_owed = 1.f;
+      int done = 0;
+      if (x.ntl > 0) {
+        const float *bias_row = (row_ok && p.bias) ? p.bias + (long long)x.b * p.bsb + (long long)h * p.bsh +
+                                                         (long long)tok * p.bss
+                                                   : nullptr;
+        // Visible columns of this row's half in tile k: [lo - 128 k, hi - 128 k) relative
+        // to the half's first column, clamped (consecutive key tiles start 128 positions
+        // apart, across the cache/new boundary too).  Both bounds only decrease, so they
+        // are kept at -128 once below it.
+        int lo = 0, hi = 0;
         if (row_ok) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 w;
-            w.x = tc::pack_bf16x2(v[c] * inv, v[c + 1] * inv);
-            w.y = tc::pack_bf16x2(v[c + 2] * inv, v[c + 3] * inv);
-            w.z = tc::pack_bf16x2(v[c + 4] * inv, v[c + 5] * inv);
-            w.w = tc::pack_bf16x2(v[c + 6] * inv, v[c + 7] * inv);
-            *reinterpret_cast<uint4 *>(out + orow * kD + hf * kHalfKeys + c32 * 32 + c) = w;
+          const long long j0 = key0(x, x.t_begin) + hf * kHalfKeys;
+          lo = (int)min(max(rlo - j0, -128LL), 1LL << 30);
+          hi = (int)min(max(qpos - j0 + 1, -128LL), 1LL << 30);
+        }
+        // pend: the factor O in tensor memory still owes once O += P(k-1) V(k-1) has
+        // landed (a reference raised after P(k-1) was computed against the old one)
+        float pend = 1.f;
+          for (int k = 0; k < x.ntl; ++k) {
+            const long long gt = gk + k;  // tile number across units
+            const uint32_t ts = tmem + (uint32_t)(gt & 1) * kKeys + hf * kHalfKeys + lane_off;  // this half of S(k)
+            const uint32_t tpk = tp + (uint32_t)(gt & 1) * (kKeys / 2);
+            const int c_lo = min(max(lo, 0), kHalfKeys), c_hi = min(max(hi, 0), kHalfKeys);
+            lo = max(lo - kKeys, -kKeys);
+            hi = max(hi - kKeys, -kKeys);
+            const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[gt & 1], (gt >> 1) & 1));
+            tc::fence_after_sync();
+            const bool whole = __all_sync(0xffffffffu, c_lo == 0 && c_hi == kHalfKeys);
+
+            // Fast path (a plain, fully visible tile of rows that have a reference already):
+            // P against the running reference m_run in the same pass as the tile maximum.
+            // Otherwise pass 1 finds the maximum first (capped or biased logits are written
+            // back transformed, invisible columns as -inf).
+            const bool fast = okw && plain && whole && __all_sync(0xffffffffu, m_run > -INFINITY);
+            float mt = -INFINITY, lt = 0.f;
+            if (fast) {
+              lt = tile_p<false, true>(ts, tpk, 0, kHalfKeys, p.qscale, m_run, &mt);
+              mt *= p.qscale;  // qscale > 0: max commutes with the scale
+            } else if (okw && plain) {
+              mt = (whole ? tile_max<false>(ts, c_lo, c_hi) : tile_max<true>(ts, c_lo, c_hi)) * p.qscale;
+            } else if (okw) {
+              float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      #pragma unroll
+              for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
+                float v[32];
+                tc::tmem_ld32(ts + c32 * 32, v);
+                const float *brow = bias_row ? bias_row + key0(x, x.t_begin + k) + hf * kHalfKeys + c32 * 32 : nullptr;
+      #pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                  const int col = c32 * 32 + c;
+                  const bool vis = col >= c_lo && col < c_hi;
+                  float xv = v[c] * p.qscale;
+                  if (p.capmul != 0.f) xv = p.capmul * fast_tanh(xv);
+                  if (vis && brow) xv = fmaf(p.biasmul, brow[c], xv);
+                  v[c] = vis ? xv : -INFINITY;
+                  mx[c & 3] = fmaxf(mx[c & 3], v[c]);
+                }
+                tc::tmem_st32(ts + c32 * 32, v);
+              }
+              mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            }
+
+            // Exchange with the partner half (slot k & 1: the partner has read slot k & 1 of
+            // tile k - 2 before it reached the barrier of tile k - 1).  The pair takes the
+            // careful path when either half did not take the fast one or saw a logit more than
+            // 2^16 above the reference; an expired wait on either side ends both loops.
+            xch[gt & 1][hf][r] = mt;
+            if (lane == 0) xok[gt & 1][hf][wq] = okw;
+            const bool careful = named_barrier_or(bar_pair, 64, !fast || mt > m_run + kDangerLog2);
+            if (!okw || !xok[gt & 1][hf ^ 1][wq]) {
+              flag(p, GQAW_DEV_TIMEOUT);
+              s_abort = 1;
+              break;
+            }
+            mt = fmaxf(mt, xch[gt & 1][hf ^ 1][r]);
+
+            // lazy rescale: the reference moves only when exceeded by more than 2^8 (both halves
+            // decide alike).  Careful path: O is rescaled now (with what it owes) and P is
+            // computed against the new reference.  Fast path: P(k) already used the old one, so
+            // the sum is rescaled after adding it and O owes the factor after O += P(k) V(k).
+            const bool need = mt > m_run + kRescaleLog2;
+            float alpha = 1.f;
+            if (need) {
+              alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mt);
+              m_run = mt;
+            }
+            const float oscale = careful ? pend * alpha : pend;
+            if (k > 0 && __any_sync(0xffffffffu, oscale != 1.f)) {
+              const bool okp = __all_sync(0xffffffffu, mbar_wait(&pv_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1));
+              if (named_barrier_or(bar_pair, 64, !okp)) {
+                flag(p, GQAW_DEV_TIMEOUT);
+                s_abort = 1;
+                break;
+              }
+              tc::fence_after_sync();
+      #pragma unroll
+              for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
+                float v[32];
+                tc::tmem_ld32(to + c32 * 32, v);
+      #pragma unroll
+                for (int c = 0; c < 32; ++c) v[c] *= oscale;
+                tc::tmem_st32(to + c32 * 32, v);
+              }
+            }
+            if (careful) {
+              // ---- pass 2: P = 2^(z - m) (plain logits are still unscaled)
+              const float base = m_run == -INFINITY ? 0.f : m_run;
+              const float zs = plain ? p.qscale : 1.f;
+              l_run = l_run * alpha + (plain && !whole ? tile_p<true>(ts, tpk, c_lo, c_hi, zs, base)
+                                                       : tile_p<false>(ts, tpk, c_lo, c_hi, zs, base));
+              pend = 1.f;
+            } else {
+              l_run = (l_run + lt) * alpha;
+              pend = alpha;
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[gt & 1]);
+            ++done;
           }
-        }
+          // the last O += P V; the row sum from both halves; what O still owes joins the
+          // final scale (the epilogue multiplies O by pend)
+          const bool okf = done == x.ntl && __all_sync(0xffffffffu, mbar_wait(&pv_done[(gk + x.ntl - 1) & 1], ((gk + x.ntl - 1) >> 1) & 1));
+          xch[2][hf][r] = l_run;
+          if (named_barrier_or(bar_pair, 64, !okf)) {
+            flag(p, GQAW_DEV_TIMEOUT);
+            done = 0;
+          }
+          l_run += xch[2][hf ^ 1][r];
+          o_owed = pend;
+          tc::fence_after_sync();
       }
-    }
-  } else {
-    // Partial block of a CTA: 33 float4 columns x 128 rows, column-major so that a warp's
-    // 32 rows are contiguous; columns 0-31 hold O, column 32 holds (m, l).
-    float4 *const part = reinterpret_cast<float4 *>(p.partials);
-    auto part_at = [&](long long cta, int c4) { return part + (cta * (kTcPartialStride / 4) + c4) * kRows + prow; };
-    if (softmax) {
+
+      // ---- epilogue of the unit: O leaves tensor memory first (then the next unit's
+      // first O += P V may overwrite it), then this half's 64 columns of (O, m, l) go out
+      const bool have_o = x.ntl > 0 && done == x.ntl;
+      float o0[32], o1[32];
+      if (have_o) {
+        tc::tmem_ld32(to, o0);
+        tc::tmem_ld32(to + 32, o1);
+      } else {
 #pragma unroll
-      for (int c32 = 0; c32 < kHalfKeys / 32; ++c32) {
-        float v[32];
-        o_chunk(c32, v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *part_at(blockIdx.x, hf * 16 + c32 * 8 + j) =
-              make_float4(v[4 * j] * o_owed, v[4 * j + 1] * o_owed, v[4 * j + 2] * o_owed, v[4 * j + 3] * o_owed);
+        for (int c = 0; c < 32; ++c) o0[c] = o1[c] = 0.f;
       }
-      if (hf == 0) *part_at(blockIdx.x, kD / 4) = make_float4(m_run, l_run, 0.f, 0.f);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      s_last = ok && atomicAdd(&p.tickets[unit], 1u) == (unsigned)ta.nsplit - 1u;
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      if (row_ok) {
-        const long long first = (long long)blockIdx.x - sp;  // split 0 of this query tile
-        const int ns = ta.nsplit < 16 ? ta.nsplit : 16;
-        float mq[16], f[16];
-        float M = -INFINITY, L = 0.f;
-        for (int q = 0; q < ns; ++q) {
-          const float4 ml = __ldcg(part_at(first + q, kD / 4));
-          mq[q] = ml.x;
-          f[q] = ml.y;  // l for now
-          M = fmaxf(M, ml.x);
-        }
-        const float mb = M == -INFINITY ? 0.f : M;
-        for (int q = 0; q < ns; ++q) {
-          const float w = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mb);
-          L += w * f[q];
-          f[q] = w;
-        }
-        const float inv = sink_reciprocal(L, mb, sink_log2(p, h));
-#pragma unroll 1
-        for (int c32 = 2 * hf; c32 < 2 * hf + 2; ++c32) {  // this half's output columns
-          float acc[32];
+      if (x.ntl > 0) {
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+      }
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+      const long long orow = ((long long)x.b * p.S + tok) * p.Nq + h;
+      if (ta.nsplit == 1) {
+        if (row_ok) {
+          const float inv = sink_reciprocal(l_run, m_run, sink_log2(p, h)) * o_owed;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-          for (int q = 0; q < ns; ++q) {
-            if (f[q] == 0.f) continue;
-            float4 v[8];
+          for (int c32 = 0; c32 < 2; ++c32) {
+            const float *v = c32 ? o1 : o0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __ldcg(part_at(first + q, c32 * 8 + j));
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              acc[4 * j] = fmaf(f[q], v[j].x, acc[4 * j]);
-              acc[4 * j + 1] = fmaf(f[q], v[j].y, acc[4 * j + 1]);
-              acc[4 * j + 2] = fmaf(f[q], v[j].z, acc[4 * j + 2]);
-              acc[4 * j + 3] = fmaf(f[q], v[j].w, acc[4 * j + 3]);
+            for (int c = 0; c < 32; c += 8) {
+              uint4 w;
+              w.x = tc::pack_bf16x2(v[c] * inv, v[c + 1] * inv);
+              w.y = tc::pack_bf16x2(v[c + 2] * inv, v[c + 3] * inv);
+              w.z = tc::pack_bf16x2(v[c + 4] * inv, v[c + 5] * inv);
+              w.w = tc::pack_bf16x2(v[c + 6] * inv, v[c + 7] * inv);
+              *reinterpret_cast<uint4 *>(out + orow * kD + hf * kHalfKeys + c32 * 32 + c) = w;
             }
           }
+        }
+      } else {
+        // Partial block of a unit: 33 float4 columns x 128 rows, column-major so that a
+        // warp's 32 rows are contiguous; columns 0-31 hold O, column 32 holds (m, l).
+        float4 *const part = reinterpret_cast<float4 *>(p.partials);
+        auto part_at = [&](long long unit, int c4) { return part + (unit * (kTcPartialStride / 4) + c4) * kRows + r; };
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 w;
-            w.x = tc::pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
-            w.y = tc::pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv);
-            w.z = tc::pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv);
-            w.w = tc::pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv);
-            *reinterpret_cast<uint4 *>(out + orow * kD + c32 * 32 + c) = w;
+        for (int c32 = 0; c32 < 2; ++c32) {
+          const float *v = c32 ? o1 : o0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *part_at(u, hf * 16 + c32 * 8 + j) =
+                make_float4(v[4 * j] * o_owed, v[4 * j + 1] * o_owed, v[4 * j + 2] * o_owed, v[4 * j + 3] * o_owed);
+        }
+        if (hf == 0) *part_at(u, kD / 4) = make_float4(m_run, l_run, 0.f, 0.f);
+        // the last split of the query tile to finish merges them (a barrier of the
+        // softmax warps: the other roles run ahead on their own units)
+        named_barrier(kSoftmaxBar, 256);
+        if (tid == 0) {
+          __threadfence();
+          s_last = x.ok && atomicAdd(&p.tickets[x.id], 1u) == (unsigned)ta.nsplit - 1u;
+        }
+        named_barrier(kSoftmaxBar, 256);
+        if (s_last) {
+          __threadfence();
+          if (row_ok) {
+            const long long first = u - x.sp;  // split 0 of this query tile
+            const int ns = ta.nsplit < 16 ? ta.nsplit : 16;
+            float mq[16], f[16];
+            float M = -INFINITY, L = 0.f;
+            for (int q = 0; q < ns; ++q) {
+              const float4 ml = __ldcg(part_at(first + q, kD / 4));
+              mq[q] = ml.x;
+              f[q] = ml.y;  // l for now
+              M = fmaxf(M, ml.x);
+            }
+            const float mb = M == -INFINITY ? 0.f : M;
+            for (int q = 0; q < ns; ++q) {
+              const float w = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - mb);
+              L += w * f[q];
+              f[q] = w;
+            }
+            const float inv = sink_reciprocal(L, mb, sink_log2(p, h));
+#pragma unroll 1
+            for (int c32 = 2 * hf; c32 < 2 * hf + 2; ++c32) {  // this half's output columns
+              float acc[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+              for (int q = 0; q < ns; ++q) {
+                if (f[q] == 0.f) continue;
+                float4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = __ldcg(part_at(first + q, c32 * 8 + j));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  acc[4 * j] = fmaf(f[q], v[j].x, acc[4 * j]);
+                  acc[4 * j + 1] = fmaf(f[q], v[j].y, acc[4 * j + 1]);
+                  acc[4 * j + 2] = fmaf(f[q], v[j].z, acc[4 * j + 2]);
+                  acc[4 * j + 3] = fmaf(f[q], v[j].w, acc[4 * j + 3]);
+                }
+              }
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 w;
+                w.x = tc::pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
+                w.y = tc::pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv);
+                w.z = tc::pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv);
+                w.w = tc::pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv);
+                *reinterpret_cast<uint4 *>(out + orow * kD + c32 * 32 + c) = w;
+              }
+            }
           }
+          if (tid == 0) p.tickets[x.id] = 0u;
         }
       }
-      if (tid == 0) p.tickets[unit] = 0u;
+      gk += x.ntl;
     }
   }
 
@@ -712,14 +770,25 @@ int mma_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t launch_mma(const Params &p, const TcArgs &ta, const TcMaps &maps, int grid, cudaStream_t stream) {
   static bool attr_done[64] = {false};
+  static int sms_cache[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !attr_done[dev]) {
     e = cudaFuncSetAttribute(mma_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done[dev] = true;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) {
+      sms_cache[dev] = sms;
+      attr_done[dev] = true;
+    } else if (grid > sms) {
+      grid = sms;
+    }
   }
+  // persistent: at most one CTA per SM, each walking the units grid-strided
+  if (dev < 64 && grid > sms_cache[dev]) grid = sms_cache[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

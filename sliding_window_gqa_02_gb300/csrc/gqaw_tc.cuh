@@ -22,6 +22,7 @@ struct TcArgs {
   int rowtiles;         // query tiles of 128 rows per (item, kv head)
   int tokens_per_tile;  // 128 / group
   int nsplit;           // key splits per query tile (<= 16)
+  long long units;      // (item, kv head, query tile, key split) units: B * Nkv * rowtiles * nsplit
 };
 
 // Tensor maps and sizes of the small-step kernel (decode and short verify steps).
