@@ -98,10 +98,10 @@ struct Plan {
   long long T, P, Lp, Lt;
 };
 
-// Per-item plan.  Returns false (and the caller flags the item) when the item's
-// seqlens_k is out of range.
-__device__ __forceinline__ bool plan_item(const Params &p, int b, Plan &pl) {
-  const long long T = (long long)p.seqlens[b] + 1;
+// Per-item plan from seqlens_k[b] (plan_from: from that value, already loaded).  Returns
+// false (and the caller flags the item) when the item's seqlens_k is out of range.
+__device__ __forceinline__ bool plan_from(const Params &p, int seqlen, Plan &pl) {
+  const long long T = (long long)seqlen + 1;
   const long long P = T - p.S;
   if (P < 0 || T > (long long)p.total) return false;
   pl.T = T;
@@ -110,6 +110,7 @@ __device__ __forceinline__ bool plan_item(const Params &p, int b, Plan &pl) {
   pl.Lt = resident_len(T, p.C, p.W);
   return true;
 }
+__device__ __forceinline__ bool plan_item(const Params &p, int b, Plan &pl) { return plan_from(p, p.seqlens[b], pl); }
 
 __device__ __forceinline__ void flag(const Params &p, uint32_t bits) { atomicOr(p.status, bits); }
 

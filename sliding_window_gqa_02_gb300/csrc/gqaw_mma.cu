@@ -218,14 +218,22 @@ struct Unit {
   bool ok, moves;
 };
 
-__device__ __forceinline__ Unit unit_at(const Params &p, const TcArgs &ta, long long u) {
+// seqlens_k of unit u's item: loaded one unit ahead, so the load's latency is not paid
+// at the unit boundary.
+__device__ __forceinline__ int unit_seqlen(const Params &p, const TcArgs &ta, long long u) {
+  return u < ta.units ? p.seqlens[(unsigned)u / (unsigned)ta.nsplit / (unsigned)ta.rowtiles / (unsigned)p.Nkv] : 0;
+}
+
+__device__ __forceinline__ Unit unit_at(const Params &p, const TcArgs &ta, long long u, int seqlen) {
   Unit x;
-  x.sp = (int)(u % ta.nsplit);
-  x.id = u / ta.nsplit;
-  x.rt = (int)(x.id % ta.rowtiles);
-  x.kvh = (int)((x.id / ta.rowtiles) % p.Nkv);
-  x.b = (int)(x.id / ta.rowtiles / p.Nkv);
-  x.ok = plan_item(p, x.b, x.pl);
+  const unsigned uu = (unsigned)u, id = uu / (unsigned)ta.nsplit;  // units < 2^31 (host check)
+  const unsigned slice = id / (unsigned)ta.rowtiles;
+  x.sp = (int)(uu - id * (unsigned)ta.nsplit);
+  x.id = id;
+  x.rt = (int)(id - slice * (unsigned)ta.rowtiles);
+  x.kvh = (int)(slice % (unsigned)p.Nkv);
+  x.b = (int)(slice / (unsigned)p.Nkv);
+  x.ok = plan_from(p, seqlen, x.pl);
   x.s0 = x.rt * ta.tokens_per_tile;
   x.s_end = x.s0 + ta.tokens_per_tile < p.S ? x.s0 + ta.tokens_per_tile : p.S;
   x.tpq = (x.s_end - x.s0 + 3) / 4;  // tokens per TMEM lane quarter
@@ -238,8 +246,8 @@ __device__ __forceinline__ Unit unit_at(const Params &p, const TcArgs &ta, long 
     const long long klo = x.P + x.s0 - p.W + 1 > 0 ? x.P + x.s0 - p.W + 1 : 0;
     x.nc = (int)((x.P - klo + kKeys - 1) / kKeys);
     const int nt = x.nc + (x.s_end + kKeys - 1) / kKeys;
-    x.t_begin = (int)((long long)x.sp * nt / ta.nsplit);
-    x.ntl = (int)((long long)(x.sp + 1) * nt / ta.nsplit) - x.t_begin;
+    x.t_begin = (int)((unsigned)(x.sp * nt) / (unsigned)ta.nsplit);
+    x.ntl = (int)((unsigned)((x.sp + 1) * nt) / (unsigned)ta.nsplit) - x.t_begin;
     x.moves = item_moves(p, x.pl);
   }
   return x;
@@ -314,9 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long gk = 0;
       int qi = 0, st = 0, ph = 0;  // tile j sits in stage j % nst, phase (j / nst) & 1
       bool fine = true;
+      Unit x = unit_at(p, ta, blockIdx.x, unit_seqlen(p, ta, blockIdx.x));
       for (long long u = blockIdx.x; u < ta.units && fine && !abort_set(&s_abort); u += gridDim.x) {
-        const Unit x = unit_at(p, ta, u);
-        if (x.ntl <= 0) continue;
+        // the next unit is decoded while this one's loads wait for ring stages
+        const int sq_next = unit_seqlen(p, ta, u + gridDim.x);
+        Unit nx;
+        bool have_nx = false;
+        auto decode_next = [&]() {
+          if (!have_nx) nx = unit_at(p, ta, u + gridDim.x, sq_next);
+          have_nx = true;
+        };
         const int slice = x.b * p.Nkv + x.kvh;
         for (int k = 0; k < x.ntl; ++k) {
           if (gk >= nst && !mbar_wait(&empty[st], ph ^ 1)) {  // the tile nst back has been read
@@ -353,8 +368,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::tma_load_3d(smem + kSmemQ + kHalf + q * 4096, &maps.q, 64, x.kvh * g, qtok, q_full, qpol);
             }
             ++qi;
+            if (u + gridDim.x < ta.units) {  // the next unit's query tile into L2
+              decode_next();
+              for (int q = 0; q < 4; ++q)
+                for (int c0 = 0; c0 < 128; c0 += 64)
+                  tc::tma_prefetch_3d(&maps.q, c0, nx.kvh * g, nx.b * p.S + nx.s0 + q * nx.tpq);
+            }
           }
+          if (k == 0) decode_next();
         }
+        decode_next();
+        x = nx;
       }
       if (!fine) {
         flag(p, GQAW_DEV_TIMEOUT);
@@ -400,9 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kst == 0) kph ^= 1;
       };
       bool fine = true;
+      Unit x = unit_at(p, ta, blockIdx.x, unit_seqlen(p, ta, blockIdx.x));
       for (long long u = blockIdx.x; u < ta.units && fine; u += gridDim.x) {
-        const Unit x = unit_at(p, ta, u);
-        if (x.ntl <= 0) continue;
+        // the next unit is decoded right after this one's first S product is issued
+        const int sq_next = unit_seqlen(p, ta, u + gridDim.x);
+        if (x.ntl <= 0) {
+          x = unit_at(p, ta, u + gridDim.x, sq_next);
+          continue;
+        }
         fine = mbar_wait(q_full, qi & 1) && mbar_wait(&k_full[kst], kph);
         if (!fine) break;
         tc::fence_after_sync();
@@ -410,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(&s_full[gk & 1]);
         tc::mma_commit(&k_free[kst]);
         next_k();
+        const Unit nx = unit_at(p, ta, u + gridDim.x, sq_next);
         if (x.ntl == 1) tc::mma_commit(q_free);
         if (x.ntl > 1 && !(fine = mbar_wait(&k_full[kst], kph))) break;
         for (int k = 0; k < x.ntl && fine; ++k) {
@@ -434,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         gk += x.ntl;
         ++qi;
+        x = nx;
       }
       if (!fine) {
         flag(p, GQAW_DEV_TIMEOUT);
@@ -445,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kAppendWarp) {
     // ------------------------------------------------------------ bookkeeping, appends
     for (long long u = blockIdx.x; u < ta.units; u += gridDim.x) {
-      const Unit x = unit_at(p, ta, u);
+      const Unit x = unit_at(p, ta, u, unit_seqlen(p, ta, u));
       if (!x.ok) {
         if (x.kvh == 0 && x.rt == 0 && x.sp == 0 && lane == 0) flag(p, GQAW_DEV_BAD_SEQLEN);
         continue;
@@ -497,8 +528,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t to = tmem + kTmemO + hf * kHalfKeys + lane_off, tp = tmem + kTmemP + hf * 32 + lane_off;
     const bool plain = p.capmul == 0.f && p.bias == nullptr;  // logits need only the scale
     long long gk = 0;  // key tiles of earlier units
+    Unit x = unit_at(p, ta, blockIdx.x, unit_seqlen(p, ta, blockIdx.x));
     for (long long u = blockIdx.x; u < ta.units; u += gridDim.x) {
-      const Unit x = unit_at(p, ta, u);
+      // the next unit is decoded while the first S product of this one is computed
+      const int sq_next = unit_seqlen(p, ta, u + gridDim.x);
+      Unit nx;
+      bool have_nx = false;
+      auto decode_next = [&]() {
+        if (!have_nx) nx = unit_at(p, ta, u + gridDim.x, sq_next);
+        have_nx = true;
+      };
       // The tile's tokens are spread evenly over the four lane quarters, tpq tokens
       // each, so a short step (S x g < 128 rows) still gives every warp real rows.
       const int tl = lane / g;                     // token within the quarter
@@ -534,7 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c_lo = min(max(lo, 0), kHalfKeys), c_hi = min(max(hi, 0), kHalfKeys);
             lo = max(lo - kKeys, -kKeys);
             hi = max(hi - kKeys, -kKeys);
-            const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[gt & 1], (gt >> 1) & 1));
+            if (k == 0) decode_next();
+        const bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[gt & 1], (gt >> 1) & 1));
             tc::fence_after_sync();
             const bool whole = __all_sync(0xffffffffu, c_lo == 0 && c_hi == kHalfKeys);
 
@@ -753,6 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       gk += x.ntl;
+      decode_next();
+      x = nx;
     }
   }
 
