@@ -360,28 +360,58 @@ class Harness:
 
     def step_e2e(self, t):
         """One step through the C ABI from pinned host buffers: copy the step's query,
-        key, value and seqlens_k in, run the step, copy the output back."""
-        i = t % len(self.q)
-        self.q[0].copy_(self.q_host[i], non_blocking=True)
-        self.k[0].copy_(self.k_host[i], non_blocking=True)
-        self.v[0].copy_(self.v_host[i], non_blocking=True)
-        self.seq[t].copy_(self.seq_host[t], non_blocking=True)
-        a = self.args_e2e[t]
-        self.gqaw.check(self.gqaw.gqa_windowed_step(a, self.stream.cuda_stream))
-        self.out_host.copy_(self.out, non_blocking=True)
+        key, value and seqlens_k in, run the step, copy the output back.  The copies run
+        on their own streams (one for input, one for read-back) into one of two device
+        slots, so those of step t + 1 overlap the kernels of step t (what a serving loop
+        does); events keep each slot's copies, kernels and read-back in order."""
+        torch = self.torch
+        s, i, cs = t % 2, t % len(self.q), self.cstream
+        cs.wait_event(self.ev_done[s])  # step t - 2's kernels have read this slot
+        with torch.cuda.stream(cs):
+            self.q_e[s].copy_(self.q_host[i], non_blocking=True)
+            self.k_e[s].copy_(self.k_host[i], non_blocking=True)
+            self.v_e[s].copy_(self.v_host[i], non_blocking=True)
+            self.seq[t].copy_(self.seq_host[t], non_blocking=True)
+            self.ev_in[s].record(cs)
+        self.stream.wait_event(self.ev_in[s])
+        self.stream.wait_event(self.ev_out[s])  # step t - 2's output has been read back
+        self.gqaw.check(self.gqaw.gqa_windowed_step(self.args_e2e[t], self.stream.cuda_stream))
+        self.ev_done[s].record(self.stream)
+        ds = self.dstream
+        ds.wait_event(self.ev_done[s])
+        with torch.cuda.stream(ds):
+            self.out_host_e[s].copy_(self.out_e[s], non_blocking=True)
+            self.ev_out[s].record(ds)
+
+    def end_e2e(self):
+        """The launching stream waits for the last read-backs (end of the timed region)."""
+        for s in range(2):
+            self.stream.wait_event(self.ev_out[s])
 
     def prepare_e2e(self):
-        # every e2e step reads its inputs from slot 0, refreshed from the host
+        torch = self.torch
         sh = self.sh
+        self.cstream = torch.cuda.Stream()  # host-to-device copies
+        self.dstream = torch.cuda.Stream()  # device-to-host read-back
+        self.q_e = [torch.empty_like(self.q[0]) for _ in range(2)]
+        self.k_e = [torch.empty_like(self.k[0]) for _ in range(2)]
+        self.v_e = [torch.empty_like(self.v[0]) for _ in range(2)]
+        self.out_e = [torch.empty_like(self.out) for _ in range(2)]
+        self.out_host_e = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory() for _ in range(2)]
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_done = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        for e in self.ev_done + self.ev_out:
+            e.record(self.stream)
         self.args_e2e = [self.gqaw.make_args(
-            self.q[0], self.k[0], self.v[0], self.pk, self.pv, self.pk, self.pv, self.seq[t], self.totals[t],
-            sh.Nq, sh.Nkv, sh.W, self.out, workspace=self.ws, softcap=sh.softcap, attention_bias=self.bias,
-            bias_strides=self.bias_strides, split_keys=self.split_keys, head_sink=self.head_sink,
-            cos_cache=self.cos, sin_cache=self.sin, k_scale=self.ks, v_scale=self.vs) for t in range(self.n)]
+            self.q_e[t % 2], self.k_e[t % 2], self.v_e[t % 2], self.pk, self.pv, self.pk, self.pv, self.seq[t],
+            self.totals[t], sh.Nq, sh.Nkv, sh.W, self.out_e[t % 2], workspace=self.ws, softcap=sh.softcap,
+            attention_bias=self.bias, bias_strides=self.bias_strides, split_keys=self.split_keys,
+            head_sink=self.head_sink, cos_cache=self.cos, sin_cache=self.sin, k_scale=self.ks, v_scale=self.vs)
+            for t in range(self.n)]
         e = self.q_host[0].element_size()
         self.h2d = (self.q_host[0].numel() + self.k_host[0].numel() + self.v_host[0].numel()) * e + self.B * 4
         self.d2h = self.out.numel() * self.out.element_size()
-
 
 
 def run_gpu(args, rank, world):
@@ -514,8 +544,10 @@ def run_gpu(args, rank, world):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    h.cstream.wait_event(e0)  # no copy of the timed steps starts before the timed region
     for t in range(Wm, Wm + K):
         h.step_e2e(t)
+    h.end_e2e()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world)
