@@ -463,3 +463,21 @@ def test_tensor_core_path_splits_and_buffers(split_keys, inplace):
         bias = wl.bias(sh.B, sh.Nq, S, total, 1600 + t, std=1.0)
         p.step(q, k, v, T + S - 1, total=total, bias=bias)
         T = T + S
+
+
+@pytest.mark.parametrize("split_keys", [0, 256])
+@pytest.mark.parametrize("inplace", [True, False])
+def test_tensor_core_path_more_units_than_sms(split_keys, inplace):
+    """The multi-token kernel is persistent (one CTA per SM walking its units): with 4
+    items x 8 kv heads x 5 query tiles (S = 130, group 4) there are 160 units -- more with
+    key splits -- so CTAs run several units back to back, their key-tile rings and
+    barrier phases running on across units.  A ragged batch (one item from an empty
+    cache, one crossing a block eviction) and a second step on the advanced cache."""
+    sh = wl.Shape("tcu", B=4, Nq=32, Nkv=8, D=128, W=100, C=109, dtype=wl.BF16)
+    pk, pv = wl.cache(sh, 17)
+    p = _shape_pair(sh, past_key=pk, past_value=pv, inplace=inplace, split_keys=split_keys)
+    T = np.array([0, 40, 95, 300], np.int64)
+    for t in range(2):
+        q, k, v = wl.step_inputs(sh, 130, 1700 + t)
+        p.step(q, k, v, T + 130 - 1)
+        T = T + 130
