@@ -200,7 +200,8 @@ class ClockSampler:
 # The attention kernel a step runs on (the library's dispatch rule), the short name of
 # its profile summaries and the sources that define it.
 KERNELS = {
-    "mmad": ("mma_decode_kernel (tcgen05)", ("gqaw_mmad.cuh", "gqaw_mmad.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
+    "mmad": ("mma_decode_kernel (tcgen05)",
+             ("gqaw_mmad.cuh", "gqaw_mmad.cu", "gqaw_mmad_q8.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
     "mma": ("mma_attend_kernel (tcgen05)", ("gqaw_mma.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
     "attend": ("attend_kernel", ("gqaw_attend.cuh", "gqaw_internal.cuh", "gqaw_attend_bf16.cu", "gqaw_attend_f32.cu")),
 }
@@ -208,10 +209,10 @@ KERNELS = {
 
 def attention_kernel(sh, S, quant=None):
     g = sh.Nq // sh.Nkv
+    if sh.dtype == "bf16" and sh.D == 128 and S * g <= 32:
+        return "mmad"  # code caches too (widened to fp16 tiles in the kernel)
     if quant:
         return "attend"
-    if sh.dtype == "bf16" and sh.D == 128 and S * g <= 32:
-        return "mmad"
     if sh.dtype == "bf16" and sh.D == 128 and S >= 2 and g <= 32 and 32 % g == 0:
         return "mma"
     return "attend"

@@ -37,9 +37,11 @@
 // Part 1.1, k_scale and v_scale): the TMA streams tiles of 1-byte codes (half the bytes)
 // and dedicated widening warps turn each code row into an fp16 operand row of the same
 // swizzled layout (int8 exactly through the fp16 mantissa, e4m3 by the hardware pair
-// conversion), K into one of two buffers as soon as its codes land, V once the previous
-// P.V is done; the MMAs then run on fp16 operands (an fp16 copy of the query), the key
-// scale is folded into the logit scale and the value scale into the finished rows.
+// conversion), K into its buffer once the previous tile's S^T is done, V into one of two
+// buffers once the P.V of two tiles back is done, so that widening, S^T, softmax and P.V
+// of consecutive tiles overlap; the MMAs then run on fp16 operands (an fp16 copy of the
+// query), the key scale is folded into the logit scale and the value scale into the
+// finished rows.
 //
 // Every mbarrier wait is bounded; a wait that expires flags GQAW_DEV_TIMEOUT and the
 // CTA winds down.  The softmax warps decide to stop only through a reducing barrier,
@@ -62,12 +64,12 @@ constexpr int kHalf = 16384;               // one 64-dim half of a K or V tile
 constexpr int kStages = 3;
 constexpr int kStageBytes = 4 * kHalf;     // K and V, two halves each
 constexpr int kCodeStage = 2 * kHalf;      // quantized cache: K and V code tiles (128 x 128 bytes each)
-constexpr int kK16 = kStages * kCodeStage;  // quantized cache: two widened K tiles (fp16, 32 KB each)
-constexpr int kV16 = kK16 + 4 * kHalf;      // quantized cache: the widened V tile
+constexpr int kK16 = kStages * kCodeStage;  // quantized cache: the widened K tile (fp16, 32 KB)
+constexpr int kV16 = kK16 + 2 * kHalf;      // quantized cache: two widened V tiles (fp16, 32 KB each)
 constexpr float kRescale = 8.0f;           // lazy rescale threshold (log2 units)
 constexpr int kBar = 1;                    // named barrier of the softmax warps
-constexpr int kNumBars = 23;
-static_assert(kV16 + 2 * kHalf == kStages * kStageBytes, "both layouts put Q at the same offset");
+constexpr int kNumBars = 24;
+static_assert(kV16 + 4 * kHalf == kStages * kStageBytes, "both layouts put Q at the same offset");
 
 template <int NPAD>
 struct Lay {
@@ -343,7 +345,8 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
   // MMA thread looks at it, and a parity wait cannot tell two phases apart.
   uint64_t *p_full = bars + 10, *o_done = bars + 12, *o_free = bars + 14;
   uint64_t *q_full = bars + 15, *q_free = bars + 17, *mma_done = bars + 19;
-  // quantized cache: widened K tile [2] ready, widened V tile ready
+  // quantized cache: widened K tile ready, widened V tile [2] ready (both per tile parity:
+  // a parity wait cannot tell apart two phases of one barrier)
   uint64_t *kconv_full = bars + 20, *vconv_full = bars + 22;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kSlot);
   __shared__ int s_abort, s_last;
@@ -360,9 +363,10 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       mbar_init(&empty[i], kQ8 ? 32 * kWidenW : 1);  // codes: free once widened
     }
     if constexpr (kQ8) {  // the widening warps' barriers (counts are at least 1)
-      mbar_init(&kconv_full[0], 32 * kWidenW);
-      mbar_init(&kconv_full[1], 32 * kWidenW);
-      mbar_init(vconv_full, 32 * kWidenW);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&kconv_full[i], 32 * kWidenW);
+        mbar_init(&vconv_full[i], 32 * kWidenW);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -390,7 +394,8 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
   pdl_wait();                // the previous kernel in the stream has completed
 
   auto stage = [&](int kc) { return smem + (kc % kStages) * (kQ8 ? kCodeStage : kStageBytes); };
-  auto k16buf = [&](int kc) { return smem + kK16 + (kc & 1) * 2 * kHalf; };
+  unsigned char *const k16buf = smem + kK16;
+  auto v16buf = [&](int kc) { return smem + kV16 + (kc & 1) * 2 * kHalf; };
   auto qbuf = [&](int ui) { return smem + L::kQ + (ui & 1) * 2 * L::kQHalf; };
   auto pbuf = [&](int kc) { return smem + L::kP + (kc & 1) * 2 * L::kQHalf; };
 
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
           return false;
         if (t.kc >= 2 && !mbar_wait(&s_free[t.kc & 1], ((t.kc - 2) >> 1) & 1)) return false;
         tc::fence_after_sync();
-        unsigned char *kb = kQ8 ? k16buf(t.kc) : stage(t.kc), *qb = qbuf(t.ui);
+        unsigned char *kb = kQ8 ? k16buf : stage(t.kc), *qb = qbuf(t.ui);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const int half = kk / 4, off = (kk % 4) * 32;
@@ -473,22 +478,21 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       bool hc = w.next(p, cur), fine = true;
       if (hc) fine = mma_s(cur);
       while (hc && fine && !*reinterpret_cast<volatile int *>(&s_abort)) {
-        // S^T of the next tile while this one is in softmax.  With a quantized cache the
-        // widening warps produce the next tile's K after this tile's V, so its S^T is
-        // issued after this tile's P.V.
+        // S^T of the next tile while this one is in softmax.  (A quantized cache's next K
+        // needs only this tile's S^T done and the P.V of two tiles back, both issued.)
         const bool hn = w.next(p, nxt);
-        if (!kQ8 && hn && !mma_s(nxt)) {
+        if (hn && !mma_s(nxt)) {
           fine = false;
           break;
         }
         if (!mbar_wait(&p_full[cur.kc & 1], (cur.kc >> 1) & 1) ||
-            (kQ8 && !mbar_wait(vconv_full, cur.kc & 1)) ||
+            (kQ8 && !mbar_wait(&vconv_full[cur.kc & 1], (cur.kc >> 1) & 1)) ||
             (cur.first && cur.ui >= 1 && !mbar_wait(o_free, (cur.ui - 1) & 1))) {
           fine = false;
           break;
         }
         tc::fence_after_sync();
-        unsigned char *vb = kQ8 ? smem + kV16 : stage(cur.kc) + 2 * kHalf;
+        unsigned char *vb = kQ8 ? v16buf(cur.kc) : stage(cur.kc) + 2 * kHalf;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           // V^T: M = dims in two 64-dim halves 16 KB apart, K = keys in 8-key groups 1 KB apart
@@ -499,10 +503,6 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         tc::mma_commit(&o_done[cur.kc & 1]);
         if (!kQ8) tc::mma_commit(&empty[cur.kc % kStages]);
         if (cur.last) tc::mma_commit(&q_free[cur.ui & 1]);
-        if (kQ8 && hn && !mma_s(nxt)) {
-          fine = false;
-          break;
-        }
         cur = nxt;
         hc = hn;
       }
@@ -516,9 +516,10 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
   } else if (warp >= 4 * CG) {
     // ------------------------------------------------------------ widening warps
     if constexpr (kQ8) {
-      // Thread i widens rows i, i + 32 * WW, ... of each code tile: K(k) into fp16 buffer
-      // k & 1 once MMA1 of tile k - 2 is done with it, V(k) into the single fp16 buffer
-      // once P.V of tile k - 1 is done (keys past P as zeros).
+      // Thread i widens rows i, i + 32 * WW, ... of each code tile: K(k) into the fp16 K
+      // buffer once S^T of tile k - 1 is done with it, V(k) into fp16 buffer k & 1 once
+      // P.V of tile k - 2 is done (keys past P as zeros).  Each wait is for a phase the
+      // barrier can have reached only after the one these warps saw a tile earlier.
       const int i0 = tid - 128 * CG;
       constexpr int kStep = 32 * kWidenW;
       Walker w{ufirst - 1, ulast, tb, te, TPU, 0, 0, 0, -1, DUnit()};
@@ -529,16 +530,16 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         const long long j0 = t.x.lo + (long long)t.lt * kKeys;
         const int nvalid = (int)(t.x.pl.P - j0 < kKeys ? t.x.pl.P - j0 : kKeys);
         fine = mbar_wait(&full[kc % kStages], (kc / kStages) & 1);
-        if (fine && kc >= 2) fine = mbar_wait(&s_full[kc & 1], ((kc - 2) >> 1) & 1);
+        if (fine && kc >= 1) fine = mbar_wait(&s_full[(kc - 1) & 1], ((kc - 1) >> 1) & 1);
         tc::fence_after_sync();
-        for (int r = i0; r < kKeys; r += kStep) widen_row<QT>(stage(kc), k16buf(kc), r, false);
+        for (int r = i0; r < kKeys; r += kStep) widen_row<QT>(stage(kc), k16buf, r, false);
         tc::fence_proxy_async_smem();
         mbar_arrive(&kconv_full[kc & 1]);
-        if (fine && kc >= 1) fine = mbar_wait(&o_done[(kc - 1) & 1], ((kc - 1) >> 1) & 1);
+        if (fine && kc >= 2) fine = mbar_wait(&o_done[kc & 1], ((kc - 2) >> 1) & 1);
         tc::fence_after_sync();
-        for (int r = i0; r < kKeys; r += kStep) widen_row<QT>(stage(kc) + kHalf, smem + kV16, r, r >= nvalid);
+        for (int r = i0; r < kKeys; r += kStep) widen_row<QT>(stage(kc) + kHalf, v16buf(kc), r, r >= nvalid);
         tc::fence_proxy_async_smem();
-        mbar_arrive(vconv_full);
+        mbar_arrive(&vconv_full[kc & 1]);
         mbar_arrive(&empty[kc % kStages]);  // both code tiles of this stage are widened
       }
       if (!fine) {
@@ -970,6 +971,11 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
     e = cudaFuncSetAttribute(mma_decode_kernel<16, 8, 2, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay<16>::kAlloc);
     if (e != cudaSuccess) return e;
+    if constexpr (QT == GQAW_I8) {
+      e = cudaFuncSetAttribute(mma_decode_kernel<16, 4, 1, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Lay<16>::kAlloc);
+      if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(mma_decode_kernel<16, 16, 2, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay<16>::kAlloc);
     if (e != cudaSuccess) return e;
@@ -985,8 +991,10 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
   if (grid > V) grid = V;
   const int nv = p.S * p.group;
   // softmax warps: 4 per column group, two groups (four for 32 bf16 rows): more warps to
-  // overlap the per-row work than rows need
-  const int cg = nv <= 16 || QT != 0 ? 2 : 4;
+  // overlap the per-row work than rows need.  int8 codes take about twice the widening
+  // arithmetic of e4m3 (the pair conversion): for units of up to 4 rows they get four
+  // widening warps and one column group (measured 13% faster; e4m3 is faster with two).
+  const int cg = QT == GQAW_I8 && nv <= 4 ? 1 : nv <= 16 || QT != 0 ? 2 : 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(cg == 1 ? Warps<1, QT>::kThreads : cg == 2 ? Warps<2, QT>::kThreads : Warps<4, 0>::kThreads);
@@ -997,14 +1005,19 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.dynamicSmemBytes = nv <= 16 ? Lay<16>::kAlloc : Lay<32>::kAlloc;
-  if (nv <= 4)
-    e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4, 2, QT>, p, ta, maps);
-  else if (nv <= 8)
+  if (nv <= 4) {
+    if constexpr (QT == GQAW_I8)
+      e = cg == 1 ? cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4, 1, QT>, p, ta, maps)
+                  : cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4, 2, QT>, p, ta, maps);
+    else
+      e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 4, 2, QT>, p, ta, maps);
+  } else if (nv <= 8) {
     e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 8, 2, QT>, p, ta, maps);
-  else if (nv <= 16)
+  } else if (nv <= 16) {
     e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<16, 16, 2, QT>, p, ta, maps);
-  else
+  } else {
     e = cudaLaunchKernelEx(&cfg, mma_decode_kernel<32, 32, QT == 0 ? 4 : 2, QT>, p, ta, maps);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
