@@ -1,0 +1,234 @@
+"""A model of the small-step tensor-core kernel's barrier protocol for code caches (no GPU).
+
+``mma_decode_kernel`` (csrc/gqaw_mmad.cuh) runs four roles per CTA that meet only at
+mbarriers: the TMA producer, the widening warps, the MMA issuer and the softmax warps.
+With a code cache, per key tile k:
+
+  producer   Q of a unit into buffer u & 1 once the unit two back is done with it;
+             codes of tile k into stage k % 3 once tile k - 3 is widened;
+  widening   K(k) into the single fp16 K tile once S^T(k - 1) is done;
+             V(k) into fp16 V tile k & 1 once P.V(k - 2) is done;
+  MMA        S^T(k + 1) before P.V(k); P.V(k) once P(k) and V(k) are ready (and, on a
+             unit's first tile, once the previous unit's O has been read);
+  softmax    reads S^T(k), frees it; writes P(k) into buffer k & 1 once P.V(k - 2) is
+             done; may rescale O once P.V(k - 1) is done; reads O after a unit's last P.V.
+
+This model runs the four roles as coroutines under a random scheduler, with TMA loads
+and MMAs completing in any order and a commit arriving once every MMA issued before it
+has completed (MMAs into one accumulator run in issue order).  It checks that every
+parity wait finds its barrier exactly k or k + 1 phases along (a parity wait cannot tell
+phases two apart), that no buffer is rewritten while an MMA or role still uses it, and
+that the roles never deadlock.  A planted early reuse of a V tile must be caught, so the
+model is not vacuous.
+"""
+from __future__ import annotations
+
+import random
+
+import pytest
+
+
+class _Bar:
+    def __init__(self, count):
+        self.count, self.pending, self.n = count, count, 0
+
+    def arrive(self):
+        assert self.pending > 0
+        self.pending -= 1
+        if self.pending == 0:
+            self.n += 1  # one more completed phase
+            self.pending = self.count
+
+
+def _run(units, seed, v_reuse_lag=2, max_steps=400000):
+    """Run the protocol over units of the given key-tile counts; returns the violations.
+    ``v_reuse_lag``: the widening warps reuse V tile k & 1 once P.V(k - lag) is done (2 is
+    the kernel's rule)."""
+    rnd = random.Random(seed)
+    tiles, kc = [], 0
+    for ui, nt in enumerate(units):
+        for lt in range(nt):
+            tiles.append(dict(kc=kc, ui=ui, first=lt == 0, last=lt == nt - 1))
+            kc += 1
+    bars = {("full", i): _Bar(1) for i in range(3)}
+    bars.update({("empty", i): _Bar(1) for i in range(3)})
+    for i in range(2):
+        for name in ("s_full", "s_free", "p_full", "o_done", "q_full", "q_free", "kconv", "vconv"):
+            bars[(name, i)] = _Bar(1)
+    bars["o_free"] = _Bar(1)
+    mmas, commits, loads, errors = [], [], [], []
+    held = dict(K16=None, V16=[None, None], P=[None, None])
+
+    def ready(name, k):
+        n = bars[name].n
+        if n > k + 1:
+            errors.append("wait on %s for phase %d after %d phases (ambiguous)" % (name, k, n))
+        if n < k:
+            errors.append("wait on %s for phase %d after only %d phases (passes early)" % (name, k, n))
+        return n >= k + 1
+
+    def in_use(buf):
+        return [m for m in mmas if not m["done"] and (buf in m["reads"] or buf in m["writes"])]
+
+    def role_writes(buf, who):
+        if in_use(buf):
+            errors.append("%s rewrites %s while %s uses it" % (who, buf, in_use(buf)[0]["name"]))
+
+    def issue(name, reads, writes):
+        for w in writes:
+            # MMAs into one accumulator run in issue order
+            if [m for m in in_use(w) if not (w in m["writes"] and w not in m["reads"])]:
+                errors.append("MMA %s writes %s while it is in use" % (name, w))
+        mmas.append(dict(name=name, reads=reads, writes=writes, done=False))
+
+    def commit(name):
+        commits.append((name, [m for m in mmas if not m["done"]]))
+
+    def producer():
+        for t in tiles:
+            k, u = t["kc"], t["ui"]
+            if t["first"]:
+                while u >= 2 and not ready(("q_free", u & 1), (u - 2) >> 1):
+                    yield
+                role_writes(("Q", u & 1), "TMA of Q")
+                loads.append([("q_full", u & 1), False])
+            while k >= 3 and not ready(("empty", k % 3), k // 3 - 1):
+                yield
+            loads.append([("full", k % 3), False])
+            yield
+
+    def widening():
+        lag = v_reuse_lag
+        for t in tiles:
+            k = t["kc"]
+            while not ready(("full", k % 3), k // 3):
+                yield
+            while k >= 1 and not ready(("s_full", (k - 1) & 1), (k - 1) >> 1):
+                yield
+            role_writes("K16", "widening of K(%d)" % k)
+            held["K16"] = k
+            bars[("kconv", k & 1)].arrive()
+            yield
+            while k >= lag and not ready(("o_done", (k - lag) & 1), (k - lag) >> 1):
+                yield
+            role_writes(("V16", k & 1), "widening of V(%d)" % k)
+            held["V16"][k & 1] = k
+            bars[("vconv", k & 1)].arrive()
+            bars[("empty", k % 3)].arrive()
+            yield
+
+    def mma():
+        def s_of(t):
+            k, u = t["kc"], t["ui"]
+            while t["first"] and not ready(("q_full", u & 1), u >> 1):
+                yield
+            while not ready(("kconv", k & 1), k >> 1):
+                yield
+            while k >= 2 and not ready(("s_free", k & 1), (k - 2) >> 1):
+                yield
+            if held["K16"] != k:
+                errors.append("S(%d) reads the K tile of tile %s" % (k, held["K16"]))
+            issue("S(%d)" % k, ["K16", ("Q", u & 1)], [("S", k & 1)])
+            commit(("s_full", k & 1))
+            yield
+
+        if not tiles:
+            return
+        yield from s_of(tiles[0])
+        for i, t in enumerate(tiles):
+            if i + 1 < len(tiles):
+                yield from s_of(tiles[i + 1])
+            k, u = t["kc"], t["ui"]
+            while not ready(("p_full", k & 1), k >> 1):
+                yield
+            while not ready(("vconv", k & 1), k >> 1):
+                yield
+            while t["first"] and u >= 1 and not ready("o_free", u - 1):
+                yield
+            if held["V16"][k & 1] != k or held["P"][k & 1] != k:
+                errors.append("P.V(%d) reads V of tile %s, P of tile %s" % (k, held["V16"][k & 1], held["P"][k & 1]))
+            issue("PV(%d)" % k, [("V16", k & 1), ("P", k & 1)], ["O"])
+            commit(("o_done", k & 1))
+            if t["last"]:
+                commit(("q_free", u & 1))
+            yield
+
+    def softmax():
+        for t in tiles:
+            k, u = t["kc"], t["ui"]
+            while not ready(("s_full", k & 1), k >> 1):
+                yield
+            if in_use(("S", k & 1)):
+                errors.append("softmax reads S(%d) before it is complete" % k)
+            yield
+            bars[("s_free", k & 1)].arrive()
+            while k >= 2 and not ready(("o_done", k & 1), (k - 2) >> 1):
+                yield
+            role_writes(("P", k & 1), "softmax P(%d)" % k)
+            held["P"][k & 1] = k
+            if not t["first"] and rnd.random() < 0.3:  # a rescale of O
+                while not ready(("o_done", (k - 1) & 1), (k - 1) >> 1):
+                    yield
+                role_writes("O", "rescale at tile %d" % k)
+            bars[("p_full", k & 1)].arrive()
+            yield
+            if t["last"]:
+                while not ready(("o_done", k & 1), k >> 1):
+                    yield
+                role_writes("O", "epilogue of unit %d" % u)
+                bars["o_free"].arrive()
+                yield
+
+    roles = {"producer": producer(), "widening": widening(), "mma": mma(), "softmax": softmax()}
+    steps = 0
+    while roles and not errors and steps < max_steps:
+        steps += 1
+        pick = rnd.choice(list(roles) + ["async", "async"])
+        if pick == "async":  # one TMA load or MMA completes; commits whose MMAs are done arrive
+            pending = [m for m in mmas if not m["done"]] + [x for x in loads if not x[1]]
+            if pending:
+                x = rnd.choice(pending)
+                if isinstance(x, dict):
+                    x["done"] = True
+                else:
+                    x[1] = True
+                    bars[x[0]].arrive()
+            for c in list(commits):
+                if all(m["done"] for m in c[1]):
+                    commits.remove(c)
+                    bars[c[0]].arrive()
+            continue
+        try:
+            next(roles[pick])
+        except StopIteration:
+            del roles[pick]
+    if not errors and roles:
+        errors.append("roles %s never finished (deadlock)" % sorted(roles))
+    return errors
+
+
+def _cases(n, seed):
+    rnd = random.Random(seed)
+    return [[rnd.randint(1, 6) for _ in range(rnd.randint(1, 6))] for _ in range(n)]
+
+
+def test_protocol_has_no_hazard_ambiguous_wait_or_deadlock():
+    for i, units in enumerate(_cases(600, 1)):
+        errors = _run(units, seed=i)
+        assert not errors, (units, i, errors[:3])
+
+
+@pytest.mark.parametrize("units", [[1], [1, 1, 1, 1], [7], [2, 1, 3, 1, 2]])
+def test_small_unit_mixes(units):
+    for seed in range(200):
+        assert not _run(units, seed), (units, seed)
+
+
+def test_model_catches_early_v_reuse():
+    """Reusing a V tile once P.V of three tiles back is done (one tile too early for two
+    buffers) must be reported; waiting for P.V of the previous tile (one buffer's rule) is
+    slower but safe."""
+    cases = _cases(200, 2)
+    errors = [e for i, units in enumerate(cases) for e in _run(units, i, v_reuse_lag=3)]
+    assert any("ambiguous" in e or "rewrites" in e or "reads V" in e for e in errors)
+    assert not [e for i, units in enumerate(cases) for e in _run(units, i, v_reuse_lag=1)]
