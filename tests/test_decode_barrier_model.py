@@ -1,4 +1,4 @@
-"""A model of the small-step tensor-core kernel's barrier protocol for code caches (no GPU).
+"""A model of the small-step tensor-core kernel's barrier protocol (no GPU).
 
 ``mma_decode_kernel`` (csrc/gqaw_mmad.cuh) runs four roles per CTA that meet only at
 mbarriers: the TMA producer, the widening warps, the MMA issuer and the softmax warps.
@@ -13,7 +13,10 @@ With a code cache, per key tile k:
   softmax    reads S^T(k), frees it; writes P(k) into buffer k & 1 once P.V(k - 2) is
              done; may rescale O once P.V(k - 1) is done; reads O after a unit's last P.V.
 
-This model runs the four roles as coroutines under a random scheduler, with TMA loads
+With a bf16 cache there are no widening warps: S^T(k) and P.V(k) read the TMA stage of
+tile k itself, and a commit after P.V(k) frees the stage.
+
+This model runs the roles as coroutines under a random scheduler, with TMA loads
 and MMAs completing in any order and a commit arriving once every MMA issued before it
 has completed (MMAs into one accumulator run in issue order).  It checks that every
 parity wait finds its barrier exactly k or k + 1 phases along (a parity wait cannot tell
@@ -40,10 +43,11 @@ class _Bar:
             self.pending = self.count
 
 
-def _run(units, seed, v_reuse_lag=2, max_steps=400000):
+def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000):
     """Run the protocol over units of the given key-tile counts; returns the violations.
     ``v_reuse_lag``: the widening warps reuse V tile k & 1 once P.V(k - lag) is done (2 is
-    the kernel's rule)."""
+    the kernel's rule).  ``codes=False``: a bf16 cache, where S^T and P.V read the TMA
+    stage itself and a commit after P.V frees it (no widening warps)."""
     rnd = random.Random(seed)
     tiles, kc = [], 0
     for ui, nt in enumerate(units):
@@ -57,7 +61,9 @@ def _run(units, seed, v_reuse_lag=2, max_steps=400000):
             bars[(name, i)] = _Bar(1)
     bars["o_free"] = _Bar(1)
     mmas, commits, loads, errors = [], [], [], []
-    held = dict(K16=None, V16=[None, None], P=[None, None])
+    held = dict(K16=None, V16=[None, None], P=[None, None], stage=[None, None, None])
+    consumed = set()      # ("stage", k): every reader of tile k's stage is done
+    stage_reads = {}      # bf16 cache: MMAs done reading tile k's stage (S^T and P.V)
 
     def ready(name, k):
         n = bars[name].n
@@ -74,12 +80,17 @@ def _run(units, seed, v_reuse_lag=2, max_steps=400000):
         if in_use(buf):
             errors.append("%s rewrites %s while %s uses it" % (who, buf, in_use(buf)[0]["name"]))
 
-    def issue(name, reads, writes):
+    def issue(name, reads, writes, on_done=None):
         for w in writes:
             # MMAs into one accumulator run in issue order
             if [m for m in in_use(w) if not (w in m["writes"] and w not in m["reads"])]:
                 errors.append("MMA %s writes %s while it is in use" % (name, w))
-        mmas.append(dict(name=name, reads=reads, writes=writes, done=False))
+        mmas.append(dict(name=name, reads=reads, writes=writes, done=False, on_done=on_done))
+
+    def stage_read_done(k):
+        stage_reads[k] = stage_reads.get(k, 0) + 1
+        if stage_reads[k] == 2:
+            consumed.add(("stage", k))
 
     def commit(name):
         commits.append((name, [m for m in mmas if not m["done"]]))
@@ -94,6 +105,10 @@ def _run(units, seed, v_reuse_lag=2, max_steps=400000):
                 loads.append([("q_full", u & 1), False])
             while k >= 3 and not ready(("empty", k % 3), k // 3 - 1):
                 yield
+            old = held["stage"][k % 3]
+            if old is not None and ("stage", old) not in consumed:
+                errors.append("TMA of tile %d overwrites stage %d before tile %d is consumed" % (k, k % 3, old))
+            held["stage"][k % 3] = k
             loads.append([("full", k % 3), False])
             yield
 
@@ -114,6 +129,7 @@ def _run(units, seed, v_reuse_lag=2, max_steps=400000):
             role_writes(("V16", k & 1), "widening of V(%d)" % k)
             held["V16"][k & 1] = k
             bars[("vconv", k & 1)].arrive()
+            consumed.add(("stage", k))
             bars[("empty", k % 3)].arrive()
             yield
 
@@ -122,13 +138,21 @@ def _run(units, seed, v_reuse_lag=2, max_steps=400000):
             k, u = t["kc"], t["ui"]
             while t["first"] and not ready(("q_full", u & 1), u >> 1):
                 yield
-            while not ready(("kconv", k & 1), k >> 1):
+            while codes and not ready(("kconv", k & 1), k >> 1):
+                yield
+            while not codes and not ready(("full", k % 3), k // 3):
                 yield
             while k >= 2 and not ready(("s_free", k & 1), (k - 2) >> 1):
                 yield
-            if held["K16"] != k:
-                errors.append("S(%d) reads the K tile of tile %s" % (k, held["K16"]))
-            issue("S(%d)" % k, ["K16", ("Q", u & 1)], [("S", k & 1)])
+            if codes:
+                if held["K16"] != k:
+                    errors.append("S(%d) reads the K tile of tile %s" % (k, held["K16"]))
+                issue("S(%d)" % k, ["K16", ("Q", u & 1)], [("S", k & 1)])
+            else:
+                if held["stage"][k % 3] != k:
+                    errors.append("S(%d) reads stage %d holding tile %s" % (k, k % 3, held["stage"][k % 3]))
+                issue("S(%d)" % k, [("stage", k % 3), ("Q", u & 1)], [("S", k & 1)],
+                      on_done=lambda k=k: stage_read_done(k))
             commit(("s_full", k & 1))
             yield
 
@@ -141,14 +165,23 @@ def _run(units, seed, v_reuse_lag=2, max_steps=400000):
             k, u = t["kc"], t["ui"]
             while not ready(("p_full", k & 1), k >> 1):
                 yield
-            while not ready(("vconv", k & 1), k >> 1):
+            while codes and not ready(("vconv", k & 1), k >> 1):
                 yield
             while t["first"] and u >= 1 and not ready("o_free", u - 1):
                 yield
-            if held["V16"][k & 1] != k or held["P"][k & 1] != k:
-                errors.append("P.V(%d) reads V of tile %s, P of tile %s" % (k, held["V16"][k & 1], held["P"][k & 1]))
-            issue("PV(%d)" % k, [("V16", k & 1), ("P", k & 1)], ["O"])
-            commit(("o_done", k & 1))
+            if held["P"][k & 1] != k:
+                errors.append("P.V(%d) reads P of tile %s" % (k, held["P"][k & 1]))
+            if codes:
+                if held["V16"][k & 1] != k:
+                    errors.append("P.V(%d) reads V of tile %s" % (k, held["V16"][k & 1]))
+                issue("PV(%d)" % k, [("V16", k & 1), ("P", k & 1)], ["O"])
+                commit(("o_done", k & 1))
+            else:
+                if held["stage"][k % 3] != k:
+                    errors.append("P.V(%d) reads stage %d holding tile %s" % (k, k % 3, held["stage"][k % 3]))
+                issue("PV(%d)" % k, [("stage", k % 3), ("P", k & 1)], ["O"], on_done=lambda k=k: stage_read_done(k))
+                commit(("o_done", k & 1))
+                commit(("empty", k % 3))
             if t["last"]:
                 commit(("q_free", u & 1))
             yield
@@ -179,7 +212,9 @@ def _run(units, seed, v_reuse_lag=2, max_steps=400000):
                 bars["o_free"].arrive()
                 yield
 
-    roles = {"producer": producer(), "widening": widening(), "mma": mma(), "softmax": softmax()}
+    roles = {"producer": producer(), "mma": mma(), "softmax": softmax()}
+    if codes:
+        roles["widening"] = widening()
     steps = 0
     while roles and not errors and steps < max_steps:
         steps += 1
@@ -190,6 +225,8 @@ def _run(units, seed, v_reuse_lag=2, max_steps=400000):
                 x = rnd.choice(pending)
                 if isinstance(x, dict):
                     x["done"] = True
+                    if x["on_done"]:
+                        x["on_done"]()
                 else:
                     x[1] = True
                     bars[x[0]].arrive()
@@ -212,16 +249,18 @@ def _cases(n, seed):
     return [[rnd.randint(1, 6) for _ in range(rnd.randint(1, 6))] for _ in range(n)]
 
 
-def test_protocol_has_no_hazard_ambiguous_wait_or_deadlock():
+@pytest.mark.parametrize("codes", [True, False])
+def test_protocol_has_no_hazard_ambiguous_wait_or_deadlock(codes):
     for i, units in enumerate(_cases(600, 1)):
-        errors = _run(units, seed=i)
+        errors = _run(units, seed=i, codes=codes)
         assert not errors, (units, i, errors[:3])
 
 
+@pytest.mark.parametrize("codes", [True, False])
 @pytest.mark.parametrize("units", [[1], [1, 1, 1, 1], [7], [2, 1, 3, 1, 2]])
-def test_small_unit_mixes(units):
+def test_small_unit_mixes(units, codes):
     for seed in range(200):
-        assert not _run(units, seed), (units, seed)
+        assert not _run(units, seed, codes=codes), (units, seed)
 
 
 def test_model_catches_early_v_reuse():
