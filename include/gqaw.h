@@ -129,8 +129,18 @@ typedef struct gqaw_step_args {
                                     again after a device error); it holds the device
                                     status word, the list of items whose rows move, the
                                     split-K tickets and partial results.  Every completed
-                                    step leaves it ready for the next one.  Steps that
-                                    share a workspace must not overlap on the GPU. */
+                                    step leaves its counters and tickets at zero.  Where
+                                    the tickets sit depends on the step's shape (B, S,
+                                    kernel, split count): the library remembers, per
+                                    workspace address, the ticket region of the last
+                                    step enqueued on it, and a step whose region differs
+                                    first clears its own (one cudaMemsetAsync on its
+                                    stream), so one workspace serves steps of any shape
+                                    in stream order.  A CUDA graph replays only the
+                                    clears recorded while it was captured: between replays
+                                    and direct calls of another shape on one workspace,
+                                    call gqaw_workspace_init().  Steps that share a
+                                    workspace must not overlap on the GPU. */
   size_t workspace_bytes;
   int32_t *resident_len_out;     /* NULL, or (B,) int32 receiving L(T_b) */
   const float *head_sink;        /* NULL, or (Nq,) fp32: one sink logit per query head
@@ -171,7 +181,8 @@ int gqaw_rollback_exact(int64_t T, int64_t k, int64_t C, int64_t W);
  * (gqaw_last_error() says why).  Always at least 256. */
 size_t gqaw_workspace_bytes(const gqaw_step_args *args);
 
-/* Zero all `workspace_bytes` bytes of `workspace` on `stream` (cudaMemsetAsync). */
+/* Zero all `workspace_bytes` bytes of `workspace` on `stream` (cudaMemsetAsync), and
+ * note that the workspace is clean (the next step needs no ticket clear). */
 gqaw_status gqaw_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /* One whole step, enqueued on `stream` (a cudaStream_t; NULL = the legacy default
@@ -224,13 +235,17 @@ size_t gqaw_step_args_size(void);
  * library call.
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current) and zeroes its status word with cudaMemsetAsync on
+ * with that device current) and zeroes the whole array with cudaMemsetAsync on
  * `stream`; make that first call before any stream capture.  Later calls reuse the
  * address.  Every call on a device shares the one array, which keeps the previous
- * call's contents (each step overwrites every partial it reads, so nothing else needs
- * clearing); calls that overlap on the GPU (several streams at once) race on it and
- * must be ordered by the caller.  The device status word lives in the array and is not
- * reported by this entry point.
+ * call's contents.  So every call first clears, with one cudaMemsetAsync of a few KB on
+ * `stream`, the part of the array that its step needs at zero: the device status word,
+ * the cache-update counters and list, and the split-K tickets, whose place depends on
+ * the step's shape.  A call therefore never depends on what an earlier call left there,
+ * whatever its shape, even one that stopped on a device error.  The split-K partials
+ * that follow are always written before they are read.  Calls that overlap on the GPU
+ * (several streams at once) race on the array and must be ordered by the caller.  The
+ * device status word lives in the array and is not reported by this entry point.
  *
  * Returns GQAW_EWORKSPACE, before enqueuing anything, when the step needs more scratch
  * than the array holds (gqaw_workspace_bytes(args) > GQAW_NOALLOC_SCRATCH_BYTES); the

@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include <cudaTypedefs.h>
@@ -56,6 +57,61 @@ gqaw_status fail(gqaw_status s, const char *fmt, ...) {
 }
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Ticket regions of caller workspaces.  Every completed step leaves its own tickets at
+// zero, but where the tickets and the partial results sit depends on the step's shape
+// (B, S, the kernel, the split count): a step of another shape may find its tickets
+// where an earlier step left partial results, and a ticket that does not start at zero
+// never reaches its count (the unit's output is never written).  So the library keeps,
+// per workspace address, the ticket region of the last step enqueued on it, and clears
+// a step's region first (one cudaMemsetAsync on its stream) when it differs.
+struct WsRecord {
+  const void *ws;
+  size_t t0, t1;  // ticket region [t0, t1) of the last step; t1 == 0: the workspace is all zero
+};
+constexpr int kWsRecords = 64;
+std::mutex g_ws_mutex;
+WsRecord g_ws[kWsRecords] = {};
+int g_ws_next = 0;
+
+// Must the ticket region [t0, t1) of `ws` be cleared before this step?  Records it.
+// A workspace the library has no record of (never seen, or its record was evicted by
+// 64 others) is cleared to be safe.
+bool tickets_need_clear(const void *ws, size_t t0, size_t t1) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  for (WsRecord &r : g_ws)
+    if (r.ws == ws) {
+      const bool clear = r.t1 != 0 && (r.t0 != t0 || r.t1 != t1);
+      r.t0 = t0;
+      r.t1 = t1;
+      return clear;
+    }
+  g_ws[g_ws_next] = WsRecord{ws, t0, t1};
+  g_ws_next = (g_ws_next + 1) % kWsRecords;
+  return true;
+}
+
+// The workspace [ws, ws + bytes) has just been zeroed: its record says so, and records
+// of workspaces inside it are dropped.
+void note_zeroed(const void *ws, size_t bytes) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  const char *lo = static_cast<const char *>(ws), *hi = lo + bytes;
+  bool found = false;
+  for (WsRecord &r : g_ws) {
+    const char *p = static_cast<const char *>(r.ws);
+    if (r.ws == ws) {
+      r.t0 = r.t1 = 0;
+      found = true;
+    } else if (p && p >= lo && p < hi) {
+      r = WsRecord{nullptr, 0, 0};
+    }
+  }
+  if (!found) {
+    g_ws[g_ws_next] = WsRecord{ws, 0, 0};
+    g_ws_next = (g_ws_next + 1) % kWsRecords;
+  }
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Launch {
@@ -165,7 +221,8 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   // Workspace: [0, 256) status word and the two counters of the cache-update list;
   // the list itself (B items); per-unit tickets; two partial-result slots per
   // attention CTA.  Everything must start at zero (gqaw_workspace_init); every step
-  // leaves the counters and tickets at zero again.
+  // leaves the counters and tickets at zero again, and a step whose tickets sit
+  // elsewhere than the previous step's clears them first (tickets_need_clear).
   L->off_list = 256;
   L->off_tickets = L->off_list + align256((size_t)a->batch_size * 4);
   L->off_partials = L->off_tickets + align256((size_t)L->units * 4);
@@ -515,6 +572,16 @@ gqaw_status run_attend(const gqaw_step_args *a, const Launch &L, const gqaw::Par
   return GQAW_OK;
 }
 
+// Clears the step's ticket region when the workspace last served a step of another
+// layout (see tickets_need_clear).
+gqaw_status clear_tickets_if_needed(const gqaw_step_args *a, const Launch &L, cudaStream_t st) {
+  if (!tickets_need_clear(a->workspace, L.off_tickets, L.off_partials)) return GQAW_OK;
+  const cudaError_t e =
+      cudaMemsetAsync(static_cast<char *>(a->workspace) + L.off_tickets, 0, L.off_partials - L.off_tickets, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (ticket region)");
+  return GQAW_OK;
+}
+
 gqaw_status run_finish(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
   const cudaError_t e = gqaw::launch_finish(p, (int)L.ncopy, st);
   if (e != cudaSuccess) return cuda_fail(e, "finish kernel launch");
@@ -527,6 +594,18 @@ gqaw_status run_finish(const gqaw_step_args *a, const Launch &L, const gqaw::Par
 namespace gqaw {
 // Lets other translation units of the library report an error through gqaw_last_error().
 void set_error(const char *msg) { t_error = msg; }
+
+// Bytes at the start of a step's workspace that must be zero when the step starts (the
+// status word, the cache-update counters and list, the tickets); 0 if the sizes are
+// invalid.
+size_t workspace_counter_bytes(const gqaw_step_args *args) {
+  Launch L;
+  if (plan_launch(args, &L) != GQAW_OK) return 0;
+  return L.off_partials;
+}
+
+// A workspace was zeroed by other means than gqaw_workspace_init (see note_zeroed).
+void workspace_zeroed(const void *ws, size_t bytes) { note_zeroed(ws, bytes); }
 }  // namespace gqaw
 
 extern "C" {
@@ -557,6 +636,7 @@ gqaw_status gqaw_workspace_init(void *workspace, size_t workspace_bytes, void *s
   if (workspace_bytes < 256) return fail(GQAW_EWORKSPACE, "workspace_bytes %zu < 256", workspace_bytes);
   const cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  note_zeroed(workspace, workspace_bytes);
   return GQAW_OK;
 }
 
@@ -566,6 +646,8 @@ gqaw_status gqa_windowed_step(const gqaw_step_args *args, void *stream) {
   gqaw_status s = prepare(args, &L, &p);
   if (s != GQAW_OK || args->batch_size == 0) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = clear_tickets_if_needed(args, L, st);
+  if (s != GQAW_OK) return s;
   s = run_attend(args, L, p, st);
   if (s != GQAW_OK) return s;
   return run_finish(args, L, p, st);
@@ -576,6 +658,8 @@ gqaw_status gqaw_attend(const gqaw_step_args *args, void *stream) {
   gqaw::Params p;
   gqaw_status s = prepare(args, &L, &p);
   if (s != GQAW_OK || args->batch_size == 0) return s;
+  s = clear_tickets_if_needed(args, L, static_cast<cudaStream_t>(stream));
+  if (s != GQAW_OK) return s;
   return run_attend(args, L, p, static_cast<cudaStream_t>(stream));
 }
 

@@ -12,6 +12,13 @@
 // name g_scratch is only a host-side stand-in, never a device address; the device
 // address is looked up once per device with cudaGetSymbolAddress (with that device
 // current) and cached.
+//
+// Every call shares the array and finds there what the previous call left.  Where a
+// step keeps its counters and tickets depends on its shape, and a step that stopped on
+// a device error may leave them non-zero; so each call first clears the part of the
+// array that a step needs at zero (status word, counters, list, tickets: a few KB, one
+// cudaMemsetAsync on the call's stream).  The partial results that follow are always
+// written before they are read.
 #include <cstdio>
 #include <mutex>
 
@@ -19,6 +26,8 @@
 
 namespace gqaw {
 void set_error(const char *msg);
+size_t workspace_counter_bytes(const gqaw_step_args *args);
+void workspace_zeroed(const void *ws, size_t bytes);
 }
 
 namespace {
@@ -30,8 +39,7 @@ std::mutex g_mutex;
 void *g_scratch_dev[kMaxDevices] = {nullptr};
 
 // Device address of g_scratch on the current device; the first call for a device
-// looks it up and zeroes the whole array (on `stream`): the step's counters and
-// tickets must start at zero, and every step leaves them at zero again.
+// looks it up (with that device current) and zeroes the whole array on `stream`.
 gqaw_status scratch_for_current_device(void **out, cudaStream_t stream) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -84,6 +92,14 @@ extern "C" gqaw_status gqa_windowed_step_noalloc(const gqaw_step_args *args, voi
   void *scratch = nullptr;
   const gqaw_status s = scratch_for_current_device(&scratch, static_cast<cudaStream_t>(stream));
   if (s != GQAW_OK) return s;
+  // status word, counters, list and tickets of this step's layout start at zero
+  const size_t counters = gqaw::workspace_counter_bytes(args);
+  const cudaError_t e = cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    gqaw::set_error(cudaGetErrorString(e));
+    return GQAW_ECUDA;
+  }
+  gqaw::workspace_zeroed(scratch, counters);
   gqaw_step_args a = *args;  // the caller's workspace fields are ignored
   a.workspace = scratch;
   a.workspace_bytes = GQAW_NOALLOC_SCRATCH_BYTES;

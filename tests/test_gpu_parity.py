@@ -361,6 +361,48 @@ def test_phases_equal_one_call():
         T = T + 1
 
 
+def test_workspace_reused_across_shapes():
+    """One workspace, sized for the largest step, serves steps of different shapes on
+    one cache (single-token steps and 32-token chunks, forced key splits): a chunk's
+    tickets lie where the single-token step before it left partial results, and the
+    library clears them when the layout changes.  Checked against the oracle."""
+    from sliding_window_gqa_02_gb300 import gqaw
+
+    sh = wl.SHAPES["pages"]
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream().cuda_stream
+    pk, pv = wl.cache(sh, 25, B=1)
+    o = OracleCache(1, sh.Nq, sh.Nkv, sh.D, sh.C, sh.W, oracle.F32, past_key=wl.to_numpy(pk),
+                    past_value=wl.to_numpy(pv))
+    gk, gv = pk.to(dev), pv.to(dev)
+    T, shapes = 300, [1, 32, 1, 32, 32, 1]
+    need = 0
+    for S in shapes:  # the workspace is sized for the largest of the steps
+        q0 = torch.empty((1, S, sh.Nq * sh.D), device=dev)
+        a = gqaw.make_args(q0, q0[..., :sh.Nkv * sh.D], q0[..., :sh.Nkv * sh.D], gk, gv, gk, gv,
+                           torch.zeros(1, dtype=torch.int32, device=dev), 2000, sh.Nq, sh.Nkv, sh.W, q0,
+                           split_keys=32)
+        need = max(need, gqaw.gqaw_workspace_bytes(a))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    gqaw.check(gqaw.gqaw_workspace_init(int(ws.data_ptr()), need, stream))
+    for c, S in enumerate(shapes):
+        q, k, v = wl.step_inputs(sh, S, 2500 + c, B=1)
+        dq, dk, dv = (x.to(dev) for x in (q, k, v))
+        seq = torch.tensor([T + S - 1], dtype=torch.int32, device=dev)
+        out = torch.full_like(dq, float("nan"))
+        res = torch.full((1,), -1, dtype=torch.int32, device=dev)
+        a = gqaw.make_args(dq, dk, dv, gk, gv, gk, gv, seq, T + S, sh.Nq, sh.Nkv, sh.W, out, workspace=ws,
+                           resident_len_out=res, split_keys=32)
+        gqaw.check(gqaw.gqa_windowed_step(a, stream))
+        torch.cuda.synchronize()
+        st, flags = gqaw.gqaw_device_status(int(ws.data_ptr()), stream=stream)
+        ro = o.step(wl.to_numpy(q), wl.to_numpy(k), wl.to_numpy(v), np.array([T + S - 1], np.int32))
+        rg = {"output": out.cpu(), "resident_len": res.cpu().numpy(), "present_key": wl.to_numpy(gk.cpu()),
+              "present_value": wl.to_numpy(gv.cpu()), "device_flags": flags}
+        compare(rg, ro, sh.dtype)
+        T += S
+
+
 def test_bias_broadcast_strides():
     """Bias shapes (1, Nq, S, total) and (B, 1, S, total): stride 0 broadcasts."""
     sh = wl.Shape("b", B=3, Nq=8, Nkv=2, D=64, W=16, C=20, dtype=wl.BF16, softcap=5.0)

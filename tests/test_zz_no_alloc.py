@@ -79,6 +79,42 @@ def test_noalloc_matches_step_multi_token():
     _pair_run(wl.SHAPES["pages"], 1, 4, 500, 500, seed=23)
 
 
+def test_noalloc_alternating_shapes():
+    """Calls of different shapes in a row on one cache: single-token steps and 32-token
+    chunks, with forced key splits so every call uses split-K tickets and partials.  A
+    chunk's tickets lie where the single-token call before it left partial results (fp32
+    pages shape: 8 units then 256), so each call must clear its own ticket region; the
+    reference side gets a fresh workspace for every call."""
+    from sliding_window_gqa_02_gb300 import gqaw
+
+    sh = wl.SHAPES["pages"]
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream().cuda_stream
+    pk, pv = wl.cache(sh, 24, B=1)
+    ka, va = pk.to(dev), pv.to(dev)
+    kb, vb = pk.to(dev), pv.to(dev)
+    T = 300
+    for c, S in enumerate([1, 32, 1, 32, 32, 1]):
+        q, k, v = (x.to(dev) for x in wl.step_inputs(sh, S, 2400 + c, B=1))
+        seq = torch.tensor([T + S - 1], dtype=torch.int32, device=dev)
+        oa, ob = torch.empty_like(q), torch.full_like(q, float("nan"))
+        kw = dict(split_keys=32)
+        a = gqaw.make_args(q, k, v, ka, va, ka, va, seq, T + S, sh.Nq, sh.Nkv, sh.W, oa, **kw)
+        ws = gqaw.new_workspace(a, dev, stream)
+        a = gqaw.make_args(q, k, v, ka, va, ka, va, seq, T + S, sh.Nq, sh.Nkv, sh.W, oa, workspace=ws, **kw)
+        b = gqaw.make_args(q, k, v, kb, vb, kb, vb, seq, T + S, sh.Nq, sh.Nkv, sh.W, ob, **kw)
+        gqaw.check(gqaw.gqa_windowed_step(a, stream))
+        gqaw.check(gqaw.gqa_windowed_step_noalloc(b, stream))
+        torch.cuda.synchronize()
+        ref = oa.float()
+        assert torch.isfinite(ob.float()).all(), "call %d (S=%d): rows left unwritten" % (c, S)
+        err = (ob.float() - ref).abs().max().item() / ref.abs().max().item()
+        assert err <= TOL[sh.dtype], (c, S, err)
+        n = gqaw.gqaw_resident_len(T + S, sh.C, sh.W)
+        assert torch.equal(ka[0, :, :n], kb[0, :, :n]) and torch.equal(va[0, :, :n], vb[0, :, :n])
+        T += S
+
+
 def test_noalloc_rejects_steps_needing_more_scratch():
     """A step whose split-K scratch exceeds the static array is refused on the host."""
     from sliding_window_gqa_02_gb300 import gqaw
