@@ -203,7 +203,8 @@ KERNELS = {
     "mmad": ("mma_decode_kernel (tcgen05)",
              ("gqaw_mmad.cuh", "gqaw_mmad.cu", "gqaw_mmad_q8.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
     "mma": ("mma_attend_kernel (tcgen05)", ("gqaw_mma.cu", "gqaw_tc.cuh", "gqaw_internal.cuh")),
-    "attend": ("attend_kernel", ("gqaw_attend.cuh", "gqaw_internal.cuh", "gqaw_attend_bf16.cu", "gqaw_attend_f32.cu")),
+    "attend": ("attend_kernel", ("gqaw_attend.cuh", "gqaw_internal.cuh", "gqaw_attend_launch.cuh",
+                                 "gqaw_attend_bf16.cu", "gqaw_attend_f32.cu")),
 }
 
 

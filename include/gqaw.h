@@ -91,6 +91,10 @@ typedef enum gqaw_dtype {
 #define GQAW_DEV_BAD_SEQLEN 1u /* some seqlens_k[b] + 1 - S < 0 or > total_sequence_length */
 #define GQAW_DEV_TIMEOUT 2u    /* a bounded in-kernel wait expired (an internal fault) */
 #define GQAW_DEV_BAD_POSITION 4u /* a rotary position outside [0, rotary_cache_len) */
+#define GQAW_DEV_QUERY_RANGE 8u  /* quantized cache on the tensor-core small-step path
+                                    (head_size 128, S x group <= 32): a finite query
+                                    element of magnitude >= 65520, which has no finite
+                                    fp16 value; the output is then unspecified */
 
 /* Arguments of one step.  All tensor pointers are DEVICE pointers.  Layouts are
  * row-major with the shapes given; "BNSH" is (batch, kv head, row, head_size).
@@ -148,7 +152,13 @@ typedef struct gqaw_step_args {
   int32_t smooth_softmax;        /* non-zero: a sink logit of 0 for every head ([P3]
                                     Part 1.3); ignored when head_sink is given */
   int32_t do_rotary;             /* non-zero: turn the new query and key rows by the
-                                    rotary embedding before use ([P3] Part 1.3) */
+                                    rotary embedding before use ([P3] Part 1.3).  The
+                                    turn is computed in fp32 and rounded once to the
+                                    cache dtype (or its code), so the stored key rows
+                                    may differ by one rounding step from a turn in
+                                    higher precision: present keys are bit-exact copies
+                                    of the step's inputs only without do_rotary (values
+                                    always are) */
   int32_t rotary_interleaved;    /* non-zero: pairs (2i, 2i+1); 0: pairs (i, i + rd/2) */
   int32_t rotary_dim;            /* rd: even, 2 <= rd <= D; 0 means D.  Dimensions from
                                     rd on are not turned */
@@ -161,7 +171,12 @@ typedef struct gqaw_step_args {
   int32_t cache_dtype;           /* 0: the caches hold `dtype`; GQAW_I8 or GQAW_E4M3: they
                                     hold 1-byte codes of a quantized cache ([P3] Part 1.1,
                                     k_scale and v_scale); needs dtype GQAW_BF16 and
-                                    head_size 64, 128 or 256 */
+                                    head_size 64, 128 or 256.  With head_size 128 and
+                                    S x group <= 32 the tensor cores take the query as
+                                    fp16: elements must stay below 65520 in magnitude
+                                    (else GQAW_DEV_QUERY_RANGE), and those below fp16's
+                                    normal range (6.1e-5) keep its subnormal spacing
+                                    (6e-8) */
   const float *k_scale;          /* quantized cache: device fp32 scalar, > 0; a key code c
                                     stands for c * k_scale.  Otherwise ignored */
   const float *v_scale;          /* quantized cache: the same for values */

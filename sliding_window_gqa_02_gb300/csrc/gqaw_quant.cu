@@ -32,7 +32,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const Params p)
   const long long n8 = (long long)p.B * p.S * p.Nkv * p.D / 8;  // 8-element groups per tensor
   const long long nq8 = p.q16 ? (long long)p.B * p.S * p.Nq * p.D / 8 : 0;
   const float sk = *p.ks, sv = *p.vs;
-  // the fp16 copy of the query (the tensor-core kernel's operand), when asked for
+  // the fp16 copy of the query (the tensor-core kernel's operand), when asked for.  A
+  // finite bfloat16 element at or beyond 65520 in magnitude has no finite fp16 value:
+  // flagged (GQAW_DEV_QUERY_RANGE), the item's output is then unspecified.
+  bool out_of_range = false;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < nq8;
        idx += (long long)gridDim.x * blockDim.x) {
     float f[8];
@@ -41,10 +44,13 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const Params p)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      const float2 back = __half22float2(h);
+      out_of_range |= (isinf(back.x) && !isinf(f[2 * i])) || (isinf(back.y) && !isinf(f[2 * i + 1]));
       w[i] = *reinterpret_cast<const uint32_t *>(&h);
     }
     static_cast<uint4 *>(p.q16)[idx] = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  if (out_of_range) flag(p, GQAW_DEV_QUERY_RANGE);
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < 2 * n8;
        idx += (long long)gridDim.x * blockDim.x) {
     const bool val = idx >= n8;

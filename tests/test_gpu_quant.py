@@ -111,3 +111,22 @@ def test_long_context_decode_sampled():
         q, k, v = wl.step_inputs(sh, 1, 5400 + t)
         p.step(q, k, v, T)
         T = T + 1
+
+
+@pytest.mark.parametrize("big,flagged", [(65280.0, False), (99840.0, True)])
+def test_query_beyond_fp16_range_flagged(big, flagged):
+    """On the tensor-core small-step path the query of a quantized cache becomes fp16: a
+    finite bfloat16 element with no finite fp16 value (99840) sets GQAW_DEV_QUERY_RANGE;
+    the largest bfloat16 below fp16's limit (65280) does not."""
+    from gpu_driver import GpuCache
+    from sliding_window_gqa_02_gb300 import gqaw
+
+    sh = wl.Shape("q8f", B=2, Nq=8, Nkv=2, D=128, W=200, C=210, dtype=wl.BF16)
+    pk, pv = wl.code_cache(sh, 56, "e4m3")
+    ks, vs = SCALES["e4m3"]
+    g = GpuCache(sh.B, sh.Nq, sh.Nkv, sh.D, sh.C, sh.W, sh.dtype, past_key=pk, past_value=pv, cache_dtype="e4m3",
+                 k_scale=ks, v_scale=vs)
+    q, k, v = wl.step_inputs(sh, 1, 5600)
+    q[1, 0, 5] = big
+    rg = g.step(q, k, v, np.array([150, 160], np.int64))
+    assert bool(rg["device_flags"] & gqaw.GQAW_DEV_QUERY_RANGE) == flagged
