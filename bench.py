@@ -91,8 +91,11 @@ def resident_len(T, C, W):
 
 
 def algorithmic_bytes(sh, S, T_before, B, cache_bytes=None):
-    """Bytes the step must move (in-window cache rows + new rows read, append written,
-    compaction read + written, Q in, output out), per item, from the pre-step lengths.
+    """Bytes the step must move, per item from the pre-step lengths: the in-window cache
+    rows and the new rows read, the appended rows written, the surviving rows of a
+    reclaimed block written at their new place (and read too where they lie below the
+    window the attention reads: a surviving row inside the window is read once, for both
+    uses), the query read and the output written.  Returns (attention bytes, step bytes).
     ``cache_bytes``: bytes of a cache element (1 for a quantized cache).  Bias bytes are
     added by the caller."""
     e = 2 if sh.dtype == "bf16" else 4
@@ -104,10 +107,11 @@ def algorithmic_bytes(sh, S, T_before, B, cache_bytes=None):
         Lp, Lt = resident_len(P, sh.C, sh.W), resident_len(T, sh.C, sh.W)
         kept = Lt - S
         seed = Lp + S - Lt
-        attn += row * (min(P, sh.W - 1) + S)
+        nwin = min(P, sh.W - 1)
+        attn += row * (nwin + S)
         app += row * min(S, Lt)
         if seed > 0 and kept > 0:
-            comp += row * 2 * kept
+            comp += row * (kept + max(kept - nwin, 0))
     qo = B * S * sh.Nq * sh.D * e * 2
     return attn + qo, attn + app + comp + qo
 

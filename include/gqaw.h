@@ -95,6 +95,8 @@ typedef enum gqaw_dtype {
                                     (head_size 128, S x group <= 32): a finite query
                                     element of magnitude >= 65520, which has no finite
                                     fp16 value; the output is then unspecified */
+#define GQAW_DEV_INTERNAL 16u    /* an internal consistency check failed (a library
+                                    fault): the step's results are unspecified */
 
 /* Arguments of one step.  All tensor pointers are DEVICE pointers.  Layouts are
  * row-major with the shapes given; "BNSH" is (batch, kv head, row, head_size).

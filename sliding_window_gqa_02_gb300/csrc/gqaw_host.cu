@@ -120,6 +120,7 @@ struct Launch {
   int quant;              // cache_dtype of a quantized cache, or 0
   size_t off_kq, off_vq;  // quantized cache: the codes of the step's new rows
   size_t off_q16;         // quantized cache on the tensor-core kernel: the fp16 query copy
+  size_t off_stash;       // small-step kernel, bf16 caches: one row stash per CTA
   long long units, ctas, ncopy;
   size_t off_list, off_tickets, off_partials, ws_bytes;
   int rot_dim;            // > 0: the rotary embedding is on, over this many dimensions
@@ -283,8 +284,14 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     L->off_tickets = L->off_list + align256((size_t)a->batch_size * 4);
     L->off_partials = L->off_tickets + align256((size_t)L->tda.units * 4);
     L->ws_bytes = L->off_partials + align256((size_t)ctas * 2 * L->tda.npad * (128 + 2) * 4);
+    L->off_stash = 0;
+    if (!L->quant) {  // rows a CTA moves inside the attention pass for a later writer
+      L->off_stash = L->ws_bytes;
+      L->ws_bytes += align256((size_t)ctas * gqaw::kMoveStashBytes);
+    }
   }
   // Rotary embedding: the turned query and key rows, in the input layouts.
+  if (!L->td) L->off_stash = 0;
   L->off_qrot = L->off_krot = 0;
   if (L->rot_dim > 0) {
     const size_t tokens = (size_t)a->batch_size * a->sequence_length;
@@ -382,6 +389,19 @@ gqaw_status check_pointers(const gqaw_step_args *a, const Launch &L) {
   return GQAW_OK;
 }
 
+// Can the step leave out the cache-update kernel?  On the small-step kernel with a bf16
+// cache updated in place, S <= G = C - W + 1 means a step reclaims at most one G-row
+// block (seed = 0 or G); with S <= W and G <= the rows a CTA may stash, the surviving
+// rows of a reclaiming item all lie in the window the step reads and the attention
+// kernel moves them itself (kFused in gqaw_mmad.cuh), while a non-reclaiming item only
+// appends.  So no item is ever recorded for the cache-update kernel.
+bool finish_not_needed(const gqaw_step_args *a, const Launch &L) {
+  const long long G = (long long)a->capacity - a->local_window_size + 1;
+  return L.td && !L.quant && a->past_key == a->present_key && a->past_value == a->present_value &&
+         a->sequence_length <= G && a->sequence_length <= a->local_window_size &&
+         G <= gqaw::kMoveStashRows;
+}
+
 void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
   std::memset(p, 0, sizeof(*p));
   p->q = a->query;
@@ -454,6 +474,8 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
     p->vs = a->v_scale;
     p->q16 = L.td ? ws + L.off_q16 : nullptr;
   }
+  p->stash = L.off_stash ? reinterpret_cast<unsigned char *>(ws + L.off_stash) : nullptr;
+  p->no_finish = finish_not_needed(a, L) ? 1 : 0;
 }
 
 gqaw_status prepare(const gqaw_step_args *a, Launch *L, gqaw::Params *p) {
@@ -534,12 +556,18 @@ gqaw_status run_mmad(const gqaw_step_args *a, const Launch &L, const gqaw::Param
   // quantized cache: 128 one-byte codes per row, one 128 x 128 box per tile; fp16 query
   const cuuint64_t c8_str[1] = {D};
   const cuuint32_t c8_box[2] = {128, 128};
+  // bf16 caches: 8-row boxes for the stores of rows moved inside the attention pass
+  const cuuint32_t r8_box[2] = {64, 8};
   const bool q8 = L.quant != 0;
   const CUtensorMapDataType qt = q8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapDataType ct = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  std::memset(&maps.kc8, 0, sizeof(maps.kc8));
+  std::memset(&maps.vc8, 0, sizeof(maps.vc8));
   if (!encode_map(&maps.q, q8 ? p.q16 : p.q, 3, q_dims, q_str, q_box, qt) ||
       !encode_map(&maps.kc, a->past_key, 2, c_dims, q8 ? c8_str : c_str, q8 ? c8_box : c_box, ct) ||
-      !encode_map(&maps.vc, a->past_value, 2, c_dims, q8 ? c8_str : c_str, q8 ? c8_box : c_box, ct))
+      !encode_map(&maps.vc, a->past_value, 2, c_dims, q8 ? c8_str : c_str, q8 ? c8_box : c_box, ct) ||
+      (!q8 && (!encode_map(&maps.kc8, a->past_key, 2, c_dims, c_str, r8_box, ct) ||
+               !encode_map(&maps.vc8, a->past_value, 2, c_dims, c_str, r8_box, ct))))
     return fail(GQAW_ECUDA, "cuTensorMapEncodeTiled failed for the small-step kernel");
   const cudaError_t e = gqaw::launch_mmad(p, L.tda, maps, (int)L.td_ctas, st);
   if (e != cudaSuccess) return cuda_fail(e, "small-step tensor-core kernel launch");
@@ -650,6 +678,7 @@ gqaw_status gqa_windowed_step(const gqaw_step_args *args, void *stream) {
   if (s != GQAW_OK) return s;
   s = run_attend(args, L, p, st);
   if (s != GQAW_OK) return s;
+  if (p.no_finish) return GQAW_OK;  // the attention kernel did the whole cache update
   return run_finish(args, L, p, st);
 }
 

@@ -58,6 +58,10 @@ struct Params {
   const void *kq_in, *vq_in;
   const float *ks, *vs;
   void *q16;                 // NULL, or an fp16 copy of the query rows for the tensor-core kernel
+  // small-step kernel, bf16 caches: the rows a CTA moves whose destination another CTA
+  // may still read, written later by the unit's last contributor (kMoveStashBytes per CTA)
+  unsigned char *stash;
+  int no_finish;             // the host launches no cache-update kernel for this step
 };
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -68,7 +68,10 @@ constexpr int kK16 = kStages * kCodeStage;  // quantized cache: the widened K ti
 constexpr int kV16 = kK16 + 2 * kHalf;      // quantized cache: two widened V tiles (fp16, 32 KB each)
 constexpr float kRescale = 8.0f;           // lazy rescale threshold (log2 units)
 constexpr int kBar = 1;                    // named barrier of the softmax warps
-constexpr int kNumBars = 24;
+constexpr int kNumBars = 25;
+constexpr int kRow = kD * 2;               // bytes of a bf16 cache row
+static_assert(kMoveStashRows <= kKeys, "a stash lies within a CTA's first tile");
+static_assert(kMoveStashBytes == kMoveStashRows * 2 * kRow, "a stash holds K and V rows of head size 128");
 static_assert(kV16 + 4 * kHalf == kStages * kStageBytes, "both layouts put Q at the same offset");
 
 template <int NPAD>
@@ -260,6 +263,43 @@ __device__ __forceinline__ DUnit dunit(const Params &p, long long u) {
   return x;
 }
 
+// What the kernel does with the rows of a unit's item (the same for each of its kv heads).
+//  kAppend:   in place, no block reclaimed: the new rows go to [L(P), L(P) + S), which no
+//             query reads, appended by the CTA holding the unit's last tile first thing.
+//  kFused:    in place, a block of seed <= kMoveStashRows rows reclaimed, every surviving
+//             row [seed, L(P)) inside the window the step reads, bf16 cache: the mover
+//             warps write the surviving rows from the staged tiles to [0, kept), and the
+//             CTA holding the unit's last tile appends the new rows at [kept, L(T)) after
+//             its tiles (block compaction and append of PR #31142 "[CPU] Add windowed kv
+//             cache for GQA", "Drifting layout", done inside the attention pass).
+//  kRegister: anything else (a separate present buffer, surviving rows below the window,
+//             a larger block, a code cache): the item is recorded for the cache-update
+//             kernel.
+enum { kAppend = 0, kFused = 1, kRegister = 2 };
+struct DMove {
+  int kind;
+  long long seed, kept;  // rows reclaimed; rows surviving (the new rows follow them)
+  long long lo_row;      // slice row of the window's first key (key position x.lo)
+  long long nwin;        // keys of the window held in the cache: rows [lo_row, L(P))
+};
+
+template <int QT>
+__device__ __forceinline__ DMove dmove(const Params &p, const DUnit &x) {
+  DMove m;
+  m.seed = x.pl.Lp + p.S - x.pl.Lt;
+  m.kept = x.pl.Lt - p.S;
+  m.nwin = x.pl.P - x.lo;
+  m.lo_row = x.pl.Lp - m.nwin;
+  const bool inplace = p.pk == p.prk && p.pv == p.prv;
+  if (inplace && m.seed == 0)
+    m.kind = kAppend;
+  else if (QT == 0 && inplace && m.kept >= 0 && m.kept <= m.nwin && m.seed <= kMoveStashRows)
+    m.kind = kFused;
+  else
+    m.kind = kRegister;
+  return m;
+}
+
 // The CTA whose range holds virtual tile x (CTA c covers [c*V/G, (c+1)*V/G)).
 __device__ __forceinline__ long long owner_cta(long long x, long long V, long long G) {
   return ((x + 1) * G - 1) / V;
@@ -312,13 +352,14 @@ struct Walker {
 // keys, the same head dimensions) and own different query rows, NC = NVT / CG each.
 // QT: 0 for bf16 caches, GQAW_I8 or GQAW_E4M3 for the codes of a quantized cache.
 // Warps: 4 * CG softmax warps, WW widening warps (quantized cache only), the TMA producer
-// warp, the MMA issuer warp.
+// warp, the MMA issuer warp, and for bf16 caches the mover warp.
 template <int CG, int QT>
 struct Warps {
   static_assert(QT == 0 || CG <= 2, "code caches: at most two column groups");
   static constexpr int kWiden = QT == 0 ? 0 : (CG == 1 ? 4 : 2);
   static constexpr int kProducer = 4 * CG + kWiden;
-  static constexpr int kThreads = 32 * (kProducer + 2);
+  static constexpr int kMover = QT == 0 ? 1 : 0;  // bf16 caches: the warp that moves rows
+  static constexpr int kThreads = 32 * (kProducer + 2 + kMover);
 };
 
 template <int NPAD, int NVT, int CG, int QT>
@@ -348,6 +389,10 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
   // quantized cache: widened K tile ready, widened V tile [2] ready (both per tile parity:
   // a parity wait cannot tell apart two phases of one barrier)
   uint64_t *kconv_full = bars + 20, *vconv_full = bars + 22;
+  // bf16 caches: the mover warp has written this CTA's stash (rows of its first unit whose
+  // destination lies in the previous CTA's range); the softmax warps wait for it before
+  // the unit's ticket
+  uint64_t *stash_bar = bars + 24;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kSlot);
   __shared__ int s_abort, s_last;
 
@@ -360,8 +405,11 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kQ8 ? 32 * kWidenW : 1);  // codes: free once widened
+      // codes: free once widened; bf16: once the P.V that reads V has completed and the
+      // mover warp is done with the tile
+      mbar_init(&empty[i], kQ8 ? 32 * kWidenW : 2);
     }
+    if constexpr (!kQ8) mbar_init(stash_bar, 1);
     if constexpr (kQ8) {  // the widening warps' barriers (counts are at least 1)
       for (int i = 0; i < 2; ++i) {
         mbar_init(&kconv_full[i], 32 * kWidenW);
@@ -513,6 +561,86 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       tc::mma_commit(mma_done);  // every MMA issued has completed before TMEM is released
       if (!mbar_wait(mma_done, 0)) flag(p, GQAW_DEV_TIMEOUT);
     }
+  } else if (!kQ8 && warp == kProducer + 2) {
+    // ------------------------------------------------------------ mover (bf16 caches)
+    // For each staged tile of a fused unit, the tile's surviving rows go to their
+    // compacted rows (destination = source row - seed): 8-row-aligned runs by tensor TMA
+    // stores straight from the swizzled tile, ragged rows by the lanes (one 16-byte part of
+    // a row each).  A destination in this CTA's own range was read by this CTA in an
+    // earlier or the same tile, and one below the window is read by nobody; the rows whose
+    // destination lies in the previous CTA's range -- the first min(seed, rows) rows of a
+    // range that starts inside a unit -- go to this CTA's stash instead, for the unit's
+    // last contributor.  The stage is released once the stores have read it.
+    Walker w{ufirst - 1, ulast, tb, te, TPU, 0, 0, 0, -1, DUnit()};
+    DTile t;
+    DMove mv{};
+    bool fine = true;
+    const int tensor = lane >> 4, half = (lane >> 3) & 1, chunk = lane & 7;  // this lane's part of a row
+    while (fine && !*reinterpret_cast<volatile int *>(&s_abort) && w.next(p, t)) {
+      const int kc = t.kc, st = kc % kStages;
+      if (!mbar_wait(&full[st], (kc / kStages) & 1)) {
+        fine = false;
+        break;
+      }
+      if (t.first) mv = dmove<QT>(p, t.x);
+      if (mv.kind == kFused) {
+        tc::fence_proxy_async_smem();  // the landed tile, as this thread saw it, to the stores
+        const unsigned char *sb = stage(kc);
+        const long long r0 = mv.lo_row + (long long)t.lt * kKeys;  // slice row of tile row 0
+        const int nvalid = (int)(mv.nwin - (long long)t.lt * kKeys < kKeys ? mv.nwin - (long long)t.lt * kKeys : kKeys);
+        const int tA = (int)(mv.seed - r0 > 0 ? mv.seed - r0 : 0);  // rows below tA are reclaimed
+        const bool stash = t.first && t.lt > 0;                    // the range starts inside the unit
+        const int nst = stash ? (int)(mv.seed < nvalid ? mv.seed : nvalid) : 0;
+        const long long grow0 = ((long long)t.x.b * p.Nkv + t.x.kvh) * p.C + r0 - mv.seed;
+        auto part = [&](int r) {  // this lane's 16 bytes of tile row r (128-byte swizzle)
+          return *reinterpret_cast<const uint4 *>(sb + tensor * 2 * kHalf + half * kHalf + r * 128 +
+                                                  ((chunk ^ (r & 7)) << 4));
+        };
+        if (stash) {
+          unsigned char *dst = p.stash + (size_t)cta * kMoveStashBytes;
+          for (int r = tA; r < nst; ++r)
+            *reinterpret_cast<uint4 *>(dst + (size_t)r * 2 * kRow + tensor * kRow + half * 128 + chunk * 16) = part(r);
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(stash_bar);
+        }
+        const int lo = tA > nst ? tA : nst, hi = nvalid;
+        if (hi > lo) {
+          unsigned char *gb = static_cast<unsigned char *>(tensor ? p.prv : p.prk);
+          auto ragged = [&](int r) {
+            *reinterpret_cast<uint4 *>(gb + (size_t)(grow0 + r) * kRow + half * 128 + chunk * 16) = part(r);
+          };
+          if (lo == 0 && hi == kKeys) {  // the whole tile: one 128-row box per half of K and V
+            if (lane < 4)
+              tc::tma_store_2d((lane >> 1) ? &maps.vc : &maps.kc, (lane & 1) * 64, (int)grow0,
+                               sb + (lane >> 1) * 2 * kHalf + (lane & 1) * kHalf);
+          } else {
+            const int c0 = (lo + 7) & ~7, c1 = hi & ~7;  // 8-row-aligned run [c0, c1)
+            if (c1 > c0) {
+              for (int i = lane; i < (c1 - c0) / 2; i += 32) {  // (c1 - c0) / 8 boxes x 4 halves
+                const int rr = c0 + (i >> 2) * 8, tn = (i >> 1) & 1, hf = i & 1;
+                tc::tma_store_2d(tn ? &maps.vc8 : &maps.kc8, hf * 64, (int)(grow0 + rr),
+                                 sb + tn * 2 * kHalf + hf * kHalf + rr * 128);
+              }
+              for (int r = lo; r < c0; ++r) ragged(r);
+              for (int r = c1; r < hi; ++r) ragged(r);
+            } else {
+              for (int r = lo; r < hi; ++r) ragged(r);
+            }
+          }
+          tc::bulk_commit();
+          tc::bulk_wait_read();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    if (!fine) {
+      flag(p, GQAW_DEV_TIMEOUT);
+      s_abort = 1;
+    }
+    tc::bulk_commit();
+    tc::bulk_wait_all();  // every store of this CTA is performed before it exits
   } else if (warp >= 4 * CG) {
     // ------------------------------------------------------------ widening warps
     if constexpr (kQ8) {
@@ -576,22 +704,32 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       const int nt = r1 > (int)lt0 ? r1 - (int)lt0 : 0;  // real tiles here
       const int fx = x.real > 0 ? x.real - 1 : 0;       // the tile that adds the new keys
       const bool has_fix = lt0 <= fx && fx < lt1;
-      const bool moves = item_moves(p, x.pl);
+      const DMove mv = dmove<QT>(p, x);
       const long long P = x.pl.P;
       if (lt0 == 0 && x.kvh == 0 && tid == 0) {
         if (p.resident_out) p.resident_out[x.b] = (int32_t)x.pl.Lt;
-        if (moves) p.move_list[atomicAdd(p.move_count, 1u)] = x.b;
+        if (mv.kind == kRegister) {
+          if (p.no_finish)  // the host ruled this out: no cache-update kernel follows
+            flag(p, GQAW_DEV_INTERNAL);
+          else
+            p.move_list[atomicAdd(p.move_count, 1u)] = x.b;
+        }
       }
-      if (has_fix && !moves) {  // append the new rows at L(P) + s: no query of this step reads them
+      // present rows [r_begin, r_end) <- the new rows r - kept (K and V), all softmax threads
+      auto append = [&](long long r_begin, long long r_end) {
         constexpr int kRowB = kQ8 ? kD : 2 * kD, kVecs = kRowB / 16;  // row bytes, 16-byte vectors
-        for (int e = tid; e < 2 * S * kVecs; e += kSoft) {
-          const int tensor = e / (S * kVecs), rem = e % (S * kVecs), s = rem / kVecs, vec = rem % kVecs;
-          const size_t in_row = ((size_t)x.b * S + s) * p.Nkv + x.kvh;
-          const size_t out_row = ((size_t)x.b * p.Nkv + x.kvh) * (size_t)p.C + (size_t)(x.pl.Lp + s);
+        const int n = r_end > r_begin ? (int)(r_end - r_begin) : 0;
+        for (int e = tid; e < 2 * n * kVecs; e += kSoft) {
+          const int tensor = e / (n * kVecs), rem = e % (n * kVecs), rr = rem / kVecs, vec = rem % kVecs;
+          const long long r = r_begin + rr;
+          const size_t in_row = ((size_t)x.b * S + (size_t)(r - mv.kept)) * p.Nkv + x.kvh;
+          const size_t out_row = ((size_t)x.b * p.Nkv + x.kvh) * (size_t)p.C + (size_t)r;
           reinterpret_cast<uint4 *>(static_cast<char *>(tensor ? p.prv : p.prk) + out_row * kRowB)[vec] =
               reinterpret_cast<const uint4 *>(static_cast<const char *>(tensor ? p.v : p.k) + in_row * kRowB)[vec];
         }
-      }
+      };
+      // append the new rows at L(P) + s (kept = L(P)): no query of this step reads them
+      if (has_fix && mv.kind == kAppend) append(mv.kept, x.pl.Lt);
       for (int n = tid; n < NVT; n += kSoft)  // rows past S x g: the item's first bias row
         brow[n] = !p.bias ? 0
                           : (long long)x.b * p.bsb +
@@ -736,6 +874,14 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       }
       if (stop) break;
       named_barrier(kBar, kSoft);  // every thread is done with the last tile's maxima in red
+      if (has_fix && mv.kind == kFused) {
+        // The new rows at [kept, L(T)), now that this CTA has read its tiles: the rows in
+        // its own range (from a_fix on) or below the window; those in an earlier CTA's
+        // range are written by the unit's last contributor.
+        const long long a_fix = mv.lo_row + (long long)lt0 * kKeys;
+        append(mv.kept, x.pl.Lt < mv.lo_row ? x.pl.Lt : mv.lo_row);
+        append(mv.kept > a_fix ? mv.kept : a_fix, x.pl.Lt);
+      }
 
       // ---- the unit's state in this CTA: O^T (TMEM), reference maxima, sums
       bool ok = true;
@@ -888,6 +1034,8 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         }
         named_barrier(kBar, kSoft);
         if (tid == 0) {
+          // a range starting inside a fused unit stashed rows for the last contributor
+          if (mv.kind == kFused && lt0 > 0 && nt > 0 && !mbar_wait(stash_bar, 0)) flag(p, GQAW_DEV_TIMEOUT);
           __threadfence();
           s_last = atomicAdd(&p.tickets[u], 1u) == (unsigned)(cl - cf);
         }
@@ -933,6 +1081,30 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
               const size_t orow = ((size_t)x.b * S + n / g) * p.Nq + h;
               out[orow * kD + t] = __float2bfloat16_rn(sink_divide(A[i], Lsum[i], M[i], sink_log2(p, h)) * vsc);
             }
+          }
+          if (mv.kind == kFused) {
+            // Every contributor has read its tiles: write the rows they left for the last
+            // one -- each later contributor's stash (the first min(seed, rows) rows of its
+            // range, moved down by seed) and the new rows in an earlier range than the
+            // appending CTA's.
+            for (long long c = cf + 1; c <= cl; ++c) {
+              const long long lt0c = c * V / G - u * TPU;  // >= 1: c starts inside the unit
+              if (lt0c >= x.real) continue;                // no key tile of the unit in c
+              const long long ac = mv.lo_row + lt0c * kKeys;
+              const long long nv = mv.nwin - lt0c * kKeys < kKeys ? mv.nwin - lt0c * kKeys : kKeys;
+              const int nst = (int)(mv.seed < nv ? mv.seed : nv);
+              const unsigned char *src = p.stash + (size_t)c * kMoveStashBytes;
+              const size_t grow0 = ((size_t)x.b * p.Nkv + x.kvh) * (size_t)p.C + (size_t)(ac - mv.seed);
+              for (int e = tid; e < nst * 32; e += kSoft) {  // 32 parts of 16 bytes per row (K and V)
+                const int r = e >> 5, part = e & 31, tn = part >> 4, off = (part & 15) * 16;
+                *reinterpret_cast<uint4 *>(static_cast<char *>(tn ? p.prv : p.prk) + (grow0 + r) * kRow + off) =
+                    __ldcg(reinterpret_cast<const uint4 *>(src + (size_t)r * 2 * kRow + tn * kRow + off));
+              }
+            }
+            const long long cfix = owner_cta(u * TPU + fx, V, G);
+            const long long lt0f = cfix * V / G - u * TPU > 0 ? cfix * V / G - u * TPU : 0;
+            const long long a_fix = mv.lo_row + lt0f * kKeys;
+            append(mv.kept > mv.lo_row ? mv.kept : mv.lo_row, a_fix < x.pl.Lt ? a_fix : x.pl.Lt);
           }
           if (tid == 0) p.tickets[u] = 0u;  // ready for the next step
         }

@@ -30,6 +30,8 @@ struct TdMaps {
   CUtensorMap q;   // query (B*S, Nq, D): box (64, g, S), all query rows of one (item, kv head)
   CUtensorMap kc;  // past_key as (B*Nkv*C, D): box (64, 128)
   CUtensorMap vc;  // past_value
+  CUtensorMap kc8; // past_key as (B*Nkv*C, D): box (64, 8), for stores of moved rows (bf16 caches)
+  CUtensorMap vc8; // past_value
 };
 
 struct TdArgs {
@@ -41,9 +43,14 @@ struct TdArgs {
 // Row stride of a split partial: 128 accumulators, max, sum, padded to 16 bytes.
 constexpr int kTcPartialStride = 132;
 
+// Small-step kernel, bf16 caches: the rows (K and V, head size 128) a CTA may stash for
+// the last contributor of a unit whose rows it moves, and the bytes of one CTA's stash.
+constexpr int kMoveStashRows = 32;
+constexpr int kMoveStashBytes = kMoveStashRows * 2 * 128 * 2;
+
 namespace tc {
 
-// ---------------------------------------------------------------- tensor TMA loads
+// ---------------------------------------------------------------- tensor TMA loads and stores
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar,
                                             uint64_t policy) {
@@ -62,6 +69,25 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+
+// Store a box from shared memory (laid out as the map's swizzle says) to the tensor at
+// coordinates (c0, c1), in this thread's bulk async-group.  The box must lie inside the
+// tensor and c0 * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, const void *src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
+
+// Close this thread's current bulk async-group.
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until this thread's bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until this thread's bulk groups have completed (their writes are performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Bring a box of a tensor into L2 ahead of its load (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {

@@ -28,6 +28,7 @@ GQAW_DEV_BAD_SEQLEN = 1
 GQAW_DEV_TIMEOUT = 2
 GQAW_DEV_BAD_POSITION = 4
 GQAW_DEV_QUERY_RANGE = 8
+GQAW_DEV_INTERNAL = 16
 
 STATUS_NAMES = {0: "GQAW_OK", 1: "GQAW_EINVAL", 2: "GQAW_EUNSUPPORTED", 3: "GQAW_ECUDA",
                 4: "GQAW_EWORKSPACE", 5: "GQAW_EDEVICE"}

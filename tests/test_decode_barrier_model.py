@@ -14,15 +14,19 @@ With a code cache, per key tile k:
              done; may rescale O once P.V(k - 1) is done; reads O after a unit's last P.V.
 
 With a bf16 cache there are no widening warps: S^T(k) and P.V(k) read the TMA stage of
-tile k itself, and a commit after P.V(k) frees the stage.
+tile k itself, and the stage is freed by two arrivals: a commit after P.V(k), and the
+mover warp once the TMA stores of the rows it moves out of tile k have read the stage
+(it waits for tile k's load, issues the stores, waits until they have read shared memory,
+then arrives -- on every tile, with or without rows to move).
 
 This model runs the roles as coroutines under a random scheduler, with TMA loads
 and MMAs completing in any order and a commit arriving once every MMA issued before it
 has completed (MMAs into one accumulator run in issue order).  It checks that every
 parity wait finds its barrier exactly k or k + 1 phases along (a parity wait cannot tell
 phases two apart), that no buffer is rewritten while an MMA or role still uses it, and
-that the roles never deadlock.  A planted early reuse of a V tile must be caught, so the
-model is not vacuous.
+that the roles never deadlock.  A planted early reuse of a V tile, and a mover that
+frees a stage before its stores have read it, must be caught, so the model is not
+vacuous.
 """
 from __future__ import annotations
 
@@ -43,7 +47,7 @@ class _Bar:
             self.pending = self.count
 
 
-def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000):
+def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=False):
     """Run the protocol over units of the given key-tile counts; returns the violations.
     ``v_reuse_lag``: the widening warps reuse V tile k & 1 once P.V(k - lag) is done (2 is
     the kernel's rule).  ``codes=False``: a bf16 cache, where S^T and P.V read the TMA
@@ -55,7 +59,7 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000):
             tiles.append(dict(kc=kc, ui=ui, first=lt == 0, last=lt == nt - 1))
             kc += 1
     bars = {("full", i): _Bar(1) for i in range(3)}
-    bars.update({("empty", i): _Bar(1) for i in range(3)})
+    bars.update({("empty", i): _Bar(1 if codes else 2) for i in range(3)})
     for i in range(2):
         for name in ("s_full", "s_free", "p_full", "o_done", "q_full", "q_free", "kconv", "vconv"):
             bars[(name, i)] = _Bar(1)
@@ -89,7 +93,7 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000):
 
     def stage_read_done(k):
         stage_reads[k] = stage_reads.get(k, 0) + 1
-        if stage_reads[k] == 2:
+        if stage_reads[k] == 3:  # S^T, P.V and the mover's stores
             consumed.add(("stage", k))
 
     def commit(name):
@@ -186,6 +190,22 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000):
                 commit(("q_free", u & 1))
             yield
 
+    def mover():
+        for t in tiles:
+            k = t["kc"]
+            while not ready(("full", k % 3), k // 3):
+                yield
+            if held["stage"][k % 3] != k:
+                errors.append("mover reads stage %d holding tile %s" % (k % 3, held["stage"][k % 3]))
+            store = dict(name="ST(%d)" % k, reads=[("stage", k % 3)], writes=[], done=False,
+                         on_done=lambda k=k: stage_read_done(k))
+            mmas.append(store)  # an asynchronous reader of the stage, like an MMA
+            yield
+            while not mover_early and not store["done"]:  # the bulk group has read the stage
+                yield
+            bars[("empty", k % 3)].arrive()
+            yield
+
     def softmax():
         for t in tiles:
             k, u = t["kc"], t["ui"]
@@ -215,6 +235,8 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000):
     roles = {"producer": producer(), "mma": mma(), "softmax": softmax()}
     if codes:
         roles["widening"] = widening()
+    else:
+        roles["mover"] = mover()
     steps = 0
     while roles and not errors and steps < max_steps:
         steps += 1
@@ -271,3 +293,11 @@ def test_model_catches_early_v_reuse():
     errors = [e for i, units in enumerate(cases) for e in _run(units, i, v_reuse_lag=3)]
     assert any("ambiguous" in e or "rewrites" in e or "reads V" in e for e in errors)
     assert not [e for i, units in enumerate(cases) for e in _run(units, i, v_reuse_lag=1)]
+
+
+def test_model_catches_mover_freeing_a_stage_early():
+    """A mover that frees a stage as soon as it has issued its stores (before they have
+    read shared memory) lets the next load overwrite a stage still being read."""
+    cases = _cases(300, 3)
+    errors = [e for i, units in enumerate(cases) for e in _run(units, i, codes=False, mover_early=True)]
+    assert any("before tile" in e or "rewrites" in e for e in errors)

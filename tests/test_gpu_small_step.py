@@ -126,3 +126,49 @@ def test_slack_compactions_many_steps():
         q, k, v = wl.step_inputs(sh, 1, 4600 + t)
         p.step(q, k, v, T)
         T = T + 1
+
+
+# ------------------------------------------------------------------ block compaction inside the attention pass
+
+
+@pytest.mark.parametrize("S,split_keys", [(8, 0), (8, 128), (8, 256), (4, 128), (2, 128), (1, 128), (16, 384)])
+def test_compaction_inside_attention_splits(S, split_keys):
+    """C = W + S - 1 (a block of S rows reclaimed on every step once the cache is full):
+    the kernel moves the surviving rows from its staged tiles and appends the new rows,
+    and the host launches no cache-update kernel.  Forced splits put CTA range
+    boundaries inside every unit -- rows stashed for the last contributor -- and the
+    varying lengths give last tiles of fewer rows than the block (appends left to the
+    last contributor).  Softcap and a bias as in the verify workload; 8 steps with
+    accepted counts k ~ U{0..S}."""
+    from sliding_window_gqa_02_gb300 import gqaw
+
+    W, g = 300, min(4, 32 // S)  # S x g <= 32 query rows per unit
+    sh = wl.Shape("cmp", B=4, Nq=4 * g, Nkv=4, D=128, W=W, C=W + S - 1, dtype=wl.BF16, softcap=30.0)
+    pk, pv = wl.cache(sh, 43 + S)
+    p = Pair(sh.B, sh.Nq, sh.Nkv, sh.D, sh.C, sh.W, sh.dtype, softcap=30.0, past_key=pk, past_value=pv,
+             split_keys=split_keys)
+    T = np.array([290, 299, 300, 1000], np.int64) + np.arange(4)
+    TM = int(T.max()) + 8 * S + 8
+    bias = wl.bias(sh.B, sh.Nq, S, TM, 43 + S)
+    strides = (sh.Nq * S * TM, S * TM, TM)
+    for t in range(8):
+        q, k, v = wl.step_inputs(sh, S, 4300 + 10 * S + t)
+        n0 = gqaw.gqaw_launch_count()
+        p.step(q, k, v, T + S - 1, total=int(T.max()) + S, bias=bias, bias_strides=strides)
+        assert gqaw.gqaw_launch_count() - n0 == 1  # the attention kernel alone
+        T = T + wl.accepted(sh.B, S, 4300 + t)
+
+
+@pytest.mark.parametrize("W,S", [(4, 4), (8, 8), (33, 1), (2, 2)])
+def test_compaction_inside_attention_small_windows(W, S):
+    """Windows of a few keys with C = W + S - 1 (every surviving row is inside the
+    window, the new rows may outnumber them), and a block of 33 rows with S = 1 (larger
+    than the rows a CTA may stash: the cache-update kernel takes it)."""
+    sh = wl.Shape("cmpw", B=3, Nq=8, Nkv=2, D=128, W=W, C=W + S - 1 if W != 33 else 2 * W, dtype=wl.BF16)
+    pk, pv = wl.cache(sh, 44)
+    p = Pair(sh.B, sh.Nq, sh.Nkv, sh.D, sh.C, sh.W, sh.dtype, past_key=pk, past_value=pv, split_keys=128)
+    T = np.array([0, 7, 100], np.int64)
+    for t in range(12):
+        q, k, v = wl.step_inputs(sh, S, 4400 + t)
+        p.step(q, k, v, T + S - 1)
+        T = T + S
