@@ -7,6 +7,7 @@ decode token for all 64 items through the C ABI.  The K/V window read per step
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl gqaw|reference]
                     [--workload longctx-decode|longctx-decode-sink|longctx-decode-rope|longctx-decode-i8|
+                     longctx-decode-modeA|
                      longctx-decode-e4m3|pages-decode|slack-decode|verify4|verify8|longctx-prefill|
                      longctx-prefill-rope]
                     [--no-extra] [--no-cpu-baseline]
@@ -55,6 +56,9 @@ def workload_spec(name):
     if name in ("longctx-decode-i8", "longctx-decode-e4m3"):  # the same decode on a quantized cache
         return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False,
                     quant=name.rsplit("-", 1)[1])
+    if name == "longctx-decode-modeA":  # the same decode into a separate present buffer (ping-pong)
+        return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False,
+                    separate=True)
     if name == "longctx-decode-rope":  # the same decode with the rotary embedding fused in
         return dict(shape=wl.SHAPES["longctx"], S=1, lo=4096, hi=32768, bias=False, graph=False, accept=False,
                     rope=True)
@@ -80,6 +84,7 @@ def workload_config(name, B=None):
             "kv_num_heads": sh.Nkv, "head_size": sh.D, "local_window_size": sh.W, "capacity": sh.C,
             "cache_dtype": sh.dtype, "softcap": sh.softcap, "bias": spec["bias"],
             "head_sink": bool(spec.get("sink", False)), "rotary": bool(spec.get("rope", False)),
+            "present": "separate buffer" if spec.get("separate") else "in place",
             "kv_cache": spec.get("quant") or sh.dtype, "contexts": "U[%d,%d]" % (spec["lo"], spec["hi"])}
 
 
@@ -90,17 +95,35 @@ def resident_len(T, C, W):
     return gqaw.gqaw_resident_len(int(T), int(C), int(W))
 
 
-def algorithmic_bytes(sh, S, T_before, B, cache_bytes=None):
+def attention_moves_rows(sh, S, P, separate, quant=None):
+    """Does the attention kernel write an item's surviving rows itself (the small-step
+    kernel with a bf16 cache: a separate present buffer, or in place with a reclaimed
+    block of at most 32 rows whose surviving rows all lie in the window)?  Returns the
+    rows it writes that way."""
+    if attention_kernel(sh, S, quant) != "mmad" or quant:
+        return 0
+    Lp, Lt = resident_len(P, sh.C, sh.W), resident_len(P + S, sh.C, sh.W)
+    seed, kept, nwin = Lp + S - Lt, Lt - S, min(P, sh.W - 1)
+    if separate or (seed > 0 and 0 <= kept <= nwin and seed <= 32):
+        return max(0, min(kept, nwin))
+    return 0
+
+
+def algorithmic_bytes(sh, S, T_before, B, cache_bytes=None, separate=False, quant=None):
     """Bytes the step must move, per item from the pre-step lengths: the in-window cache
     rows and the new rows read, the appended rows written, the surviving rows of a
     reclaimed block written at their new place (and read too where they lie below the
     window the attention reads: a surviving row inside the window is read once, for both
-    uses), the query read and the output written.  Returns (attention bytes, step bytes).
+    uses), the query read and the output written.  With a ``separate`` present buffer every
+    surviving row is written (and read where it lies below the window), reclaimed block
+    or not.  Returns (attention kernel bytes, step bytes): the attention kernel's are its
+    reads, the query and output, and the rows it writes (appends, and the surviving rows
+    it moves from its staged tiles).
     ``cache_bytes``: bytes of a cache element (1 for a quantized cache).  Bias bytes are
     added by the caller."""
     e = 2 if sh.dtype == "bf16" else 4
     row = sh.Nkv * sh.D * (cache_bytes or e) * 2  # K and V of one position, all kv heads
-    attn = comp = app = 0
+    attn = comp = app = kern_w = 0
     for b in range(B):
         P = int(T_before[b])
         T = P + S
@@ -110,10 +133,11 @@ def algorithmic_bytes(sh, S, T_before, B, cache_bytes=None):
         nwin = min(P, sh.W - 1)
         attn += row * (nwin + S)
         app += row * min(S, Lt)
-        if seed > 0 and kept > 0:
+        if (seed > 0 or separate) and kept > 0:
             comp += row * (kept + max(kept - nwin, 0))
+        kern_w += row * (min(S, Lt) + attention_moves_rows(sh, S, P, separate, quant))
     qo = B * S * sh.Nq * sh.D * e * 2
-    return attn + qo, attn + app + comp + qo
+    return attn + qo + kern_w, attn + app + comp + qo
 
 
 def cache_events(sh, S, T_before):
@@ -333,6 +357,10 @@ class Harness:
         self.vs = torch.tensor([0.025 if self.quant == "i8" else 0.005], dtype=torch.float32, device=self.dev)
         self.pk, self.pv = pk.to(self.dev), pv.to(self.dev)
         del pk, pv
+        # a separate present buffer: the two caches alternate as past and present
+        self.separate = bool(spec.get("separate"))
+        self.pk2 = torch.empty_like(self.pk) if self.separate else self.pk
+        self.pv2 = torch.empty_like(self.pv) if self.separate else self.pv
         T0 = wl.lengths(B, spec["lo"], spec["hi"], seed)
         # per-step pre-step lengths (decode: +1; verify: + accepted; prefill: +S)
         Ts = [T0.copy()]
@@ -377,11 +405,17 @@ class Harness:
         gqaw.check(gqaw.gqaw_workspace_init(int(self.ws.data_ptr()), ws_bytes, self.stream.cuda_stream))
         self.args = [self._args(t, self.ws) for t in range(n)]
 
+    def caches(self, t):
+        """(past_key, past_value, present_key, present_value) of step t."""
+        if t % 2 == 0:
+            return self.pk, self.pv, self.pk2, self.pv2
+        return self.pk2, self.pv2, self.pk, self.pv
+
     def _args(self, t, ws):
         i = t % len(self.q)
         sh = self.sh
         return self.gqaw.make_args(
-            self.q[i], self.k[i], self.v[i], self.pk, self.pv, self.pk, self.pv, self.seq[t], self.totals[t],
+            self.q[i], self.k[i], self.v[i], *self.caches(t), self.seq[t], self.totals[t],
             sh.Nq, sh.Nkv, sh.W, self.out, workspace=ws, softcap=sh.softcap, attention_bias=self.bias,
             bias_strides=self.bias_strides, split_keys=self.split_keys, head_sink=self.head_sink,
             cos_cache=self.cos, sin_cache=self.sin, k_scale=self.ks, v_scale=self.vs)
@@ -441,7 +475,7 @@ class Harness:
         for e in self.ev_done + self.ev_out:
             e.record(self.stream)
         self.args_e2e = [self.gqaw.make_args(
-            self.q_e[t % 2], self.k_e[t % 2], self.v_e[t % 2], self.pk, self.pv, self.pk, self.pv, self.seq[t],
+            self.q_e[t % 2], self.k_e[t % 2], self.v_e[t % 2], *self.caches(t), self.seq[t],
             self.totals[t], sh.Nq, sh.Nkv, sh.W, self.out_e[t % 2], workspace=self.ws, softcap=sh.softcap,
             attention_bias=self.bias, bias_strides=self.bias_strides, split_keys=self.split_keys,
             head_sink=self.head_sink, cos_cache=self.cos, sin_cache=self.sin, k_scale=self.ks, v_scale=self.vs)
@@ -545,7 +579,7 @@ def run_gpu(args, rank, world):
     att_bytes = step_bytes = 0.0
     bias_bytes = 0.0
     for t in range(Wm, Wm + K):
-        a, s = algorithmic_bytes(sh, S, h.T[t], B, 1 if h.quant else None)
+        a, s = algorithmic_bytes(sh, S, h.T[t], B, 1 if h.quant else None, h.separate, h.quant)
         att_bytes += a
         step_bytes += s
         if h.bias is not None:
@@ -640,7 +674,8 @@ def extra_workloads(main, args):
     import torch
 
     out = {}
-    for name in ("pages-decode", "slack-decode", "verify4", "verify8", "longctx-prefill", "longctx-decode-sink",
+    for name in ("pages-decode", "slack-decode", "verify4", "verify8", "longctx-prefill", "longctx-decode-modeA",
+                 "longctx-decode-sink",
                  "longctx-decode-rope", "longctx-prefill-rope", "longctx-decode-i8", "longctx-decode-e4m3"):
         if name == main:
             continue
@@ -675,7 +710,7 @@ def extra_workloads(main, args):
             passes.append(e0.elapsed_time(e1) / K)
         check_device(h, name)
         ms = statistics.median(passes)
-        _, sb = algorithmic_bytes(h.sh, h.S, h.T[Wm], h.B, 1 if h.quant else None)
+        _, sb = algorithmic_bytes(h.sh, h.S, h.T[Wm], h.B, 1 if h.quant else None, h.separate, h.quant)
         if h.bias is not None:
             sb += 4 * h.sh.Nq * visible_columns(h.S, h.T[Wm], h.sh.W)
         hbm, _ = measured_peaks()

@@ -13,6 +13,10 @@
 //  * append (PR #32419 "Specify GroupQueryAttention windowed KV cache layout
 //    contract", Description: row i holds absolute position T - L + i): present rows
 //    [max(kept, 0), L(T)) <- the last new rows.  When S > L(T) only the tail survives.
+//  * for an entry flagged kListBelowOnly (a separate present buffer whose window rows and
+//    new rows the small-step attention kernel has written from its staged tiles), only
+//    the surviving rows below the window: present row r <- past row r + seed for
+//    r in [0, lo_row - seed), lo_row = L(P) - min(P, W - 1) the window's first row.
 //
 // In place, the move reads rows [seed, seed + kept) and writes rows [0, kept): an
 // overlapping forward move.  It runs in ascending batches; each batch loads all its
@@ -52,7 +56,9 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) 
   const int cvec = rowb / 16 / ncg;  // vectors per row in one column group
 
   for (long long job0 = blockIdx.x; job0 < njobs; job0 += gridDim.x) {
-    const int b = p.move_list[job0 / per_item];
+    const int entry = p.move_list[job0 / per_item];
+    const int b = entry & (kListBelowOnly - 1);
+    const bool below_only = (entry & kListBelowOnly) != 0;
     int job = (int)(job0 % per_item);
     const int cg = job % ncg;
     job /= ncg;
@@ -62,16 +68,19 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) 
     if (!plan_item(p, b, pl)) continue;  // registered items were valid; defensive
     const long long kept = pl.Lt - p.S;
     const long long seed = pl.Lp + p.S - pl.Lt;
+    const long long nwin = pl.P < p.W - 1 ? pl.P : p.W - 1;
+    // rows to move: all surviving ones, or those below the window
+    const long long nmove = below_only ? pl.Lp - nwin - seed : kept;
     const size_t sl = (size_t)b * p.Nkv + kvh;
     const char *src = static_cast<const char *>(tensor ? p.pv : p.pk) + sl * p.C * rowb;
     char *dst = static_cast<char *>(tensor ? p.prv : p.prk) + sl * p.C * rowb;
     const bool inplace = src == dst;
     const int col0 = cg * cvec * 16;
 
-    if (kept > 0 && (seed > 0 || !inplace)) {
+    if (nmove > 0 && (seed > 0 || !inplace)) {
       const int rows_per_batch = kFinishThreads * kCopyVecs / cvec;
-      for (long long r0 = 0; r0 < kept; r0 += rows_per_batch) {
-        const int nrow = (int)(kept - r0 < rows_per_batch ? kept - r0 : rows_per_batch);
+      for (long long r0 = 0; r0 < nmove; r0 += rows_per_batch) {
+        const int nrow = (int)(nmove - r0 < rows_per_batch ? nmove - r0 : rows_per_batch);
         const int nvec = nrow * cvec;
         uint4 buf[kCopyVecs];
 #pragma unroll
@@ -94,6 +103,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) 
       }
     }
 
+    if (below_only) continue;  // the new rows are in place already
     // Append: present row r (r >= max(kept, 0)) holds new token seed + r - Lp.
     const long long a0 = kept > 0 ? kept : 0;
     const long long napp = pl.Lt - a0;

@@ -139,6 +139,7 @@ bool head_size_ok(int D) { return D == 8 || D == 16 || D == 32 || D == 64 || D =
 gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   if (!a) return fail(GQAW_EINVAL, "args is NULL");
   if (a->batch_size < 0) return fail(GQAW_EINVAL, "batch_size %d < 0", a->batch_size);
+  if (a->batch_size >= (1 << 30)) return fail(GQAW_EUNSUPPORTED, "batch_size %d >= 2^30", a->batch_size);
   if (a->sequence_length < 1) return fail(GQAW_EINVAL, "sequence_length %d < 1", a->sequence_length);
   if (a->num_heads < 1 || a->kv_num_heads < 1)
     return fail(GQAW_EINVAL, "num_heads %d and kv_num_heads %d must be >= 1", a->num_heads, a->kv_num_heads);
@@ -561,13 +562,14 @@ gqaw_status run_mmad(const gqaw_step_args *a, const Launch &L, const gqaw::Param
   const bool q8 = L.quant != 0;
   const CUtensorMapDataType qt = q8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapDataType ct = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  std::memset(&maps.kc8, 0, sizeof(maps.kc8));
-  std::memset(&maps.vc8, 0, sizeof(maps.vc8));
+  std::memset(&maps.kp, 0, 4 * sizeof(maps.kp));
   if (!encode_map(&maps.q, q8 ? p.q16 : p.q, 3, q_dims, q_str, q_box, qt) ||
       !encode_map(&maps.kc, a->past_key, 2, c_dims, q8 ? c8_str : c_str, q8 ? c8_box : c_box, ct) ||
       !encode_map(&maps.vc, a->past_value, 2, c_dims, q8 ? c8_str : c_str, q8 ? c8_box : c_box, ct) ||
-      (!q8 && (!encode_map(&maps.kc8, a->past_key, 2, c_dims, c_str, r8_box, ct) ||
-               !encode_map(&maps.vc8, a->past_value, 2, c_dims, c_str, r8_box, ct))))
+      (!q8 && (!encode_map(&maps.kp, a->present_key, 2, c_dims, c_str, c_box, ct) ||
+               !encode_map(&maps.vp, a->present_value, 2, c_dims, c_str, c_box, ct) ||
+               !encode_map(&maps.kp8, a->present_key, 2, c_dims, c_str, r8_box, ct) ||
+               !encode_map(&maps.vp8, a->present_value, 2, c_dims, c_str, r8_box, ct))))
     return fail(GQAW_ECUDA, "cuTensorMapEncodeTiled failed for the small-step kernel");
   const cudaError_t e = gqaw::launch_mmad(p, L.tda, maps, (int)L.td_ctas, st);
   if (e != cudaSuccess) return cuda_fail(e, "small-step tensor-core kernel launch");

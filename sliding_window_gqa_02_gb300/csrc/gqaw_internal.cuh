@@ -118,6 +118,11 @@ __device__ __forceinline__ bool plan_item(const Params &p, int b, Plan &pl) { re
 
 __device__ __forceinline__ void flag(const Params &p, uint32_t bits) { atomicOr(p.status, bits); }
 
+// Flag of a cache-update list entry (item index | flag): present is a separate buffer and
+// the attention kernel has written the surviving rows of the window and the new rows;
+// only the surviving rows below the window (which the step does not read) are left.
+constexpr int kListBelowOnly = 1 << 30;
+
 // Does item b need the cache-update kernel?  Yes when a block of rows is reclaimed
 // (seed = L(P) + S - L(T) > 0: rows move, and the new rows land on rows the attention
 // may still read) or when present is a separate buffer (every surviving row is

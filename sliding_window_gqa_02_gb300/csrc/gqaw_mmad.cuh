@@ -266,22 +266,28 @@ __device__ __forceinline__ DUnit dunit(const Params &p, long long u) {
 // What the kernel does with the rows of a unit's item (the same for each of its kv heads).
 //  kAppend:   in place, no block reclaimed: the new rows go to [L(P), L(P) + S), which no
 //             query reads, appended by the CTA holding the unit's last tile first thing.
-//  kFused:    in place, a block of seed <= kMoveStashRows rows reclaimed, every surviving
-//             row [seed, L(P)) inside the window the step reads, bf16 cache: the mover
-//             warps write the surviving rows from the staged tiles to [0, kept), and the
-//             CTA holding the unit's last tile appends the new rows at [kept, L(T)) after
-//             its tiles (block compaction and append of PR #31142 "[CPU] Add windowed kv
-//             cache for GQA", "Drifting layout", done inside the attention pass).
-//  kRegister: anything else (a separate present buffer, surviving rows below the window,
-//             a larger block, a code cache): the item is recorded for the cache-update
-//             kernel.
+//  kFused:    bf16 cache, and either in place with a block of seed <= kMoveStashRows
+//             rows reclaimed and every surviving row [seed, L(P)) inside the window the
+//             step reads, or a separate present buffer (mobius issue #111, Part 1.2,
+//             "Mode A"): the mover warp writes the surviving rows of the staged tiles to
+//             [0, kept) of present, and the CTA holding the unit's last tile appends the
+//             new rows at [kept, L(T)) after its tiles (block compaction and append of PR
+//             #31142 "[CPU] Add windowed kv cache for GQA", "Drifting layout", done inside
+//             the attention pass).  With a separate present buffer nothing the step reads
+//             is overwritten (no stash, no deferred rows); its surviving rows below the
+//             window, which no tile holds, are left to the cache-update kernel (`below`).
+//  kRegister: anything else (surviving rows below the window or a larger block in place,
+//             a code cache): the item is recorded for the cache-update kernel.
 enum { kAppend = 0, kFused = 1, kRegister = 2 };
 struct DMove {
   int kind;
+  bool sep;              // present is a separate buffer
+  bool below;            // separate present: surviving rows [seed, lo_row) lie below the window
   long long seed, kept;  // rows reclaimed; rows surviving (the new rows follow them)
   long long lo_row;      // slice row of the window's first key (key position x.lo)
   long long nwin;        // keys of the window held in the cache: rows [lo_row, L(P))
 };
+
 
 template <int QT>
 __device__ __forceinline__ DMove dmove(const Params &p, const DUnit &x) {
@@ -291,9 +297,11 @@ __device__ __forceinline__ DMove dmove(const Params &p, const DUnit &x) {
   m.nwin = x.pl.P - x.lo;
   m.lo_row = x.pl.Lp - m.nwin;
   const bool inplace = p.pk == p.prk && p.pv == p.prv;
+  m.sep = !inplace;
+  m.below = m.sep && m.kept > m.nwin;
   if (inplace && m.seed == 0)
     m.kind = kAppend;
-  else if (QT == 0 && inplace && m.kept >= 0 && m.kept <= m.nwin && m.seed <= kMoveStashRows)
+  else if (QT == 0 && (m.sep || (m.kept >= 0 && m.kept <= m.nwin && m.seed <= kMoveStashRows)))
     m.kind = kFused;
   else
     m.kind = kRegister;
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         const long long r0 = mv.lo_row + (long long)t.lt * kKeys;  // slice row of tile row 0
         const int nvalid = (int)(mv.nwin - (long long)t.lt * kKeys < kKeys ? mv.nwin - (long long)t.lt * kKeys : kKeys);
         const int tA = (int)(mv.seed - r0 > 0 ? mv.seed - r0 : 0);  // rows below tA are reclaimed
-        const bool stash = t.first && t.lt > 0;                    // the range starts inside the unit
+        const bool stash = !mv.sep && t.first && t.lt > 0;         // in place, the range starts inside the unit
         const int nst = stash ? (int)(mv.seed < nvalid ? mv.seed : nvalid) : 0;
         const long long grow0 = ((long long)t.x.b * p.Nkv + t.x.kvh) * p.C + r0 - mv.seed;
         auto part = [&](int r) {  // this lane's 16 bytes of tile row r (128-byte swizzle)
@@ -612,14 +620,14 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
           };
           if (lo == 0 && hi == kKeys) {  // the whole tile: one 128-row box per half of K and V
             if (lane < 4)
-              tc::tma_store_2d((lane >> 1) ? &maps.vc : &maps.kc, (lane & 1) * 64, (int)grow0,
+              tc::tma_store_2d((lane >> 1) ? &maps.vp : &maps.kp, (lane & 1) * 64, (int)grow0,
                                sb + (lane >> 1) * 2 * kHalf + (lane & 1) * kHalf);
           } else {
             const int c0 = (lo + 7) & ~7, c1 = hi & ~7;  // 8-row-aligned run [c0, c1)
             if (c1 > c0) {
               for (int i = lane; i < (c1 - c0) / 2; i += 32) {  // (c1 - c0) / 8 boxes x 4 halves
                 const int rr = c0 + (i >> 2) * 8, tn = (i >> 1) & 1, hf = i & 1;
-                tc::tma_store_2d(tn ? &maps.vc8 : &maps.kc8, hf * 64, (int)(grow0 + rr),
+                tc::tma_store_2d(tn ? &maps.vp8 : &maps.kp8, hf * 64, (int)(grow0 + rr),
                                  sb + tn * 2 * kHalf + hf * kHalf + rr * 128);
               }
               for (int r = lo; r < c0; ++r) ragged(r);
@@ -708,11 +716,11 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       const long long P = x.pl.P;
       if (lt0 == 0 && x.kvh == 0 && tid == 0) {
         if (p.resident_out) p.resident_out[x.b] = (int32_t)x.pl.Lt;
-        if (mv.kind == kRegister) {
+        if (mv.kind == kRegister || mv.below) {
           if (p.no_finish)  // the host ruled this out: no cache-update kernel follows
             flag(p, GQAW_DEV_INTERNAL);
           else
-            p.move_list[atomicAdd(p.move_count, 1u)] = x.b;
+            p.move_list[atomicAdd(p.move_count, 1u)] = mv.kind == kRegister ? x.b : (x.b | kListBelowOnly);
         }
       }
       // present rows [r_begin, r_end) <- the new rows r - kept (K and V), all softmax threads
@@ -878,9 +886,13 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         // The new rows at [kept, L(T)), now that this CTA has read its tiles: the rows in
         // its own range (from a_fix on) or below the window; those in an earlier CTA's
         // range are written by the unit's last contributor.
-        const long long a_fix = mv.lo_row + (long long)lt0 * kKeys;
-        append(mv.kept, x.pl.Lt < mv.lo_row ? x.pl.Lt : mv.lo_row);
-        append(mv.kept > a_fix ? mv.kept : a_fix, x.pl.Lt);
+        if (mv.sep) {  // nothing the step reads is overwritten
+          append(mv.kept > 0 ? mv.kept : 0, x.pl.Lt);
+        } else {
+          const long long a_fix = mv.lo_row + (long long)lt0 * kKeys;
+          append(mv.kept, x.pl.Lt < mv.lo_row ? x.pl.Lt : mv.lo_row);
+          append(mv.kept > a_fix ? mv.kept : a_fix, x.pl.Lt);
+        }
       }
 
       // ---- the unit's state in this CTA: O^T (TMEM), reference maxima, sums
@@ -1035,7 +1047,8 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         named_barrier(kBar, kSoft);
         if (tid == 0) {
           // a range starting inside a fused unit stashed rows for the last contributor
-          if (mv.kind == kFused && lt0 > 0 && nt > 0 && !mbar_wait(stash_bar, 0)) flag(p, GQAW_DEV_TIMEOUT);
+          if (mv.kind == kFused && !mv.sep && lt0 > 0 && nt > 0 && !mbar_wait(stash_bar, 0))
+            flag(p, GQAW_DEV_TIMEOUT);
           __threadfence();
           s_last = atomicAdd(&p.tickets[u], 1u) == (unsigned)(cl - cf);
         }
@@ -1082,7 +1095,7 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
               out[orow * kD + t] = __float2bfloat16_rn(sink_divide(A[i], Lsum[i], M[i], sink_log2(p, h)) * vsc);
             }
           }
-          if (mv.kind == kFused) {
+          if (mv.kind == kFused && !mv.sep) {
             // Every contributor has read its tiles: write the rows they left for the last
             // one -- each later contributor's stash (the first min(seed, rows) rows of its
             // range, moved down by seed) and the new rows in an earlier range than the

@@ -30,8 +30,11 @@ struct TdMaps {
   CUtensorMap q;   // query (B*S, Nq, D): box (64, g, S), all query rows of one (item, kv head)
   CUtensorMap kc;  // past_key as (B*Nkv*C, D): box (64, 128)
   CUtensorMap vc;  // past_value
-  CUtensorMap kc8; // past_key as (B*Nkv*C, D): box (64, 8), for stores of moved rows (bf16 caches)
-  CUtensorMap vc8; // past_value
+  // bf16 caches: stores of the rows moved inside the attention pass, into present
+  CUtensorMap kp;  // present_key as (B*Nkv*C, D): box (64, 128)
+  CUtensorMap vp;  // present_value
+  CUtensorMap kp8; // present_key as (B*Nkv*C, D): box (64, 8)
+  CUtensorMap vp8; // present_value
 };
 
 struct TdArgs {

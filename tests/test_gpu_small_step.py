@@ -172,3 +172,22 @@ def test_compaction_inside_attention_small_windows(W, S):
         q, k, v = wl.step_inputs(sh, S, 4400 + t)
         p.step(q, k, v, T + S - 1)
         T = T + S
+
+
+@pytest.mark.parametrize("split_keys", [0, 512])
+def test_separate_present_long_context(split_keys):
+    """Separate present buffers (mobius issue #111, Part 1.2, Mode A) on the long-context
+    shape: the attention kernel writes the surviving rows of the window and the new rows,
+    the cache-update kernel only the rows below the window (up to G - 1 = 1024 of them);
+    items placed so that some steps reclaim a block.  Three decode steps, every item."""
+    sh = wl.Shape("sepl", B=8, Nq=32, Nkv=8, D=128, W=4096, C=5120, dtype=wl.BF16)
+    pk, pv = wl.cache(sh, 45)
+    p = Pair(sh.B, sh.Nq, sh.Nkv, sh.D, sh.C, sh.W, sh.dtype, past_key=pk, past_value=pv, inplace=False,
+             split_keys=split_keys)
+    G = sh.C - sh.W + 1
+    T = wl.lengths(sh.B, 4096, 32768, 45)
+    T[0], T[1], T[2] = sh.C + G, sh.C + 2 * G - 1, 4100  # reclaim at the first / second step; no block yet
+    for t in range(3):
+        q, k, v = wl.step_inputs(sh, 1, 4500 + t)
+        p.step(q, k, v, T)
+        T = T + 1
