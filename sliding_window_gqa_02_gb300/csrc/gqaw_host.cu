@@ -280,6 +280,14 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     L->tda.units = (long long)a->batch_size * a->kv_num_heads;
     const long long vt = L->tda.units * L->tda.tpu;
     long long ctas = std::min(vt, kSms);
+    // Stream-K splits units at CTA range boundaries; a CTA that touches two units pays two
+    // unit epilogues (dependent global round trips: the step's own keys, the partials, the
+    // ticket, the merge), about kEpilogueTiles key tiles each on a busy memory system.
+    // When the units fit in one wave, one whole unit per CTA can finish sooner: its CTAs
+    // read TPU tiles and run one epilogue, against about V/SMs tiles and two epilogues.
+    constexpr long long kEpilogueTiles = 6;
+    if (L->tda.units < kSms && L->tda.tpu + kEpilogueTiles <= ceil_div(vt, kSms) + 2 * kEpilogueTiles)
+      ctas = L->tda.units;
     if (a->split_keys > 0) ctas = std::max(1LL, std::min(ctas, ceil_div(vt * 128, a->split_keys)));
     L->td_ctas = ctas;
     L->off_tickets = L->off_list + align256((size_t)a->batch_size * 4);

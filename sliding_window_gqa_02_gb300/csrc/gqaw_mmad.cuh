@@ -762,7 +762,19 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < NC; ++i) bnext[i] = __ldg(p.bias + brow[col0 + i] + col);
       };
-      if (p.bias && nt > 0) fetch_bias((int)lt0);
+      // ... and brought into L2 three tiles ahead of that: under a full memory system a DRAM
+      // load can take longer than a tile, and the softmax would wait for it
+      auto prefetch_bias = [&](int lt_) {
+        const long long j0_ = x.lo + (long long)lt_ * kKeys;
+        const int nv_ = (int)(P - j0_ < kKeys ? P - j0_ : kKeys);
+        const long long col = j0_ + (t < nv_ ? t : nv_ - 1);
+#pragma unroll
+        for (int i = 0; i < NC; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.bias + brow[col0 + i] + col));
+      };
+      if (p.bias && nt > 0) {
+        fetch_bias((int)lt0);
+        for (int l = (int)lt0 + 1; l < r1 && l <= (int)lt0 + 2; ++l) prefetch_bias(l);
+      }
       for (int lt = (int)lt0; lt < r1; ++lt, ++kc) {
         const long long j0 = x.lo + (long long)lt * kKeys;
         const int nvalid = (int)(P - j0 < kKeys ? P - j0 : kKeys);
@@ -776,6 +788,7 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < NC; ++i) bv[i] = bnext[i];
           if (lt + 1 < r1) fetch_bias(lt + 1);
+          if (lt + 3 < r1) prefetch_bias(lt + 3);
         }
         bool ok = mbar_wait(&s_full[kc & 1], (kc >> 1) & 1);
         tc::fence_after_sync();
