@@ -359,12 +359,12 @@ struct Walker {
 // groups.  4 * CG softmax warps: warps w and w + 4 read the same TMEM lanes (the same
 // keys, the same head dimensions) and own different query rows, NC = NVT / CG each.
 // QT: 0 for bf16 caches, GQAW_I8 or GQAW_E4M3 for the codes of a quantized cache.
-// Warps: 4 * CG softmax warps, WW widening warps (quantized cache only), the TMA producer
-// warp, the MMA issuer warp, and for bf16 caches the mover warp.
+// Warps: 4 * CG softmax warps, 4 widening warps (quantized cache only: one per TMEM lane
+// quarter), the TMA producer warp, the MMA issuer warp, and for bf16 caches the mover warp.
 template <int CG, int QT>
 struct Warps {
   static_assert(QT == 0 || CG <= 2, "code caches: at most two column groups");
-  static constexpr int kWiden = QT == 0 ? 0 : (CG == 1 ? 4 : 2);
+  static constexpr int kWiden = QT == 0 ? 0 : 4;
   static constexpr int kProducer = 4 * CG + kWiden;
   static constexpr int kMover = QT == 0 ? 1 : 0;  // bf16 caches: the warp that moves rows
   static constexpr int kThreads = 32 * (kProducer + 2 + kMover);
@@ -440,17 +440,22 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
   // Q and P^T rows past the unit's query rows stay zero for the whole kernel.
   for (int e = tid; e < (8 * L::kQHalf) / 16; e += blockDim.x)
     reinterpret_cast<uint4 *>(smem + L::kQ)[e] = make_uint4(0, 0, 0, 0);
-  if (warp == 0) tc::tmem_alloc(tmem_slot, L::kCols);
+  // TMEM columns: S^T (two buffers of NPAD) and O^T (NPAD); with a code cache also two
+  // widened K tiles, the A operand of S^T: 128 keys (lanes) x 128 fp16 dimensions in 64
+  // columns of pairs each, at columns 128 and 192
+  constexpr uint32_t kTmemK = 128;
+  constexpr uint32_t kTCols = kQ8 ? 256 : L::kCols;
+  static_assert(3 * NPAD <= (int)kTmemK, "S^T and O^T before the K tiles");
+  if (warp == 0) tc::tmem_alloc(tmem_slot, kTCols);
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 2 * NPAD;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 2 * NPAD, tmem_k = tmem + kTmemK;
   pdl_wait();                // the previous kernel in the stream has completed
 
   auto stage = [&](int kc) { return smem + (kc % kStages) * (kQ8 ? kCodeStage : kStageBytes); };
-  unsigned char *const k16buf = smem + kK16;
   auto v16buf = [&](int kc) { return smem + kV16 + (kc & 1) * 2 * kHalf; };
   auto qbuf = [&](int ui) { return smem + L::kQ + (ui & 1) * 2 * L::kQHalf; };
   auto pbuf = [&](int kc) { return smem + L::kP + (kc & 1) * 2 * L::kQHalf; };
@@ -519,13 +524,20 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
           return false;
         if (t.kc >= 2 && !mbar_wait(&s_free[t.kc & 1], ((t.kc - 2) >> 1) & 1)) return false;
         tc::fence_after_sync();
-        unsigned char *kb = kQ8 ? k16buf : stage(t.kc), *qb = qbuf(t.ui);
+        // One descriptor per operand and tile; a K step adds its byte offset (over 16) to the
+        // address field.  (The MMA thread shares its SM sub-partition with busy warps: every
+        // instruction it saves shortens the issue of the tile's MMAs.)
+        const uint64_t kd = tc::smem_desc_sw128(stage(t.kc), 16, 1024);
+        const uint64_t qd = tc::smem_desc_sw128(qbuf(t.ui), 16, 1024);
+        const uint32_t ds = tmem_s + (t.kc & 1) * NPAD, ka = tmem_k + (t.kc & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const int half = kk / 4, off = (kk % 4) * 32;
-          const uint64_t a = tc::smem_desc_sw128(kb + half * kHalf + off, 16, 1024);
-          const uint64_t bq = tc::smem_desc_sw128(qb + half * L::kQHalf + off, 16, 1024);
-          tc::mma_bf16_ss(tmem_s + (t.kc & 1) * NPAD, a, bq, kIdescS, kk > 0);
+          const uint64_t bq = qd + (uint64_t)((half * L::kQHalf + off) >> 4);
+          if (kQ8)  // K from tensor memory (buffer kc & 1): 8 columns (16 dimensions) per step
+            tc::mma_bf16_ts(ds, ka + kk * 8, bq, kIdescS, kk > 0);
+          else
+            tc::mma_bf16_ss(ds, kd + (uint64_t)((half * kHalf + off) >> 4), bq, kIdescS, kk > 0);
         }
         tc::mma_commit(&s_full[t.kc & 1]);
         return true;
@@ -548,14 +560,14 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        unsigned char *vb = kQ8 ? v16buf(cur.kc) : stage(cur.kc) + 2 * kHalf;
+        // V^T: M = dims in two 64-dim halves 16 KB apart, K = keys in 8-key groups 1 KB apart
+        const uint64_t vd = tc::smem_desc_sw128(kQ8 ? v16buf(cur.kc) : stage(cur.kc) + 2 * kHalf, kHalf, 1024);
+        const uint64_t pd = tc::smem_desc_sw128(pbuf(cur.kc), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          // V^T: M = dims in two 64-dim halves 16 KB apart, K = keys in 8-key groups 1 KB apart
-          const uint64_t a = tc::smem_desc_sw128(vb + kk * 16 * 128, kHalf, 1024);
-          const uint64_t bp = tc::smem_desc_sw128(pbuf(cur.kc) + (kk / 4) * L::kQHalf + (kk % 4) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem_o, a, bp, kIdescO, !(cur.first && kk == 0));
-        }
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc::mma_bf16_ss(tmem_o, vd + (uint64_t)((kk * 16 * 128) >> 4),
+                          pd + (uint64_t)(((kk / 4) * L::kQHalf + (kk % 4) * 32) >> 4), kIdescO,
+                          !(cur.first && kk == 0));
         tc::mma_commit(&o_done[cur.kc & 1]);
         if (!kQ8) tc::mma_commit(&empty[cur.kc % kStages]);
         if (cur.last) tc::mma_commit(&q_free[cur.ui & 1]);
@@ -652,12 +664,15 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
   } else if (warp >= 4 * CG) {
     // ------------------------------------------------------------ widening warps
     if constexpr (kQ8) {
-      // Thread i widens rows i, i + 32 * WW, ... of each code tile: K(k) into the fp16 K
-      // buffer once S^T of tile k - 1 is done with it, V(k) into fp16 buffer k & 1 once
-      // P.V of tile k - 2 is done (keys past P as zeros).  Each wait is for a phase the
-      // barrier can have reached only after the one these warps saw a tile earlier.
+      // Thread i (lane i % 32 of lane quarter i / 32) widens row i of each code tile: K(k)
+      // into its lane of TMEM K buffer k & 1 (the A operand of S^T) once S^T of tile k - 2
+      // is done with it, V(k) into fp16 buffer k & 1 in shared memory once P.V of tile k - 2
+      // is done (keys past P as zeros).  Each wait is for a phase the barrier can have
+      // reached only after the one these warps saw a tile earlier (S^T(k) needs K(k)).
       const int i0 = tid - 128 * CG;
       constexpr int kStep = 32 * kWidenW;
+      static_assert(kStep == kKeys, "one key row per widening thread");
+      const uint32_t k_lane = tmem_k + ((uint32_t)((warp & 3) * 32) << 16);
       Walker w{ufirst - 1, ulast, tb, te, TPU, 0, 0, 0, -1, DUnit()};
       DTile t;
       bool fine = true;
@@ -666,10 +681,28 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         const long long j0 = t.x.lo + (long long)t.lt * kKeys;
         const int nvalid = (int)(t.x.pl.P - j0 < kKeys ? t.x.pl.P - j0 : kKeys);
         fine = mbar_wait(&full[kc % kStages], (kc / kStages) & 1);
-        if (fine && kc >= 1) fine = mbar_wait(&s_full[(kc - 1) & 1], ((kc - 1) >> 1) & 1);
+        if (fine && kc >= 2) fine = mbar_wait(&s_full[kc & 1], ((kc - 2) >> 1) & 1);
         tc::fence_after_sync();
-        for (int r = i0; r < kKeys; r += kStep) widen_row<QT>(stage(kc), k16buf, r, false);
-        tc::fence_proxy_async_smem();
+        {
+          const unsigned char *codes = stage(kc) + i0 * 128;
+          uint4 u[8];  // all eight loads first: their latencies overlap
+#pragma unroll
+          for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4 *>(codes + ((c ^ (i0 & 7)) << 4));
+#pragma unroll
+          for (int c = 0; c < 8; c += 2) {  // 16 codes -> 8 columns of fp16 pairs, dimension 2j low
+            uint32_t h[16], h0[8], h1[8];
+            widen16<QT>(u[c], h0);
+            widen16<QT>(u[c + 1], h1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              h[j] = h0[j];
+              h[8 + j] = h1[j];
+            }
+            tc::tmem_st16_async(k_lane + (uint32_t)((kc & 1) * 64 + c * 8), h);
+          }
+          tc::tmem_wait_st();
+        }
+        tc::fence_before_sync();
         mbar_arrive(&kconv_full[kc & 1]);
         if (fine && kc >= 2) fine = mbar_wait(&o_done[kc & 1], ((kc - 2) >> 1) & 1);
         tc::fence_after_sync();
@@ -1147,7 +1180,7 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
   pdl_launch_dependents();  // every role of this CTA is done: the cache update may be launched
   if (warp == 0) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, L::kCols);
+    tc::tmem_dealloc(tmem, kTCols);
   }
 }
 

@@ -6,7 +6,7 @@ With a code cache, per key tile k:
 
   producer   Q of a unit into buffer u & 1 once the unit two back is done with it;
              codes of tile k into stage k % 3 once tile k - 3 is widened;
-  widening   K(k) into the single fp16 K tile once S^T(k - 1) is done;
+  widening   K(k) into fp16 K tile k & 1 (tensor memory) once S^T(k - 2) is done;
              V(k) into fp16 V tile k & 1 once P.V(k - 2) is done;
   MMA        S^T(k + 1) before P.V(k); P.V(k) once P(k) and V(k) are ready (and, on a
              unit's first tile, once the previous unit's O has been read);
@@ -65,7 +65,7 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=F
             bars[(name, i)] = _Bar(1)
     bars["o_free"] = _Bar(1)
     mmas, commits, loads, errors = [], [], [], []
-    held = dict(K16=None, V16=[None, None], P=[None, None], stage=[None, None, None])
+    held = dict(K16=[None, None], V16=[None, None], P=[None, None], stage=[None, None, None])
     consumed = set()      # ("stage", k): every reader of tile k's stage is done
     stage_reads = {}      # bf16 cache: MMAs done reading tile k's stage (S^T and P.V)
 
@@ -122,10 +122,10 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=F
             k = t["kc"]
             while not ready(("full", k % 3), k // 3):
                 yield
-            while k >= 1 and not ready(("s_full", (k - 1) & 1), (k - 1) >> 1):
+            while k >= 2 and not ready(("s_full", k & 1), (k - 2) >> 1):
                 yield
-            role_writes("K16", "widening of K(%d)" % k)
-            held["K16"] = k
+            role_writes(("K16", k & 1), "widening of K(%d)" % k)
+            held["K16"][k & 1] = k
             bars[("kconv", k & 1)].arrive()
             yield
             while k >= lag and not ready(("o_done", (k - lag) & 1), (k - lag) >> 1):
@@ -149,9 +149,9 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=F
             while k >= 2 and not ready(("s_free", k & 1), (k - 2) >> 1):
                 yield
             if codes:
-                if held["K16"] != k:
-                    errors.append("S(%d) reads the K tile of tile %s" % (k, held["K16"]))
-                issue("S(%d)" % k, ["K16", ("Q", u & 1)], [("S", k & 1)])
+                if held["K16"][k & 1] != k:
+                    errors.append("S(%d) reads the K tile of tile %s" % (k, held["K16"][k & 1]))
+                issue("S(%d)" % k, [("K16", k & 1), ("Q", u & 1)], [("S", k & 1)])
             else:
                 if held["stage"][k % 3] != k:
                     errors.append("S(%d) reads stage %d holding tile %s" % (k, k % 3, held["stage"][k % 3]))
