@@ -360,14 +360,22 @@ struct Walker {
 // keys, the same head dimensions) and own different query rows, NC = NVT / CG each.
 // QT: 0 for bf16 caches, GQAW_I8 or GQAW_E4M3 for the codes of a quantized cache.
 // Warps: 4 * CG softmax warps, 4 widening warps (quantized cache only: one per TMEM lane
-// quarter), the TMA producer warp, the MMA issuer warp, and for bf16 caches the mover warp.
+// quarter), the TMA producer warp, the warp whose first thread issues the S^T MMAs, for
+// bf16 caches the mover warp, and the warp whose first thread issues the P.V MMAs.  The two
+// issuing threads sit in warps of their own: each MMA issue and each barrier wait of such a
+// thread costs tens of cycles on a sub-partition shared with busy warps, and one thread
+// issuing both products per tile set the pace of decode tiles.  With four column groups
+// (32 query rows, softcap and bias: paced by the softmax warps) one thread issues both,
+// S^T of the next tile before P.V of this one: a fifth spinning warp slowed those warps.
 template <int CG, int QT>
 struct Warps {
   static_assert(QT == 0 || CG <= 2, "code caches: at most two column groups");
   static constexpr int kWiden = QT == 0 ? 0 : 4;
   static constexpr int kProducer = 4 * CG + kWiden;
   static constexpr int kMover = QT == 0 ? 1 : 0;  // bf16 caches: the warp that moves rows
-  static constexpr int kThreads = 32 * (kProducer + 2 + kMover);
+  static constexpr bool kSplitMMA = CG < 4;
+  static constexpr int kPV = kSplitMMA ? kProducer + 2 + kMover : kProducer + 1;
+  static constexpr int kThreads = 32 * (kProducer + 2 + kMover + (kSplitMMA ? 1 : 0));
 };
 
 template <int NPAD, int NVT, int CG, int QT>
@@ -433,7 +441,7 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       mbar_init(&o_done[i], 1);
     }
     mbar_init(o_free, kSoft);
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, Warps<CG, QT>::kSplitMMA ? 2 : 1);  // a commit from each MMA-issuing thread
     mbar_fence_init();
     s_abort = 0;
   }
@@ -510,8 +518,16 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       for (int q = qissued - 1 > 0 ? qissued - 1 : 0; q <= qissued; ++q)
         if (q >= 0 && !mbar_wait(&q_full[q & 1], (q >> 1) & 1)) flag(p, GQAW_DEV_TIMEOUT);
     }
-  } else if (warp == kProducer + 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kProducer + 1 || warp == Warps<CG, QT>::kPV) {
+    // ------------------------------------------------------------ MMA issuers
+    // The first thread of warp kProducer + 1 issues S^T of every tile; the first thread of
+    // warp kPV issues P.V.  They write different accumulators (S^T buffers, O^T), and
+    // every order between them goes through a barrier: P.V(k) needs P(k), which the
+    // softmax writes only after S^T(k) has completed, so a commit of the P.V thread also
+    // covers the S^T of the same tile (the stage it freed, the last tile's Q).  A
+    // tcgen05.commit tracks the MMAs of its own thread; each thread commits its own
+    // barriers, and both commit mma_done before TMEM is released.
+    const bool s_role = warp == kProducer + 1;
     if (lane == 0) {
       // K: K-major, Q: K-major; V^T: MN-major, P^T: K-major (fp16 operands for a quantized cache)
       constexpr uint32_t kIdescS = kQ8 ? idesc_f16_f32(kKeys, NPAD, 0, 0) : tc::idesc_bf16_f32(kKeys, NPAD, 0, 0);
@@ -542,23 +558,11 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         tc::mma_commit(&s_full[t.kc & 1]);
         return true;
       };
-      DTile cur, nxt;
-      bool hc = w.next(p, cur), fine = true;
-      if (hc) fine = mma_s(cur);
-      while (hc && fine && !*reinterpret_cast<volatile int *>(&s_abort)) {
-        // S^T of the next tile while this one is in softmax.  (A quantized cache's next K
-        // needs only this tile's S^T done and the P.V of two tiles back, both issued.)
-        const bool hn = w.next(p, nxt);
-        if (hn && !mma_s(nxt)) {
-          fine = false;
-          break;
-        }
+      auto mma_pv = [&](const DTile &cur) -> bool {
         if (!mbar_wait(&p_full[cur.kc & 1], (cur.kc >> 1) & 1) ||
             (kQ8 && !mbar_wait(&vconv_full[cur.kc & 1], (cur.kc >> 1) & 1)) ||
-            (cur.first && cur.ui >= 1 && !mbar_wait(o_free, (cur.ui - 1) & 1))) {
-          fine = false;
-          break;
-        }
+            (cur.first && cur.ui >= 1 && !mbar_wait(o_free, (cur.ui - 1) & 1)))
+          return false;
         tc::fence_after_sync();
         // V^T: M = dims in two 64-dim halves 16 KB apart, K = keys in 8-key groups 1 KB apart
         const uint64_t vd = tc::smem_desc_sw128(kQ8 ? v16buf(cur.kc) : stage(cur.kc) + 2 * kHalf, kHalf, 1024);
@@ -571,8 +575,29 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         tc::mma_commit(&o_done[cur.kc & 1]);
         if (!kQ8) tc::mma_commit(&empty[cur.kc % kStages]);
         if (cur.last) tc::mma_commit(&q_free[cur.ui & 1]);
-        cur = nxt;
-        hc = hn;
+        return true;
+      };
+      DTile cur, nxt;
+      bool fine = true;
+      if constexpr (Warps<CG, QT>::kSplitMMA) {
+        if (s_role) {  // S^T of each tile, as soon as its K, Q and S^T buffer are ready
+          while (fine && !*reinterpret_cast<volatile int *>(&s_abort) && w.next(p, cur)) fine = mma_s(cur);
+        } else {       // P.V of each tile, as soon as its P and V are ready
+          while (fine && !*reinterpret_cast<volatile int *>(&s_abort) && w.next(p, cur)) fine = mma_pv(cur);
+        }
+      } else {  // one thread: S^T of the next tile while this one is in softmax, then its P.V
+        bool hc = w.next(p, cur);
+        if (hc) fine = mma_s(cur);
+        while (hc && fine && !*reinterpret_cast<volatile int *>(&s_abort)) {
+          const bool hn = w.next(p, nxt);
+          if (hn && !mma_s(nxt)) {
+            fine = false;
+            break;
+          }
+          fine = mma_pv(cur);
+          cur = nxt;
+          hc = hn;
+        }
       }
       if (!fine) {
         flag(p, GQAW_DEV_TIMEOUT);

@@ -8,8 +8,9 @@ With a code cache, per key tile k:
              codes of tile k into stage k % 3 once tile k - 3 is widened;
   widening   K(k) into fp16 K tile k & 1 (tensor memory) once S^T(k - 2) is done;
              V(k) into fp16 V tile k & 1 once P.V(k - 2) is done;
-  MMA        S^T(k + 1) before P.V(k); P.V(k) once P(k) and V(k) are ready (and, on a
-             unit's first tile, once the previous unit's O has been read);
+  MMA S      S^T(k) once K(k), Q and S^T buffer k & 1 are ready (its own thread);
+  MMA PV     P.V(k) once P(k) and V(k) are ready (and, on a unit's first tile, once the
+             previous unit's O has been read), on a second thread;
   softmax    reads S^T(k), frees it; writes P(k) into buffer k & 1 once P.V(k - 2) is
              done; may rescale O once P.V(k - 1) is done; reads O after a unit's last P.V.
 
@@ -20,8 +21,9 @@ mover warp once the TMA stores of the rows it moves out of tile k have read the 
 then arrives -- on every tile, with or without rows to move).
 
 This model runs the roles as coroutines under a random scheduler, with TMA loads
-and MMAs completing in any order and a commit arriving once every MMA issued before it
-has completed (MMAs into one accumulator run in issue order).  It checks that every
+and MMAs completing in any order and a commit arriving once every MMA its own thread
+issued before it has completed (a tcgen05.commit tracks only its thread's MMAs; MMAs
+into one accumulator run in issue order).  It checks that every
 parity wait finds its barrier exactly k or k + 1 phases along (a parity wait cannot tell
 phases two apart), that no buffer is rewritten while an MMA or role still uses it, and
 that the roles never deadlock.  A planted early reuse of a V tile, and a mover that
@@ -47,7 +49,7 @@ class _Bar:
             self.pending = self.count
 
 
-def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=False):
+def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=False, empty_by_s=False):
     """Run the protocol over units of the given key-tile counts; returns the violations.
     ``v_reuse_lag``: the widening warps reuse V tile k & 1 once P.V(k - lag) is done (2 is
     the kernel's rule).  ``codes=False``: a bf16 cache, where S^T and P.V read the TMA
@@ -84,20 +86,20 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=F
         if in_use(buf):
             errors.append("%s rewrites %s while %s uses it" % (who, buf, in_use(buf)[0]["name"]))
 
-    def issue(name, reads, writes, on_done=None):
+    def issue(name, reads, writes, on_done=None, thread=None):
         for w in writes:
             # MMAs into one accumulator run in issue order
             if [m for m in in_use(w) if not (w in m["writes"] and w not in m["reads"])]:
                 errors.append("MMA %s writes %s while it is in use" % (name, w))
-        mmas.append(dict(name=name, reads=reads, writes=writes, done=False, on_done=on_done))
+        mmas.append(dict(name=name, reads=reads, writes=writes, done=False, on_done=on_done, thread=thread))
 
     def stage_read_done(k):
         stage_reads[k] = stage_reads.get(k, 0) + 1
         if stage_reads[k] == 3:  # S^T, P.V and the mover's stores
             consumed.add(("stage", k))
 
-    def commit(name):
-        commits.append((name, [m for m in mmas if not m["done"]]))
+    def commit(name, thread):
+        commits.append((name, [m for m in mmas if not m["done"] and m.get("thread") == thread]))
 
     def producer():
         for t in tiles:
@@ -137,7 +139,7 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=F
             bars[("empty", k % 3)].arrive()
             yield
 
-    def mma():
+    def mma_s():
         def s_of(t):
             k, u = t["kc"], t["ui"]
             while t["first"] and not ready(("q_full", u & 1), u >> 1):
@@ -151,21 +153,22 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=F
             if codes:
                 if held["K16"][k & 1] != k:
                     errors.append("S(%d) reads the K tile of tile %s" % (k, held["K16"][k & 1]))
-                issue("S(%d)" % k, [("K16", k & 1), ("Q", u & 1)], [("S", k & 1)])
+                issue("S(%d)" % k, [("K16", k & 1), ("Q", u & 1)], [("S", k & 1)], thread="S")
             else:
                 if held["stage"][k % 3] != k:
                     errors.append("S(%d) reads stage %d holding tile %s" % (k, k % 3, held["stage"][k % 3]))
                 issue("S(%d)" % k, [("stage", k % 3), ("Q", u & 1)], [("S", k & 1)],
-                      on_done=lambda k=k: stage_read_done(k))
-            commit(("s_full", k & 1))
+                      on_done=lambda k=k: stage_read_done(k), thread="S")
+            commit(("s_full", k & 1), "S")
+            if empty_by_s and not codes:  # planted: the S^T thread releases the stage
+                commit(("empty", k % 3), "S")
             yield
 
-        if not tiles:
-            return
-        yield from s_of(tiles[0])
-        for i, t in enumerate(tiles):
-            if i + 1 < len(tiles):
-                yield from s_of(tiles[i + 1])
+        for t in tiles:
+            yield from s_of(t)
+
+    def mma_pv():
+        for t in tiles:
             k, u = t["kc"], t["ui"]
             while not ready(("p_full", k & 1), k >> 1):
                 yield
@@ -178,16 +181,18 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=F
             if codes:
                 if held["V16"][k & 1] != k:
                     errors.append("P.V(%d) reads V of tile %s" % (k, held["V16"][k & 1]))
-                issue("PV(%d)" % k, [("V16", k & 1), ("P", k & 1)], ["O"])
-                commit(("o_done", k & 1))
+                issue("PV(%d)" % k, [("V16", k & 1), ("P", k & 1)], ["O"], thread="PV")
+                commit(("o_done", k & 1), "PV")
             else:
                 if held["stage"][k % 3] != k:
                     errors.append("P.V(%d) reads stage %d holding tile %s" % (k, k % 3, held["stage"][k % 3]))
-                issue("PV(%d)" % k, [("stage", k % 3), ("P", k & 1)], ["O"], on_done=lambda k=k: stage_read_done(k))
-                commit(("o_done", k & 1))
-                commit(("empty", k % 3))
+                issue("PV(%d)" % k, [("stage", k % 3), ("P", k & 1)], ["O"], on_done=lambda k=k: stage_read_done(k),
+                      thread="PV")
+                commit(("o_done", k & 1), "PV")
+                if not empty_by_s:
+                    commit(("empty", k % 3), "PV")
             if t["last"]:
-                commit(("q_free", u & 1))
+                commit(("q_free", u & 1), "PV")
             yield
 
     def mover():
@@ -232,7 +237,7 @@ def _run(units, seed, v_reuse_lag=2, codes=True, max_steps=400000, mover_early=F
                 bars["o_free"].arrive()
                 yield
 
-    roles = {"producer": producer(), "mma": mma(), "softmax": softmax()}
+    roles = {"producer": producer(), "mma_s": mma_s(), "mma_pv": mma_pv(), "softmax": softmax()}
     if codes:
         roles["widening"] = widening()
     else:
@@ -301,3 +306,12 @@ def test_model_catches_mover_freeing_a_stage_early():
     cases = _cases(300, 3)
     errors = [e for i, units in enumerate(cases) for e in _run(units, i, codes=False, mover_early=True)]
     assert any("before tile" in e or "rewrites" in e for e in errors)
+
+
+def test_model_catches_stage_released_by_the_wrong_thread():
+    """With S^T and P.V on two threads, a commit covers only its own thread's MMAs: the
+    S^T thread releasing a stage (its commit does not wait for P.V of the tile) lets the
+    next load overwrite a stage that P.V still reads."""
+    cases = _cases(300, 4)
+    errors = [e for i, units in enumerate(cases) for e in _run(units, i, codes=False, empty_by_s=True)]
+    assert any("before tile" in e or "reads stage" in e or "rewrites" in e for e in errors)
