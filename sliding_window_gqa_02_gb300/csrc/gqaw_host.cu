@@ -286,9 +286,10 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
     // When the units fit in one wave, one whole unit per CTA can finish sooner: its CTAs
     // read TPU tiles and run one epilogue, against about V/SMs tiles and two epilogues.
     constexpr long long kEpilogueTiles = 6;
-    if (L->tda.units < kSms && L->tda.tpu + kEpilogueTiles <= ceil_div(vt, kSms) + 2 * kEpilogueTiles)
+    if (a->split_keys > 0)  // the caller's chunk size overrides both choices
+      ctas = std::max(1LL, std::min(ctas, ceil_div(vt * 128, a->split_keys)));
+    else if (L->tda.units < kSms && L->tda.tpu + kEpilogueTiles <= ceil_div(vt, kSms) + 2 * kEpilogueTiles)
       ctas = L->tda.units;
-    if (a->split_keys > 0) ctas = std::max(1LL, std::min(ctas, ceil_div(vt * 128, a->split_keys)));
     L->td_ctas = ctas;
     L->off_tickets = L->off_list + align256((size_t)a->batch_size * 4);
     L->off_partials = L->off_tickets + align256((size_t)L->tda.units * 4);
