@@ -124,20 +124,21 @@ __device__ __forceinline__ void widen16<GQAW_E4M3>(const uint4 &u, uint32_t (&h)
   }
 }
 
-// Row t of a code tile (128 one-byte codes in a 128-byte swizzled row) into row t of an
-// fp16 operand tile (two 64-dim halves of 128-byte swizzled rows, 16 KB apart); zero:
-// write zeros (keys past the tile's valid rows).
-template <int QT>
-__device__ __forceinline__ void widen_row(const unsigned char *codes, unsigned char *dst, int t, bool zero) {
+// Chunks [c0, c0 + NCH) (16 codes each) of row t of a code tile (128 one-byte codes in a
+// 128-byte swizzled row) into row t of an fp16 operand tile (two 64-dim halves of 128-byte
+// swizzled rows, 16 KB apart); zero: write zeros (keys past the tile's valid rows).
+template <int QT, int NCH = 8>
+__device__ __forceinline__ void widen_row(const unsigned char *codes, unsigned char *dst, int t, bool zero, int c0 = 0) {
   const int sw = t & 7;
-  uint4 u[8];  // all eight loads first: their latencies overlap
+  uint4 u[NCH];  // all loads first: their latencies overlap
 #pragma unroll
-  for (int c = 0; c < 8; ++c)
-    u[c] = zero ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4 *>(codes + t * 128 + ((c ^ sw) << 4));
+  for (int i = 0; i < NCH; ++i)
+    u[i] = zero ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4 *>(codes + t * 128 + (((c0 + i) ^ sw) << 4));
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int i = 0; i < NCH; ++i) {
+    const int c = c0 + i;
     uint32_t h[8];
-    widen16<QT>(u[c], h);
+    widen16<QT>(u[i], h);
     unsigned char *row = dst + (c >> 2) * kHalf + t * 128;
     const int cc = (c & 3) * 2;
     *reinterpret_cast<uint4 *>(row + ((cc ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -360,7 +361,9 @@ struct Walker {
 // keys, the same head dimensions) and own different query rows, NC = NVT / CG each.
 // QT: 0 for bf16 caches, GQAW_I8 or GQAW_E4M3 for the codes of a quantized cache.
 // Warps: 4 * CG softmax warps, 4 widening warps (quantized cache only: one per TMEM lane
-// quarter), the TMA producer warp, the warp whose first thread issues the S^T MMAs, for
+// quarter; 8 for int8 codes with one column group, two per quarter, each widening one
+// 64-dimension half of its rows: the int8 widening takes more arithmetic than e4m3's
+// pair conversion), the TMA producer warp, the warp whose first thread issues the S^T MMAs, for
 // bf16 caches the mover warp, and the warp whose first thread issues the P.V MMAs.  The two
 // issuing threads sit in warps of their own: each MMA issue and each barrier wait of such a
 // thread costs tens of cycles on a sub-partition shared with busy warps, and one thread
@@ -370,7 +373,7 @@ struct Walker {
 template <int CG, int QT>
 struct Warps {
   static_assert(QT == 0 || CG <= 2, "code caches: at most two column groups");
-  static constexpr int kWiden = QT == 0 ? 0 : 4;
+  static constexpr int kWiden = QT == 0 ? 0 : (QT == GQAW_I8 && CG == 1 ? 8 : 4);
   static constexpr int kProducer = 4 * CG + kWiden;
   static constexpr int kMover = QT == 0 ? 1 : 0;  // bf16 caches: the warp that moves rows
   static constexpr bool kSplitMMA = CG < 4;
@@ -694,9 +697,10 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       // is done with it, V(k) into fp16 buffer k & 1 in shared memory once P.V of tile k - 2
       // is done (keys past P as zeros).  Each wait is for a phase the barrier can have
       // reached only after the one these warps saw a tile earlier (S^T(k) needs K(k)).
-      const int i0 = tid - 128 * CG;
-      constexpr int kStep = 32 * kWidenW;
-      static_assert(kStep == kKeys, "one key row per widening thread");
+      constexpr int kParts = kWidenW / 4;      // threads per row (1 or 2)
+      constexpr int kChunks = 8 / kParts;      // 16-code chunks of a row per thread
+      const int i0 = (warp & 3) * 32 + lane;  // key row = TMEM lane of this warp's quarter
+      const int c0 = (warp - 4 * CG) / 4 * kChunks;
       const uint32_t k_lane = tmem_k + ((uint32_t)((warp & 3) * 32) << 16);
       Walker w{ufirst - 1, ulast, tb, te, TPU, 0, 0, 0, -1, DUnit()};
       DTile t;
@@ -710,20 +714,21 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         tc::fence_after_sync();
         {
           const unsigned char *codes = stage(kc) + i0 * 128;
-          uint4 u[8];  // all eight loads first: their latencies overlap
+          uint4 u[kChunks];  // all loads first: their latencies overlap
 #pragma unroll
-          for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4 *>(codes + ((c ^ (i0 & 7)) << 4));
+          for (int i = 0; i < kChunks; ++i)
+            u[i] = *reinterpret_cast<const uint4 *>(codes + (((c0 + i) ^ (i0 & 7)) << 4));
 #pragma unroll
-          for (int c = 0; c < 8; c += 2) {  // 16 codes -> 8 columns of fp16 pairs, dimension 2j low
+          for (int i = 0; i < kChunks; i += 2) {  // 16 codes -> 8 columns of fp16 pairs, dimension 2j low
             uint32_t h[16], h0[8], h1[8];
-            widen16<QT>(u[c], h0);
-            widen16<QT>(u[c + 1], h1);
+            widen16<QT>(u[i], h0);
+            widen16<QT>(u[i + 1], h1);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               h[j] = h0[j];
               h[8 + j] = h1[j];
             }
-            tc::tmem_st16_async(k_lane + (uint32_t)((kc & 1) * 64 + c * 8), h);
+            tc::tmem_st16_async(k_lane + (uint32_t)((kc & 1) * 64 + (c0 + i) * 8), h);
           }
           tc::tmem_wait_st();
         }
@@ -731,7 +736,7 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         mbar_arrive(&kconv_full[kc & 1]);
         if (fine && kc >= 2) fine = mbar_wait(&o_done[kc & 1], ((kc - 2) >> 1) & 1);
         tc::fence_after_sync();
-        for (int r = i0; r < kKeys; r += kStep) widen_row<QT>(stage(kc) + kHalf, v16buf(kc), r, r >= nvalid);
+        widen_row<QT, kChunks>(stage(kc) + kHalf, v16buf(kc), i0, i0 >= nvalid, c0);
         tc::fence_proxy_async_smem();
         mbar_arrive(&vconv_full[kc & 1]);
         mbar_arrive(&empty[kc % kStages]);  // both code tiles of this stage are widened
