@@ -1252,9 +1252,10 @@ cudaError_t launch_mmad_t(const Params &p, const TdArgs &ta, const TdMaps &maps,
   if (grid > V) grid = V;
   const int nv = p.S * p.group;
   // softmax warps: 4 per column group, two groups (four for 32 bf16 rows): more warps to
-  // overlap the per-row work than rows need.  int8 codes take about twice the widening
-  // arithmetic of e4m3 (the pair conversion): for units of up to 4 rows they get four
-  // widening warps and one column group (measured 13% faster; e4m3 is faster with two).
+  // overlap the per-row work than rows need.  int8 codes take more widening arithmetic
+  // than e4m3 (the pair conversion): for units of up to 4 rows they get eight widening
+  // warps and one column group (0.157 -> 0.142 ms per long-context step); e4m3 measured
+  // faster with four widening warps and two groups (0.126 against 0.133 ms).
   const int cg = QT == GQAW_I8 && nv <= 4 ? 1 : nv <= 16 || QT != 0 ? 2 : 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
