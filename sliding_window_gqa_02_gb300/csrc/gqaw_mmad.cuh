@@ -807,6 +807,56 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
                                 (n < NV ? (long long)(x.kvh * g + n % g) * p.bsh + (long long)(n / g) * p.bss : 0);
       named_barrier(kBar, kSoft);
 
+      // Units of at most 16 query rows of a bf16 cache: what the unit's epilogue needs of
+      // the step's own rows is loaded now, so that its round trip (thousands of cycles on a
+      // loaded memory system) overlaps the unit's key tiles instead of lengthening the
+      // epilogue, which holds up the next unit (small-slack decode 8.6 -> 7.9 us, verify4
+      // 0.1024 -> 0.1005 ms; with code caches the e4m3 decode measured 8% slower).  For the logits of the own keys, one warp per query row and
+      // four dimensions per lane: this lane's dimensions of the first kKH key rows and of
+      // its warp's query rows, and the bias of the (row, key) pair whose sum the lane will
+      // hold; for their values, this thread's dimension t of the first kKH value rows.
+      constexpr bool kHoist = NVT <= 16 && QT == 0;
+      constexpr int kSW = kSoft / 32, kRW = (NVT + kSW - 1) / kSW, kRP = (kRW + 1) / 2;
+      constexpr int kKH = NVT < 8 ? NVT : 8;  // own keys held: S <= NVT
+      const int sw = tid >> 5;
+      auto key_at = [&](int s2) {  // this lane's four dimensions (values or codes) of key row s2
+        const size_t krow = ((size_t)x.b * S + (s2 < S ? s2 : S - 1)) * p.Nkv + x.kvh;
+        return kQ8 ? static_cast<const void *>(static_cast<const unsigned char *>(p.k) + krow * kD + 4 * lane)
+                   : static_cast<const void *>(kin + krow * kD + 4 * lane);
+      };
+      auto load_key = [&](int s2) {
+        return kQ8 ? make_uint2(*static_cast<const uint32_t *>(key_at(s2)), 0u) : *static_cast<const uint2 *>(key_at(s2));
+      };
+      auto load_query = [&](int r) {  // this lane's four dimensions of the warp's row r
+        const int n = sw + r * kSW, nn = n < NV ? n : NV - 1;
+        return *reinterpret_cast<const uint2 *>(qin + (((size_t)x.b * S + nn / g) * p.Nq + x.kvh * g + nn % g) * kD +
+                                                 4 * lane);
+      };
+      auto load_bias = [&](int rp, int s0) {  // lane 2v: pair v = (row 2 rp + v / 8, key s0 + v % 8)
+        const int n = sw + (2 * rp + (lane >> 4)) * kSW, s2 = s0 + ((lane >> 1) & 7);
+        return p.bias && n < NV && s2 < S ? __ldg(p.bias + brow[n] + P + s2) : 0.f;
+      };
+      auto load_value = [&](int s2) {  // dimension t of value row s2 (code units for codes)
+        const size_t at = (((size_t)x.b * S + (s2 < S ? s2 : S - 1)) * p.Nkv + x.kvh) * kD + t;
+        if (QT == GQAW_I8) return (float)static_cast<const int8_t *>(p.v)[at];
+        if (QT == GQAW_E4M3)
+          return Pairs<CodeE4M3>::get(make_uint4(static_cast<const unsigned char *>(p.v)[at], 0, 0, 0), 0).x;
+        return __bfloat162float(vin[at]);
+      };
+      uint2 hk[kKH], hq[kRW];
+      float hv[kKH], hb[kRP];
+      if (kHoist && has_fix) {
+#pragma unroll
+        for (int j = 0; j < kKH; ++j) {
+          hk[j] = load_key(j);
+          hv[j] = load_value(j);
+        }
+#pragma unroll
+        for (int r = 0; r < kRW; ++r) hq[r] = load_query(r);
+#pragma unroll
+        for (int rp = 0; rp < kRP; ++rp) hb[rp] = load_bias(rp, 0);
+      }
+
       // per query row of this thread: the reference maximum (uniform over the CTA) and
       // this thread's share of the softmax denominator
       float m_ref[NC], lsum[NC];
@@ -989,6 +1039,73 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       }
       if (has_fix) {
         // logits of the S new keys (the step's own rows) for every query row
+        if constexpr (kHoist) {
+          // per pair of the warp's rows and eight keys, sixteen partial dot products per
+          // lane, summed over the warp by halving exchanges (lanes 2v and 2v + 1 end with
+          // the sum of pair v); the first eight keys were loaded with the unit
+          for (int s0 = 0; s0 < S; s0 += 8) {
+            uint2 kk[8];
+            float bz[kRP];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) kk[j] = s0 == 0 ? (j < kKH ? hk[j < kKH ? j : 0] : make_uint2(0u, 0u)) : load_key(s0 + j);
+#pragma unroll
+            for (int rp = 0; rp < kRP; ++rp) bz[rp] = s0 == 0 ? hb[rp] : load_bias(rp, s0);
+#pragma unroll
+            for (int rp = 0; rp < kRP; ++rp) {
+              float a[16];
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                const int r = 2 * rp + rr;
+                float qf[4] = {0.f, 0.f, 0.f, 0.f};
+                if (r < kRW && sw + r * kSW < NV) {
+                  const uint2 qw = hq[r < kRW ? r : 0];
+                  qf[0] = __uint_as_float(qw.x << 16);
+                  qf[1] = __uint_as_float(qw.x & 0xffff0000u);
+                  qf[2] = __uint_as_float(qw.y << 16);
+                  qf[3] = __uint_as_float(qw.y & 0xffff0000u);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  float kf[4];
+                  if (kQ8) {
+                    const uint4 w = make_uint4(kk[j].x, 0u, 0u, 0u);
+                    const float2 lo = QT == GQAW_I8 ? Pairs<CodeI8>::get(w, 0) : Pairs<CodeE4M3>::get(w, 0);
+                    const float2 hi = QT == GQAW_I8 ? Pairs<CodeI8>::get(w, 1) : Pairs<CodeE4M3>::get(w, 1);
+                    kf[0] = lo.x, kf[1] = lo.y, kf[2] = hi.x, kf[3] = hi.y;
+                  } else {
+                    kf[0] = __uint_as_float(kk[j].x << 16);
+                    kf[1] = __uint_as_float(kk[j].x & 0xffff0000u);
+                    kf[2] = __uint_as_float(kk[j].y << 16);
+                    kf[3] = __uint_as_float(kk[j].y & 0xffff0000u);
+                  }
+                  a[rr * 8 + j] = fmaf(qf[3], kf[3], fmaf(qf[2], kf[2], fmaf(qf[1], kf[1], qf[0] * kf[0])));
+                }
+              }
+              // halving exchanges: keep the half of the values named by this lane's bit
+#pragma unroll
+              for (int w = 8, o = 16; w >= 1; w >>= 1, o >>= 1) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < w; ++i) {
+                  const float send = up ? a[i] : a[w + i], keep = up ? a[w + i] : a[i];
+                  a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+              }
+              const float dot = a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
+              const int n = sw + (2 * rp + (lane >> 4)) * kSW, s2 = s0 + ((lane >> 1) & 7);
+              if ((lane & 1) == 0 && n < NV && s2 < S) {
+                const int sn = n / g;
+                float zz = -INFINITY;
+                if (s2 <= sn && s2 - sn > -p.W) {
+                  zz = dot * qs;
+                  if (p.capmul != 0.f) zz = p.capmul * fast_tanh(zz);
+                  if (p.bias) zz = fmaf(p.biasmul, bz[rp], zz);
+                }
+                zn[n * NPAD + s2] = zz;
+              }
+            }
+          }
+        } else {
         for (int e = tid; e < NV * S; e += kSoft) {
           const int n = e / S, s2 = e % S, sn = n / g;
           const int h = x.kvh * g + n % g;
@@ -1029,6 +1146,7 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
           }
           zn[n * NPAD + s2] = zz;
         }
+        }
         named_barrier(kBar, kSoft);
         for (int n = tid; n < NV; n += kSoft) {
           const float m0 = fin_m[n];
@@ -1068,21 +1186,28 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       for (int i = 0; i < NC; ++i) o[i] *= col0 + i < NV ? fin_f[col0 + i] : 0.f;
       if (has_fix) {
         // the step's own value rows, dimension t, eight rows per batch of independent loads
-        // (a quantized cache's value codes, in code units like the accumulator)
+        // (a quantized cache's value codes, in code units like the accumulator; with kHoist
+        // the first kKH were loaded with the unit)
         const size_t vbase = ((size_t)x.b * S * p.Nkv + x.kvh) * kD + t;
         for (int s0 = 0; s0 < S; s0 += 8) {
           float vv[8];
+          if constexpr (kHoist) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const size_t at = vbase + (size_t)(s0 + j) * p.Nkv * kD;
-            if (s0 + j >= S)
-              vv[j] = 0.f;
-            else if (QT == GQAW_I8)
-              vv[j] = (float)static_cast<const int8_t *>(p.v)[at];
-            else if (QT == GQAW_E4M3)
-              vv[j] = Pairs<CodeE4M3>::get(make_uint4(static_cast<const unsigned char *>(p.v)[at], 0, 0, 0), 0).x;
-            else
-              vv[j] = __bfloat162float(vin[at]);
+            for (int j = 0; j < 8; ++j)
+              vv[j] = s0 == 0 ? (j < kKH ? hv[j < kKH ? j : 0] : 0.f) : (s0 + j < S ? load_value(s0 + j) : 0.f);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const size_t at = vbase + (size_t)(s0 + j) * p.Nkv * kD;
+              if (s0 + j >= S)
+                vv[j] = 0.f;
+              else if (QT == GQAW_I8)
+                vv[j] = (float)static_cast<const int8_t *>(p.v)[at];
+              else if (QT == GQAW_E4M3)
+                vv[j] = Pairs<CodeE4M3>::get(make_uint4(static_cast<const unsigned char *>(p.v)[at], 0, 0, 0), 0).x;
+              else
+                vv[j] = __bfloat162float(vin[at]);
+            }
           }
 #pragma unroll
           for (int i = 0; i < NC; ++i) {
