@@ -27,6 +27,12 @@
 // columns), so several blocks share a slice without any ordering between them.
 //
 // The last block to finish empties the list for the next step.
+//
+// With separate present buffers nothing a block stores is read by another, and
+// finish_copy_kernel replaces the chains by independent jobs: one per 32 KB segment of
+// whole rows of a slice, taken one at a time from a counter in the workspace, so that
+// every block keeps a batch in flight (a chain's batches are round trips one after the
+// other, and there are fewer chains than blocks).
 #include "gqaw_internal.cuh"
 
 namespace gqaw {
@@ -132,7 +138,123 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) 
   }
 }
 
-cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream) {
+namespace {
+
+constexpr int kPlanCache = 512;  // registered items whose plans a copy block keeps in shared memory
+
+// A registered item as the copy jobs need it (b < 0: its seqlens_k is out of range).
+struct CopyPlan {
+  long long Lp, Lt, nrows;  // nrows: the rows to move (0 or less: none)
+  int b, below_only;
+};
+
+__device__ __forceinline__ CopyPlan copy_plan(const Params &p, int entry) {
+  CopyPlan cp;
+  cp.b = entry & (kListBelowOnly - 1);
+  cp.below_only = (entry & kListBelowOnly) != 0;
+  Plan pl;
+  if (!plan_item(p, cp.b, pl)) {  // registered items were valid; defensive
+    cp.b = -1;
+    cp.Lp = cp.Lt = cp.nrows = 0;
+    return cp;
+  }
+  cp.Lp = pl.Lp;
+  cp.Lt = pl.Lt;
+  const long long seed = pl.Lp + p.S - pl.Lt, nwin = pl.P < p.W - 1 ? pl.P : p.W - 1;
+  cp.nrows = cp.below_only ? pl.Lp - nwin - seed : pl.Lt - p.S;  // below the window, or all kept rows
+  return cp;
+}
+
+}  // namespace
+
+// The cache update into separate present buffers: the same rows as finish_kernel moves,
+// as independent jobs (slice, segment of R whole rows), job = slice * segments + segment,
+// taken in order from a counter (the items' row counts differ: a fixed share per block
+// left blocks idle); a slice's last segment also appends the new rows.  Each block first
+// computes the registered items' plans into shared memory (one load of seqlens_k per item).
+__global__ void __launch_bounds__(kFinishThreads, 4) finish_copy_kernel(const Params p) {
+  pdl_wait();                // the attention kernel has finished reading the cache
+  const unsigned nmove = *reinterpret_cast<volatile unsigned *>(p.move_count);
+  if (nmove == 0) {
+    pdl_launch_dependents();
+    return;
+  }
+  __shared__ CopyPlan s_plan[kPlanCache];
+  __shared__ unsigned s_maxseg, s_job;
+  __shared__ int s_last;
+  const int rowb = p.rowbytes, cvec = rowb / 16;
+  const long long R = kFinishThreads * kCopyVecs / cvec;  // rows per segment
+  if (threadIdx.x == 0) s_maxseg = 0u;
+  __syncthreads();
+  for (unsigned e = threadIdx.x; e < nmove; e += kFinishThreads) {
+    const CopyPlan cp = copy_plan(p, p.move_list[e]);
+    if (e < kPlanCache) s_plan[e] = cp;
+    if (cp.b >= 0 && cp.nrows > 0) atomicMax(&s_maxseg, (unsigned)((cp.nrows + R - 1) / R));
+  }
+  __syncthreads();
+  const long long nseg = s_maxseg > 0u ? s_maxseg : 1u;  // segment 0 of each slice appends
+  const long long nslices = (long long)nmove * p.Nkv * 2;
+  for (;;) {
+    if (threadIdx.x == 0) s_job = atomicAdd(p.job_count, 1u);
+    __syncthreads();
+    const long long job = s_job;
+    __syncthreads();  // every thread has read s_job before it is written again
+    if (job >= nslices * nseg) break;
+    const long long slice = job / nseg, sg = job % nseg;  // slice: (list entry, kv head, K or V)
+    const int tensor = (int)(slice & 1), kvh = (int)((slice >> 1) % p.Nkv);
+    const long long ei = (slice >> 1) / p.Nkv;
+    const CopyPlan cp = ei < kPlanCache ? s_plan[ei] : copy_plan(p, p.move_list[ei]);
+    if (cp.b < 0) continue;
+    const long long seed = cp.Lp + p.S - cp.Lt, kept = cp.Lt - p.S;
+    const long long last = cp.nrows > 0 ? (cp.nrows + R - 1) / R - 1 : 0;
+    if (sg > last) continue;
+    const size_t sl = (size_t)cp.b * p.Nkv + kvh;
+    const char *src = static_cast<const char *>(tensor ? p.pv : p.pk) + sl * p.C * rowb;
+    char *dst = static_cast<char *>(tensor ? p.prv : p.prk) + sl * p.C * rowb;
+    if (cp.nrows > 0) {
+      const long long r0 = sg * R, n = cp.nrows - r0 < R ? cp.nrows - r0 : R;
+      uint4 buf[kCopyVecs];
+#pragma unroll
+      for (int u = 0; u < kCopyVecs; ++u) {
+        const int e = threadIdx.x + u * kFinishThreads;
+        if (e < n * cvec) buf[u] = *reinterpret_cast<const uint4 *>(src + (r0 + e / cvec + seed) * rowb + (e % cvec) * 16);
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyVecs; ++u) {
+        const int e = threadIdx.x + u * kFinishThreads;
+        if (e < n * cvec) *reinterpret_cast<uint4 *>(dst + (r0 + e / cvec) * rowb + (e % cvec) * 16) = buf[u];
+      }
+    }
+    if (cp.below_only || sg != last) continue;  // the new rows are in place already
+    const long long a0 = kept > 0 ? kept : 0;
+    const char *newrows = static_cast<const char *>(tensor ? p.v : p.k);
+    for (long long e = threadIdx.x; e < (cp.Lt - a0) * cvec; e += kFinishThreads) {
+      const long long r = a0 + e / cvec;
+      const size_t off = (((size_t)cp.b * p.S + (size_t)(seed + r - cp.Lp)) * p.Nkv + kvh) * (size_t)rowb;
+      *reinterpret_cast<uint4 *>(dst + r * rowb + (e % cvec) * 16) =
+          *reinterpret_cast<const uint4 *>(newrows + off + (e % cvec) * 16);
+    }
+  }
+
+  pdl_launch_dependents();
+
+  // the last block resets the list for the next step
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(p.done_count, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last && threadIdx.x == 0) {
+    __threadfence();
+    *p.move_count = 0u;
+    *p.job_count = 0u;
+    *p.done_count = 0u;
+    __threadfence();
+  }
+}
+
+cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream, bool separate) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks);
   cfg.blockDim = dim3(kFinishThreads);
@@ -142,7 +264,7 @@ cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, finish_kernel, p);
+  const cudaError_t e = separate ? cudaLaunchKernelEx(&cfg, finish_copy_kernel, p) : cudaLaunchKernelEx(&cfg, finish_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -26,7 +26,7 @@ cudaError_t launch_attend_f32(const Params &p, int gb, int blocks, cudaStream_t 
 cudaError_t launch_attend_bf16(const Params &p, int gb, int blocks, cudaStream_t stream);
 int attend_tile_f32(int D);
 int attend_tile_bf16(int D);
-cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream);
+cudaError_t launch_finish(const Params &p, int blocks, cudaStream_t stream, bool separate);
 cudaError_t launch_mma(const Params &p, const TcArgs &ta, const TcMaps &maps, int grid, cudaStream_t stream);
 cudaError_t launch_rotary(const Params &p, cudaStream_t stream);
 cudaError_t launch_attend_q8(const Params &p, int gb, int blocks, cudaStream_t stream);
@@ -45,6 +45,7 @@ constexpr long long kMaxCtas = 152 * 2;
 constexpr long long kSms = 152;
 // Upper bound on the cache-update kernel's blocks (152 SMs x 2).
 constexpr long long kFinishBlocks = 152 * 2;
+constexpr long long kFinishCopyBlocks = 152 * 4;  // finish_copy_kernel: four blocks per SM
 
 gqaw_status fail(gqaw_status s, const char *fmt, ...) {
   char buf[512];
@@ -121,7 +122,7 @@ struct Launch {
   size_t off_kq, off_vq;  // quantized cache: the codes of the step's new rows
   size_t off_q16;         // quantized cache on the tensor-core kernel: the fp16 query copy
   size_t off_stash;       // small-step kernel, bf16 caches: one row stash per CTA
-  long long units, ctas, ncopy;
+  long long units, ctas, ncopy, ncopy_sep;
   size_t off_list, off_tickets, off_partials, ws_bytes;
   int rot_dim;            // > 0: the rotary embedding is on, over this many dimensions
   size_t off_qrot, off_krot;  // the turned query and key rows in the workspace
@@ -220,7 +221,7 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   L->ncg = 1;
   while (L->ncg * 2 <= nv / 2) L->ncg *= 2;
 
-  // Workspace: [0, 256) status word and the two counters of the cache-update list;
+  // Workspace: [0, 256) status word and the three counters of the cache-update kernels;
   // the list itself (B items); per-unit tickets; two partial-result slots per
   // attention CTA.  Everything must start at zero (gqaw_workspace_init); every step
   // leaves the counters and tickets at zero again, and a step whose tickets sit
@@ -233,6 +234,10 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   const long long jobs = (long long)a->batch_size * a->kv_num_heads * 2 * L->ncg;
   if (jobs > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many cache-update jobs");
   L->ncopy = std::min(jobs, kFinishBlocks);
+  // separate present buffers: a job per 32 KB segment of whole rows of a slice
+  const long long seg_rows = 8 * 256 / (L->rowbytes / 16);  // 32 KB: 256 threads x 8 16-byte vectors
+  L->ncopy_sep = std::min((long long)a->batch_size * a->kv_num_heads * 2 * ceil_div(a->capacity, seg_rows),
+                          kFinishCopyBlocks);
 
   // Multi-token steps with bf16 caches and head size 128 run on the tensor-core
   // kernel when the query-head group tiles a 32-row lane quarter exactly.
@@ -431,6 +436,7 @@ void fill_params(const gqaw_step_args *a, const Launch &L, gqaw::Params *p) {
   p->status = reinterpret_cast<uint32_t *>(ws);
   p->move_count = reinterpret_cast<uint32_t *>(ws + 4);
   p->done_count = reinterpret_cast<uint32_t *>(ws + 8);
+  p->job_count = reinterpret_cast<uint32_t *>(ws + 12);
   p->move_list = reinterpret_cast<int32_t *>(ws + L.off_list);
   p->tickets = reinterpret_cast<uint32_t *>(ws + L.off_tickets);
   p->partials = reinterpret_cast<float *>(ws + L.off_partials);
@@ -622,7 +628,9 @@ gqaw_status clear_tickets_if_needed(const gqaw_step_args *a, const Launch &L, cu
 }
 
 gqaw_status run_finish(const gqaw_step_args *a, const Launch &L, const gqaw::Params &p, cudaStream_t st) {
-  const cudaError_t e = gqaw::launch_finish(p, (int)L.ncopy, st);
+  // separate present buffers for both K and V: the copy kernel's independent jobs
+  const bool separate = p.pk != p.prk && p.pv != p.prv;
+  const cudaError_t e = gqaw::launch_finish(p, (int)(separate ? L.ncopy_sep : L.ncopy), st, separate);
   if (e != cudaSuccess) return cuda_fail(e, "finish kernel launch");
   g_launches.fetch_add(1);
   return GQAW_OK;

@@ -28,6 +28,7 @@ struct Params {
   uint32_t *status;          // device status word
   uint32_t *move_count;      // items registered for the cache-update kernel this step
   uint32_t *done_count;      // cache-update blocks finished this step
+  uint32_t *job_count;       // cache-update jobs taken this step (separate present buffers)
   int32_t *move_list;        // (B,) the registered items
   uint32_t *tickets;         // per attention unit: contributors finished
   int32_t *resident_out;     // NULL or (B,)
