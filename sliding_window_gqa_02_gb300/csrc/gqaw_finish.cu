@@ -39,7 +39,6 @@ namespace gqaw {
 
 constexpr int kFinishThreads = 256;
 constexpr int kCopyVecs = 8;  // 16-byte vectors per thread per batch (32 KB per block)
-constexpr long long kMinCopyChains = 152;  // one per SM of a GB300
 
 __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) {
   pdl_wait();                // the attention kernel has finished reading the cache
@@ -52,10 +51,10 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const Params p) 
   // launched early, their CTAs would hold whole SMs (waiting for this grid) that the
   // copies need.
   // Whole rows (one contiguous chain per slice) unless that leaves fewer chains than
-  // SMs; then rows split into column groups, up to p.ncg of them.  nmove is the same
+  // blocks; then rows split into column groups, up to p.ncg of them.  nmove is the same
   // for every block, so they all agree on the job numbering.
   int ncg = 1;
-  while (ncg < p.ncg && (long long)nmove * p.Nkv * 2 * ncg < kMinCopyChains) ncg *= 2;
+  while (ncg < p.ncg && (long long)nmove * p.Nkv * 2 * ncg < gridDim.x) ncg *= 2;
   const int per_item = p.Nkv * 2 * ncg;
   const long long njobs = (long long)nmove * per_item;
   const int rowb = p.rowbytes;

@@ -44,7 +44,8 @@ std::atomic<unsigned long long> g_launches{0ull};
 constexpr long long kMaxCtas = 152 * 2;
 constexpr long long kSms = 152;
 // Upper bound on the cache-update kernel's blocks (152 SMs x 2).
-constexpr long long kFinishBlocks = 152 * 2;
+constexpr long long kFinishBlocks = 152 * 2;      // finish_kernel: two blocks per SM,
+constexpr long long kFinishBlocksLong = 152 * 4;  // four for steps of 64 tokens or more
 constexpr long long kFinishCopyBlocks = 152 * 4;  // finish_copy_kernel: four blocks per SM
 
 gqaw_status fail(gqaw_status s, const char *fmt, ...) {
@@ -233,7 +234,10 @@ gqaw_status plan_launch(const gqaw_step_args *a, Launch *L) {
   // Cache-update kernel: grid-stride over the jobs of the registered items.
   const long long jobs = (long long)a->batch_size * a->kv_num_heads * 2 * L->ncg;
   if (jobs > 0x7fffffffLL) return fail(GQAW_EUNSUPPORTED, "too many cache-update jobs");
-  L->ncopy = std::min(jobs, kFinishBlocks);
+  // Steps of many tokens reclaim long runs of rows in few items: more, narrower chains
+  // on four blocks per SM (B=8 x 512 prefill 2.9% faster); decode steps mostly launch
+  // the kernel to find nothing to move, where the larger grid costs about a microsecond.
+  L->ncopy = std::min(jobs, a->sequence_length >= 64 ? kFinishBlocksLong : kFinishBlocks);
   // separate present buffers: a job per 32 KB segment of whole rows of a slice
   const long long seg_rows = 8 * 256 / (L->rowbytes / 16);  // 32 KB: 256 threads x 8 16-byte vectors
   L->ncopy_sep = std::min((long long)a->batch_size * a->kv_num_heads * 2 * ceil_div(a->capacity, seg_rows),
