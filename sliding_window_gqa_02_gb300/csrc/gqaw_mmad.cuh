@@ -811,7 +811,8 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       // the step's own rows is loaded now, so that its round trip (thousands of cycles on a
       // loaded memory system) overlaps the unit's key tiles instead of lengthening the
       // epilogue, which holds up the next unit (small-slack decode 8.6 -> 7.9 us, verify4
-      // 0.1024 -> 0.1005 ms; with code caches the e4m3 decode measured 8% slower).  For the logits of the own keys, one warp per query row and
+      // 0.1024 -> 0.1005 ms; with code caches the e4m3 decode measured 8% slower: registers
+      // held across the unit).  For the logits of the own keys, one warp per query row and
       // four dimensions per lane: this lane's dimensions of the first kKH key rows and of
       // its warp's query rows, and the bias of the (row, key) pair whose sum the lane will
       // hold; for their values, this thread's dimension t of the first kKH value rows.
@@ -819,13 +820,9 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
       constexpr int kSW = kSoft / 32, kRW = (NVT + kSW - 1) / kSW, kRP = (kRW + 1) / 2;
       constexpr int kKH = NVT < 8 ? NVT : 8;  // own keys held: S <= NVT
       const int sw = tid >> 5;
-      auto key_at = [&](int s2) {  // this lane's four dimensions (values or codes) of key row s2
+      auto load_key = [&](int s2) {  // this lane's four dimensions of key row s2
         const size_t krow = ((size_t)x.b * S + (s2 < S ? s2 : S - 1)) * p.Nkv + x.kvh;
-        return kQ8 ? static_cast<const void *>(static_cast<const unsigned char *>(p.k) + krow * kD + 4 * lane)
-                   : static_cast<const void *>(kin + krow * kD + 4 * lane);
-      };
-      auto load_key = [&](int s2) {
-        return kQ8 ? make_uint2(*static_cast<const uint32_t *>(key_at(s2)), 0u) : *static_cast<const uint2 *>(key_at(s2));
+        return *reinterpret_cast<const uint2 *>(kin + krow * kD + 4 * lane);
       };
       auto load_query = [&](int r) {  // this lane's four dimensions of the warp's row r
         const int n = sw + r * kSW, nn = n < NV ? n : NV - 1;
@@ -836,12 +833,8 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
         const int n = sw + (2 * rp + (lane >> 4)) * kSW, s2 = s0 + ((lane >> 1) & 7);
         return p.bias && n < NV && s2 < S ? __ldg(p.bias + brow[n] + P + s2) : 0.f;
       };
-      auto load_value = [&](int s2) {  // dimension t of value row s2 (code units for codes)
-        const size_t at = (((size_t)x.b * S + (s2 < S ? s2 : S - 1)) * p.Nkv + x.kvh) * kD + t;
-        if (QT == GQAW_I8) return (float)static_cast<const int8_t *>(p.v)[at];
-        if (QT == GQAW_E4M3)
-          return Pairs<CodeE4M3>::get(make_uint4(static_cast<const unsigned char *>(p.v)[at], 0, 0, 0), 0).x;
-        return __bfloat162float(vin[at]);
+      auto load_value = [&](int s2) {  // dimension t of value row s2
+        return __bfloat162float(vin[(((size_t)x.b * S + (s2 < S ? s2 : S - 1)) * p.Nkv + x.kvh) * kD + t]);
       };
       uint2 hk[kKH], hq[kRW];
       float hv[kKH], hb[kRP];
@@ -1047,7 +1040,8 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
             uint2 kk[8];
             float bz[kRP];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) kk[j] = s0 == 0 ? (j < kKH ? hk[j < kKH ? j : 0] : make_uint2(0u, 0u)) : load_key(s0 + j);
+            for (int j = 0; j < 8; ++j)
+              kk[j] = s0 == 0 ? (j < kKH ? hk[j < kKH ? j : 0] : make_uint2(0u, 0u)) : load_key(s0 + j);
 #pragma unroll
             for (int rp = 0; rp < kRP; ++rp) bz[rp] = s0 == 0 ? hb[rp] : load_bias(rp, s0);
 #pragma unroll
@@ -1066,18 +1060,8 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                  float kf[4];
-                  if (kQ8) {
-                    const uint4 w = make_uint4(kk[j].x, 0u, 0u, 0u);
-                    const float2 lo = QT == GQAW_I8 ? Pairs<CodeI8>::get(w, 0) : Pairs<CodeE4M3>::get(w, 0);
-                    const float2 hi = QT == GQAW_I8 ? Pairs<CodeI8>::get(w, 1) : Pairs<CodeE4M3>::get(w, 1);
-                    kf[0] = lo.x, kf[1] = lo.y, kf[2] = hi.x, kf[3] = hi.y;
-                  } else {
-                    kf[0] = __uint_as_float(kk[j].x << 16);
-                    kf[1] = __uint_as_float(kk[j].x & 0xffff0000u);
-                    kf[2] = __uint_as_float(kk[j].y << 16);
-                    kf[3] = __uint_as_float(kk[j].y & 0xffff0000u);
-                  }
+                  const float kf[4] = {__uint_as_float(kk[j].x << 16), __uint_as_float(kk[j].x & 0xffff0000u),
+                                       __uint_as_float(kk[j].y << 16), __uint_as_float(kk[j].y & 0xffff0000u)};
                   a[rr * 8 + j] = fmaf(qf[3], kf[3], fmaf(qf[2], kf[2], fmaf(qf[1], kf[1], qf[0] * kf[0])));
                 }
               }
@@ -1106,46 +1090,46 @@ __global__ void __launch_bounds__(Warps<CG, QT>::kThreads, 1)
             }
           }
         } else {
-        for (int e = tid; e < NV * S; e += kSoft) {
-          const int n = e / S, s2 = e % S, sn = n / g;
-          const int h = x.kvh * g + n % g;
-          float zz = -INFINITY;
-          if (s2 <= sn && s2 - sn > -p.W) {
-            const uint4 *qr = reinterpret_cast<const uint4 *>(qin + (((size_t)x.b * S + sn) * p.Nq + h) * kD);
-            const size_t krow = ((size_t)x.b * S + s2) * p.Nkv + x.kvh;
-            float dot = 0.f;
-            if (kQ8) {  // 16 key codes per vector
-              const uint4 *kr = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(p.k) + krow * kD);
+          for (int e = tid; e < NV * S; e += kSoft) {
+            const int n = e / S, s2 = e % S, sn = n / g;
+            const int h = x.kvh * g + n % g;
+            float zz = -INFINITY;
+            if (s2 <= sn && s2 - sn > -p.W) {
+              const uint4 *qr = reinterpret_cast<const uint4 *>(qin + (((size_t)x.b * S + sn) * p.Nq + h) * kD);
+              const size_t krow = ((size_t)x.b * S + s2) * p.Nkv + x.kvh;
+              float dot = 0.f;
+              if (kQ8) {  // 16 key codes per vector
+                const uint4 *kr = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(p.k) + krow * kD);
 #pragma unroll 4
-              for (int vv = 0; vv < kD / 16; ++vv) {
-                float qa[16];
-                Elem<__nv_bfloat16>::unpack(qr[2 * vv], qa);
-                Elem<__nv_bfloat16>::unpack(qr[2 * vv + 1], qa + 8);
-                const uint4 ku = kr[vv];
+                for (int vv = 0; vv < kD / 16; ++vv) {
+                  float qa[16];
+                  Elem<__nv_bfloat16>::unpack(qr[2 * vv], qa);
+                  Elem<__nv_bfloat16>::unpack(qr[2 * vv + 1], qa + 8);
+                  const uint4 ku = kr[vv];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float2 k2 = QT == GQAW_I8 ? Pairs<CodeI8>::get(ku, j) : Pairs<CodeE4M3>::get(ku, j);
-                  dot = fmaf(qa[2 * j], k2.x, dot);
-                  dot = fmaf(qa[2 * j + 1], k2.y, dot);
+                  for (int j = 0; j < 8; ++j) {
+                    const float2 k2 = QT == GQAW_I8 ? Pairs<CodeI8>::get(ku, j) : Pairs<CodeE4M3>::get(ku, j);
+                    dot = fmaf(qa[2 * j], k2.x, dot);
+                    dot = fmaf(qa[2 * j + 1], k2.y, dot);
+                  }
+                }
+              } else {
+                const uint4 *kr = reinterpret_cast<const uint4 *>(kin + krow * kD);
+#pragma unroll 8
+                for (int vv = 0; vv < kD / 8; ++vv) {
+                  float qa[8], ka[8];
+                  Elem<__nv_bfloat16>::unpack(qr[vv], qa);
+                  Elem<__nv_bfloat16>::unpack(kr[vv], ka);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) dot = fmaf(qa[i], ka[i], dot);
                 }
               }
-            } else {
-              const uint4 *kr = reinterpret_cast<const uint4 *>(kin + krow * kD);
-#pragma unroll 8
-              for (int vv = 0; vv < kD / 8; ++vv) {
-                float qa[8], ka[8];
-                Elem<__nv_bfloat16>::unpack(qr[vv], qa);
-                Elem<__nv_bfloat16>::unpack(kr[vv], ka);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) dot = fmaf(qa[i], ka[i], dot);
-              }
+              zz = dot * qs;
+              if (p.capmul != 0.f) zz = p.capmul * fast_tanh(zz);
+              if (p.bias) zz = fmaf(p.biasmul, p.bias[brow[n] + P + s2], zz);
             }
-            zz = dot * qs;
-            if (p.capmul != 0.f) zz = p.capmul * fast_tanh(zz);
-            if (p.bias) zz = fmaf(p.biasmul, p.bias[brow[n] + P + s2], zz);
+            zn[n * NPAD + s2] = zz;
           }
-          zn[n * NPAD + s2] = zz;
-        }
         }
         named_barrier(kBar, kSoft);
         for (int n = tid; n < NV; n += kSoft) {
