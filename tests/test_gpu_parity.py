@@ -150,6 +150,23 @@ def test_slack_decode_many_compactions():
         T = T + 1
 
 
+@pytest.mark.parametrize("D", [16, 128])
+def test_separate_present_many_items(D):
+    """A separate present buffer registers every item each step; with 600 items the
+    copy kernel keeps the first 512 plans in shared memory and computes the others per
+    job.  Contexts cross the capacity (reclaiming and drifting items in one step); head
+    size 16 runs the FFMA attention, 128 the small-step tensor-core kernel (which leaves
+    only the rows below the window)."""
+    sh = wl.Shape("many", B=600, Nq=2, Nkv=1, D=D, W=12, C=16, dtype=wl.BF16)
+    pk, pv = wl.cache(sh, 61)
+    p = _shape_pair(sh, past_key=pk, past_value=pv, inplace=False)
+    T = wl.lengths(sh.B, 5, 60, 61)
+    for t in range(3):
+        q, k, v = wl.step_inputs(sh, 1, 6100 + t)
+        p.step(q, k, v, T)
+        T = T + 1
+
+
 @pytest.mark.parametrize("inplace", [True, False])
 def test_slack_chunked_prefill_from_drifted_point(inplace):
     """C = W + 8 with 32-token chunks: a chunk can compact below the history its own
