@@ -611,7 +611,8 @@ def run_gpu(args, rank, world):
     if attend_ms:
         am = statistics.median(attend_ms)
         kern = attention_kernel(sh, S, h.quant)
-        traffic = profiled_traffic(name, kern)
+        # a committed figure is for the workload's own batch; another batch has none
+        traffic = profiled_traffic(name, kern) if not args.batch else None
         timing_note = ("median over %d passes of the mean CUDA-event time of the attention launch, each launch "
                        "timed alone (an event on each side: no overlap with the neighbouring kernels); "
                        "avg_step_ms is the headline's whole step" % len(attend_ms))
