@@ -213,7 +213,11 @@ gqaw_status gqa_windowed_step(const gqaw_step_args *args, void *stream);
  * resident_len_out; the append of the new rows of every item that reclaims no block
  * with past == present (rows [L(P), L(P) + S), which no query reads).  Items that
  * reclaim a block ([P2] block compaction), and all items when present is a separate
- * buffer, are recorded in the workspace for gqaw_update_cache(). */
+ * buffer, are recorded in the workspace for gqaw_update_cache(), except what the
+ * small-step tensor-core kernel (bf16 cache, head_size 128, S * group <= 32) writes
+ * itself from the key and value tiles it reads: the whole update of an item whose
+ * surviving rows lie in its window, and with a separate present buffer the window's
+ * rows (only the rows below the window are then recorded). */
 gqaw_status gqaw_attend(const gqaw_step_args *args, void *stream);
 
 /* Second phase only (one kernel): for the items gqaw_attend() recorded, moves the
